@@ -1,0 +1,310 @@
+"""Plain CPU oracle for paged sliding-window attention with a window-clamped
+multimodal (image) prefix, and for its two feeders: slot mapping and the
+log-sum-exp merge of split-KV partial outputs.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module.  It shares no code
+with the CUDA library (``paged_sliding_window_swa_gb300``) and neither imports
+the other.  Everything here is slow on purpose: per-token loops, a per-pair
+visibility mask over every key of the sequence (no pruning), and fp64
+softmax over the bf16/fp32 inputs widened to fp64.
+
+Sources (page title, then the section):
+
+* "vLLM PR #53147 summary: multimodal prefix restores SWA pruning"
+  (prhub.com.cn) -- "Implementation breakdown" items 1-2 (the union
+  semantics of the base window and the clamped image mask), the
+  ``compute_tile_loop_bounds`` excerpt (tile bounds), and the geometry tests
+  (expected bounds [3, 72, 4096] and [3, 68)).
+* "vllm-ascend Triton operator: _compute_slot_mapping_kernel"
+  (0539edu.com) -- section 2 "non-CP path" (slot formula), section 1 (the
+  PAD tail for graph-fixed shapes), section 5 (worked example).
+* "MLA DCP decode two-stream overlap and V-up fusion (PR #16977)"
+  (huashanblogllm.xyz) -- section 1.1 and the LSE glossary entry: partial
+  outputs merged with their LSE are equal to one softmax over the whole
+  sequence.
+
+Readings where the pages are silent or ambiguous (each also listed in the
+design notes):
+
+* softmax scale is an argument (default 1/sqrt(head_dim) in the workloads);
+  LSE is in natural log;
+* the K/V cache is slot-major ``[num_blocks, block_size, num_kv_heads, D]``,
+  slot = block * block_size + offset; query head h reads kv head
+  h // (num_heads_q // num_heads_kv);
+* image ranges are inclusive ``[s, e]`` in absolute positions; ``s >= e`` is
+  padding (the pages' test pads with [0, 0]);
+* tile bounds use the block's first row for the window's left edge
+  (``ctx + qpos_lo - W + 1``), the block's last row clamped to the query
+  length, and ``max_seq_prefix_len = seq_len`` whenever image ranges are
+  enabled or attention is non-causal;
+* split-KV: a sequence with P_s partitions gives partition p the keys
+  ``[p*L, min((p+1)*L, seq_len))`` with ``L = 128 * ceil(ceil(seq_len/P_s)/128)``;
+  a row with no allowed key in a partition has partial LSE = -inf;
+* LSE merge: partitions with LSE = -inf carry weight 0 and their partial
+  output is never read; if every partition is -inf the output is 0 and the
+  merged LSE is -inf.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+NEG_INF = -math.inf
+SPLIT_ALIGN = 128
+
+
+# ---------------------------------------------------------------------------
+# slot mapping (vllm-ascend slot-mapping article, sections 1, 2 and 5)
+# ---------------------------------------------------------------------------
+def slot_mapping(query_start_loc, positions, block_table, block_size, num_tokens,
+                 max_num_tokens, pad_id=-1):
+    """Physical KV slot of every token, then ``pad_id`` over the padded tail.
+
+    For token t of request r: block index = pos // block_size, offset =
+    pos - index * block_size, slot = block_table[r][index] * block_size +
+    offset.  Tokens in ``[num_tokens, max_num_tokens)`` get ``pad_id``.  A
+    token whose position is negative or whose block index lies outside the
+    request's block-table row is not mapped (it gets ``pad_id``); its index is
+    returned in ``bad``.
+    """
+    qsl = np.asarray(query_start_loc, dtype=np.int64)
+    pos_arr = np.asarray(positions, dtype=np.int64)
+    bt = np.asarray(block_table, dtype=np.int64)
+    stride = bt.shape[1]
+    out = [pad_id] * int(max_num_tokens)
+    bad = []
+    for r in range(len(qsl) - 1):
+        for t in range(int(qsl[r]), int(qsl[r + 1])):
+            pos = int(pos_arr[t])
+            index = pos // block_size
+            if pos < 0 or index >= stride:
+                bad.append(t)
+                continue
+            offset = pos - index * block_size
+            out[t] = int(bt[r, index]) * block_size + offset
+    del num_tokens  # the tail is everything after the last request's tokens
+    return np.array(out, dtype=np.int64).astype(np.int32), bad
+
+
+# ---------------------------------------------------------------------------
+# the visibility rule (vLLM PR #53147 summary, implementation items 1-2)
+# ---------------------------------------------------------------------------
+def visible_keys(q_abs, seq_len, window, causal, ranges):
+    """Boolean mask over every key k in [0, seq_len) for the query at q_abs.
+
+    base(q, k): for W > 0, k >= q-W+1 and (causal: k <= q; non-causal:
+    k <= q+W-1); for W <= 0, causal: k <= q, non-causal: every key.
+    mm(q, k): some valid range [s, e] holds both q and k, and (W > 0) k >= q-W+1.
+    Visible = base OR mm, for 0 <= k < seq_len.
+    """
+    k = np.arange(int(seq_len), dtype=np.int64)
+    q = int(q_abs)
+    if window > 0:
+        right = q if causal else q + window - 1
+        base = (k >= q - window + 1) & (k <= right)
+    else:
+        base = (k <= q) if causal else np.ones(k.shape, dtype=bool)
+    mm = np.zeros(k.shape, dtype=bool)
+    if ranges is not None:
+        for s, e in np.asarray(ranges).reshape(-1, 2):
+            s, e = int(s), int(e)
+            if not s < e:
+                continue                      # [0, 0] padding / empty range
+            if s <= q <= e:
+                inside = (k >= s) & (k <= e)
+                if window > 0:
+                    inside &= k >= q - window + 1   # clamped at the window's left edge
+                mm |= inside
+    return base | mm
+
+
+def split_key_ranges(seq_len, parts):
+    """Key range of each of ``parts`` split-KV partitions (possibly empty)."""
+    seq_len, parts = int(seq_len), int(parts)
+    per = -(-seq_len // parts) if parts > 0 else seq_len
+    length = -(-per // SPLIT_ALIGN) * SPLIT_ALIGN
+    return [(min(p * length, seq_len), min((p + 1) * length, seq_len)) for p in range(parts)]
+
+
+def _gather(cache, table_row, seq_len, block_size, kv_head):
+    """Rows of one kv head for keys 0..seq_len-1, fetched page by page."""
+    d = cache.shape[-1]
+    out = np.empty((int(seq_len), d), dtype=np.float64)
+    for k in range(int(seq_len)):
+        page = int(table_row[k // block_size])
+        out[k] = cache[page, k % block_size, kv_head]
+    return out
+
+
+def _as_f64(x):
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return x.detach().to("cpu", torch.float64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(x, dtype=np.float64)
+
+
+def attention(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, mm_ranges,
+              window, causal, scale, context_lens=None, rows=None, splits_per_seq=None,
+              num_splits=1):
+    """Attention of every requested (token, head) row, fp64.
+
+    ``rows``: iterable of (token, head) pairs, or None for all rows.  Returns
+    dicts keyed by (token, head): ``out`` (D-vector) and ``lse`` (float).  With
+    ``num_splits > 1`` the keys are further restricted to each partition and
+    the results are keyed by (split, token, head); partitions >= P_s of a
+    sequence, and rows with no allowed key in a partition, give lse = -inf and
+    an all-zero output.
+    """
+    qf = _as_f64(q)
+    kc = _as_f64(k_cache)
+    vc = _as_f64(v_cache)
+    bt = np.asarray(block_table)
+    qsl = np.asarray(query_start_loc, dtype=np.int64)
+    seq_lens = np.asarray(seq_lens, dtype=np.int64)
+    T, Hq, D = qf.shape
+    Hkv = kc.shape[2]
+    G = Hq // Hkv
+    B = kc.shape[1]
+    S = len(seq_lens)
+    ctx = (seq_lens - np.diff(qsl)) if context_lens is None else np.asarray(context_lens, np.int64)
+    tok_seq = np.repeat(np.arange(S), np.diff(qsl))
+    if rows is None:
+        rows = [(t, h) for t in range(T) for h in range(Hq)]
+    by_group = {}
+    for t, h in rows:
+        by_group.setdefault((int(tok_seq[t]), h // G), []).append((int(t), int(h)))
+    out, lse = {}, {}
+    for (s, hk), lst in sorted(by_group.items()):
+        K = _gather(kc, bt[s], seq_lens[s], B, hk)
+        V = _gather(vc, bt[s], seq_lens[s], B, hk)
+        rng = None if mm_ranges is None else np.asarray(mm_ranges)[s]
+        parts = 1
+        if num_splits > 1:
+            parts = int(num_splits if splits_per_seq is None else splits_per_seq[s])
+        key_ranges = split_key_ranges(seq_lens[s], parts)
+        for t, h in lst:
+            q_abs = int(ctx[s] + (t - qsl[s]))
+            vis = visible_keys(q_abs, seq_lens[s], window, causal, rng)
+            for p in range(num_splits if num_splits > 1 else 1):
+                sel = vis.copy()
+                if num_splits > 1:
+                    if p >= parts:
+                        sel[:] = False
+                    else:
+                        lo, hi = key_ranges[p]
+                        sel[:lo] = False
+                        sel[hi:] = False
+                idx = np.nonzero(sel)[0]
+                if idx.size == 0:
+                    o, l = np.zeros(D), NEG_INF
+                else:
+                    sc = scale * (K[idx] @ qf[t, h])
+                    m = sc.max()
+                    w = np.exp(sc - m)
+                    o = (w @ V[idx]) / w.sum()
+                    l = m + math.log(w.sum())
+                key = (t, h) if num_splits == 1 else (p, t, h)
+                out[key], lse[key] = o, l
+    return out, lse
+
+
+def allowed_pair_count(query_start_loc, seq_lens, mm_ranges, window, causal, context_lens=None):
+    """Number of visible (query, key) pairs of one head, by the per-pair rule."""
+    qsl = np.asarray(query_start_loc, dtype=np.int64)
+    seq_lens = np.asarray(seq_lens, dtype=np.int64)
+    ctx = (seq_lens - np.diff(qsl)) if context_lens is None else np.asarray(context_lens, np.int64)
+    total = 0
+    for s in range(len(seq_lens)):
+        rng = None if mm_ranges is None else np.asarray(mm_ranges)[s]
+        for i in range(int(qsl[s + 1] - qsl[s])):
+            total += int(visible_keys(ctx[s] + i, seq_lens[s], window, causal, rng).sum())
+    return total
+
+
+# ---------------------------------------------------------------------------
+# tile bounds (vLLM PR #53147 summary, compute_tile_loop_bounds excerpt)
+# ---------------------------------------------------------------------------
+def tile_bounds(query_start_loc, seq_lens, mm_ranges, window, causal, tile_size, block_q,
+                max_qblocks, context_lens=None):
+    """[loop_lo, loop_hi, max_seq_prefix_len] for every (sequence, query block).
+
+    Blocks past the sequence's query length are left as [0, 0, 0].  With an
+    image-range array present (``mm_ranges`` not None), every range that
+    intersects the block's rows widens the window: the left edge to
+    max(start, q_lo - W + 1), the right edge to the range end; the right edge
+    is then clamped to seq_len - 1 and both edges are converted to tiles.
+    """
+    qsl = np.asarray(query_start_loc, dtype=np.int64)
+    seq_lens = np.asarray(seq_lens, dtype=np.int64)
+    S = len(seq_lens)
+    ctx = (seq_lens - np.diff(qsl)) if context_lens is None else np.asarray(context_lens, np.int64)
+    use_mm = mm_ranges is not None and np.asarray(mm_ranges).size > 0
+    out = np.zeros((S, max_qblocks, 3), dtype=np.int64)
+    for s in range(S):
+        qlen = int(qsl[s + 1] - qsl[s])
+        seq_len = int(seq_lens[s])
+        c = int(ctx[s])
+        for b in range(max_qblocks):
+            qpos_lo = b * block_q
+            if qpos_lo >= qlen:
+                continue
+            qpos_hi = min(qpos_lo + block_q - 1, qlen - 1)
+            if use_mm or not causal:
+                max_prefix = seq_len
+            else:
+                max_prefix = min(c + qpos_hi + 1, seq_len)
+            num_tiles = -(-max_prefix // tile_size)
+            if window <= 0:
+                lo, hi = 0, num_tiles
+            else:
+                q_lo, q_hi = c + qpos_lo, c + qpos_hi
+                first = q_lo - window + 1
+                last = q_hi if causal else q_hi + window - 1
+                if use_mm:
+                    for rs, re_ in np.asarray(mm_ranges)[s].reshape(-1, 2):
+                        rs, re_ = int(rs), int(re_)
+                        if rs < re_ and rs <= q_hi and re_ >= q_lo:
+                            first = min(first, max(rs, q_lo - window + 1))
+                            last = max(last, re_)
+                last = min(last, seq_len - 1)
+                lo = max(0, first // tile_size)
+                hi = min(last // tile_size + 1, num_tiles)
+            out[s, b] = (lo, hi, max_prefix)
+    return out.astype(np.int32)
+
+
+# ---------------------------------------------------------------------------
+# LSE merge (DCP decode study notes, section 1.1 and the LSE glossary entry)
+# ---------------------------------------------------------------------------
+def lse_combine(partial_out, partial_lse):
+    """Merge P partial outputs [P, T, H, D] with their LSE [P, T, H].
+
+    L = max_p lse_p; w_p = exp(lse_p - L); out = sum_p w_p o_p / sum_p w_p;
+    lse = L + ln(sum_p w_p).  Partitions with lse = -inf have weight 0 and
+    their output is not read.  All -inf: out = 0, lse = -inf.
+    """
+    po = _as_f64(partial_out)
+    pl = _as_f64(partial_lse)
+    P, T, H, D = po.shape
+    out = np.zeros((T, H, D))
+    lse = np.full((T, H), NEG_INF)
+    for t in range(T):
+        for h in range(H):
+            vals = pl[:, t, h]
+            live = [p for p in range(P) if vals[p] != NEG_INF]
+            if not live:
+                continue
+            L = max(vals[p] for p in live)
+            w = {p: math.exp(vals[p] - L) for p in live}
+            tot = sum(w.values())
+            acc = np.zeros(D)
+            for p in live:
+                acc += w[p] * po[p, t, h]
+            out[t, h] = acc / tot
+            lse[t, h] = L + math.log(tot)
+    return out, lse
