@@ -1,0 +1,416 @@
+#!/usr/bin/env python3
+"""Benchmark: Gemma-like multimodal prefill through the paged SWA library.
+
+One step = the whole hot path over one batch: slot mapping (with the PAD tail
+up to a multiple of 8192 tokens), tile bounds, and paged attention with the
+sliding window and the window-clamped image mask, on 4 requests of ~16,550
+tokens with 60 images of 256 tokens each (Hq=16, Hkv=8, D=256, bf16, W=1024,
+causal, paged KV block 16).  Inputs are synthetic (seeded N(0,1)).
+
+Metric: attention TFLOP/s counting only visible (query, key) pairs
+(4 * D * Hq * pairs), plus prefill tokens/s and the fraction of the measured
+bf16 dense tensor-core peak.  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+(N > 1: launched by torchrun, one independent replica per GPU.)
+"""
+import os
+
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")     # the oracle leg runs on one core, stated as such
+
+import argparse
+import json
+import math
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "allowed-pair attention TFLOP/s & prefill tok/s (1×GB300), % of bf16 TC peak"
+UNIT = "TFLOP/s"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------
+def visible_pairs_per_head(lay) -> int:
+    """Visible (query, key) pairs of one head.
+
+    The visible keys of a query form one interval (left edge q-W+1, right edge
+    the larger of the base window's right edge and the end of every image
+    range holding q), so the count is a sum of interval lengths.
+    """
+    total = 0
+    qsl, ctx = lay.query_start_loc, lay.context_lens
+    for s in range(lay.num_seqs):
+        n = int(lay.seq_lens[s])
+        q = ctx[s] + np.arange(int(lay.query_lens[s]), dtype=np.int64)
+        if lay.window > 0:
+            lo = np.maximum(0, q - lay.window + 1)
+            hi = q.copy() if lay.causal else q + lay.window - 1
+        else:
+            lo = np.zeros_like(q)
+            hi = q.copy() if lay.causal else np.full_like(q, n - 1)
+        if lay.mm_ranges is not None:
+            for a, b in lay.mm_ranges[s]:
+                if a < b:
+                    sel = (q >= a) & (q <= b)
+                    hi[sel] = np.maximum(hi[sel], b)
+        hi = np.minimum(hi, n - 1)
+        total += int(np.maximum(hi - lo + 1, 0).sum())
+    del qsl
+    return total
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.proc = None
+        self.index = index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU path
+# ---------------------------------------------------------------------------
+class PrefillStep:
+    """Device-resident inputs and outputs of one Gemma-like prefill step."""
+
+    TILE, BLOCK_Q = 64, 32      # tile-bounds geometry reported alongside the attention
+
+    def __init__(self, lay, device, data_seed=1):
+        import paged_sliding_window_swa_gb300 as swa
+        self.swa, self.lay, self.dev = swa, lay, device
+        self.q, self.k, self.v = W.make_tensors(lay, device=device, data_seed=data_seed)
+        self.d = W.device_layout(lay, device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.slots = torch.empty(lay.max_num_tokens, dtype=torch.int32, device=device)
+        self.maxb = -(-lay.max_query_len // self.BLOCK_Q)
+        self.bounds = torch.empty((lay.num_seqs, self.maxb, 3), dtype=torch.int32, device=device)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((lay.num_tokens, lay.num_heads_q), dtype=torch.float32, device=device)
+
+    def feeders(self):
+        lay, d, swa = self.lay, self.d, self.swa
+        swa.swa_slot_mapping(d["query_start_loc"], d["positions"], d["block_table"], lay.block_size,
+                             lay.max_num_tokens, out=self.slots, err=self.err)
+        swa.swa_tile_bounds(d["query_start_loc"], d["seq_lens"], context_lens=d["context_lens"],
+                            mm_ranges=d["mm_ranges"], window=lay.window, causal=lay.causal,
+                            tile_size=self.TILE, block_q=self.BLOCK_Q, max_qblocks_per_seq=self.maxb,
+                            out=self.bounds, err=self.err)
+
+    def attention(self):
+        lay, d = self.lay, self.d
+        self.swa.swa_mm_paged_attention(
+            self.q, self.k, self.v, d["block_table"], d["query_start_loc"], d["seq_lens"],
+            context_lens=d["context_lens"], mm_ranges=d["mm_ranges"], max_query_len=lay.max_query_len,
+            window=lay.window, causal=lay.causal, scale=lay.scale, out=self.out, lse=self.lse,
+            err=self.err)
+
+    def launches_per_step(self):
+        return 3
+
+
+def run_gpu(args, rank, world, local_rank):
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    lay = W.gemma_like()
+    step = PrefillStep(lay, dev)
+    pairs = visible_pairs_per_head(lay)
+    flops = 4.0 * lay.head_dim * lay.num_heads_q * pairs
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step.feeders()
+        step.attention()
+    barrier()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step.feeders()
+        ev[i][1].record(stream)
+        step.attention()
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    clk = clocks.stop()
+    attn_ms = [a.elapsed_time(b) for _, a, b in ev]
+    feed_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+
+    # end to end through the public API: pinned host inputs -> device -> three
+    # calls -> host, every step inside the timed region
+    host = {"q": step.q.cpu().pin_memory(), "k": step.k.cpu().pin_memory(), "v": step.v.cpu().pin_memory()}
+    for key, t in step.d.items():
+        if t is not None:
+            host[key] = t.cpu().pin_memory()
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    lse_h = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def e2e_step():
+        step.q.copy_(host["q"], non_blocking=True)
+        step.k.copy_(host["k"], non_blocking=True)
+        step.v.copy_(host["v"], non_blocking=True)
+        for key, t in step.d.items():
+            if t is not None:
+                t.copy_(host[key], non_blocking=True)
+        step.feeders()
+        step.attention()
+        out_h.copy_(step.out, non_blocking=True)
+        lse_h.copy_(step.lse, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    torch.cuda.synchronize(dev)
+    err = int(step.err.item())
+    if rank != 0:
+        return None
+
+    pk = peaks()
+    attn_avg = statistics.mean(attn_ms)
+    achieved = flops / (attn_avg * 1e-3) / 1e12
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    tok_s = world * lay.num_tokens / (ms_per_step * 1e-3)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "gemma_like: 4 requests (16550/16294/16806/16550 tokens), 60 images x 256 "
+                        "tokens each, causal SWA W=1024 with the window-clamped image mask, Hq=16, "
+                        "Hkv=8, D=256, bf16, paged KV block 16, slot mapping padded to 73728",
+            "global_batch": lay.num_seqs * world,
+            "seq_len": int(lay.seq_lens.mean()),
+            "tokens_per_step": lay.num_tokens,
+            "visible_pairs_per_head": pairs,
+            "tflop_per_step": round(flops / 1e12, 4),
+            "step": "swa_slot_mapping + swa_tile_bounds + swa_mm_paged_attention",
+            "l2": "inputs larger than L2 (q 0.54 GB, K/V caches 0.54 GB), no flush",
+            "parallelism": f"replicas x{world}",
+        },
+        "tok_per_s": round(tok_s, 1),
+        "pct_of_bf16_peak": round(100.0 * value / world / pk["bf16_tflops"], 2),
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "swa_mm_paged_attention",
+            "achieved": round(achieved, 3),
+            "peak": pk["bf16_tflops"],
+            "unit": "TFLOP/s",
+            "frac": round(achieved / pk["bf16_tflops"], 4),
+            "traffic": None,
+            "peak_source": f"{pk['source']} bf16 dense (burst)",
+            "avg_launch_ms": round(attn_avg, 4),
+        },
+        "feeders_ms": round(statistics.mean(feed_ms), 4),
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * step.launches_per_step(),
+        "clocks": clk,
+        "device_errors": err,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(lay, step, budget_s=args.cpu_seconds)
+    return line
+
+
+# ---------------------------------------------------------------------------
+# the oracle leg (CPU)
+# ---------------------------------------------------------------------------
+def _oracle_sample(lay, q, k, v, budget_s, seed=0):
+    """Time the oracle on (token, head) rows until ``budget_s`` of work; TFLOP/s."""
+    from oracle import swa_oracle as O
+    rng = np.random.default_rng(seed)
+    qsl = lay.query_start_loc
+    s = int(rng.integers(0, lay.num_seqs))
+    hk = int(rng.integers(0, lay.num_heads_kv))
+    n = int(lay.seq_lens[s])
+    pages = lay.block_table[s, :-(-n // lay.block_size)].astype(np.int64)
+    k_s = k[torch.as_tensor(pages)][:, :, hk:hk + 1].cpu()
+    v_s = v[torch.as_tensor(pages)][:, :, hk:hk + 1].cpu()
+    G = lay.group
+    q_s = q[int(qsl[s]):int(qsl[s + 1]), hk * G:(hk + 1) * G].cpu()
+    bt = np.arange(len(pages), dtype=np.int32)[None]
+    mm = None if lay.mm_ranges is None else lay.mm_ranges[s:s + 1]
+    qs = np.array([0, int(lay.query_lens[s])])
+    t0 = time.perf_counter()
+    rows_done, pairs = 0, 0
+    while time.perf_counter() - t0 < budget_s:
+        batch = [(int(t), int(h)) for t, h in zip(rng.integers(0, len(q_s), 8), rng.integers(0, G, 8))]
+        O.attention(q_s, k_s, v_s, bt, qs, [n], mm, lay.window, lay.causal, lay.scale, rows=batch)
+        ctx = n - int(lay.query_lens[s])
+        for t, _ in batch:
+            pairs += int(O.visible_keys(ctx + t, n, lay.window, lay.causal, None if mm is None else mm[0]).sum())
+        rows_done += len(batch)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * lay.head_dim * pairs
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{rows_done} (token, head) rows of sequence {s}, kv head {hk}, "
+                      f"{pairs} visible pairs, {dt:.1f} s on 1 thread (fp64 numpy, per-pair mask)",
+            "rows_per_s": rows_done / dt,
+            "tok_per_s": rows_done / lay.num_heads_q / dt}
+
+
+def cpu_baseline(lay, step, budget_s):
+    return _oracle_sample(lay, step.q, step.k, step.v, budget_s)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    lay = W.gemma_like()
+    q, k, v = W.make_tensors(lay, device="cpu")
+    for _ in range(args.warmup):
+        _oracle_sample(lay, q, k, v, budget_s=0.5, seed=100 + _)
+    vals = []
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        vals.append(_oracle_sample(lay, q, k, v, budget_s=args.cpu_seconds / max(1, args.steps), seed=i))
+    total = time.perf_counter() - t0
+    value = statistics.mean(v["value"] for v in vals)
+    flops_step = 4.0 * lay.head_dim * lay.num_heads_q * visible_pairs_per_head(lay)
+    ms_per_step = flops_step / (value * 1e12) * 1e3
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "gemma_like (same as the GPU arm); each step times the CPU oracle "
+                               "on a bounded sample of its rows and scales to TFLOP/s",
+                   "parallelism": "single process, 1 thread"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} samples of about {args.cpu_seconds / max(1, args.steps):.1f} s "
+                                   f"each ({total:.1f} s total)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl")
+        line = run_gpu(args, rank, world, local_rank)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

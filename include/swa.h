@@ -1,0 +1,214 @@
+/*
+ * swa.h -- C ABI of the GB300 paged sliding-window attention library.
+ *
+ * Varlen prefill/decode attention over a paged KV cache with a sliding window
+ * (SWA) and a window-clamped bidirectional image-prefix mask, plus the two
+ * feeders around it: token -> KV-slot mapping and the log-sum-exp merge of
+ * split-KV partial outputs.  Hand-written CUDA for sm_103a (GB300).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Ownership.  Every array argument is a DEVICE pointer owned by the caller.
+ *   The library allocates no memory and keeps no pointer after a call returns.
+ * Streams.  `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *   default stream.  Each call only enqueues work on `stream` and never
+ *   synchronises the host.
+ * Errors.  The return value is SWA_OK (0), or a negative SWA_E_* code when the
+ *   host-side argument checks fail -- in that case nothing is launched.  Data
+ *   errors that can only be seen on the device (a block id outside the cache,
+ *   a position outside the block-table row, inconsistent lengths, a stalled
+ *   pipeline) set SWA_ERR_* bits in the optional device word `err` with
+ *   atomicOr; the affected entries get PAD / zero / -inf and the kernel keeps
+ *   going.  Kernels never trap.  Pass err = NULL to skip the report.
+ * Layouts (row-major, innermost last):
+ *   q            [num_tokens, num_heads_q, head_dim]            (bf16 or fp32)
+ *   k/v cache    [num_blocks, block_size, num_heads_kv, head_dim] (slot-major:
+ *                slot = block * block_size + offset)
+ *   block_table  [num_seqs, block_table_stride] int32, logical page -> block
+ *   mm_ranges    [num_seqs, max_mm_ranges, 2] int32, inclusive [start, end]
+ *                in absolute sequence positions; start >= end is padding
+ *   out          [num_tokens, num_heads_q, head_dim]   lse [num_tokens, num_heads_q] fp32
+ *   partial_out  [num_splits, num_tokens, num_heads_q, head_dim]
+ *   partial_lse  [num_splits, num_tokens, num_heads_q] fp32
+ * Query token i of sequence s sits at absolute position
+ *   context_lens[s] + i,  with context_lens[s] = seq_lens[s] - query_len[s];
+ * the KV cache already holds all seq_lens[s] keys of the sequence.
+ * Query head h reads kv head h / (num_heads_q / num_heads_kv).
+ */
+#ifndef SWA_GB300_H
+#define SWA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- host-side return codes ------------------------------------------- */
+#define SWA_OK             0
+#define SWA_E_NULL        -1   /* a required pointer is NULL                      */
+#define SWA_E_SIZE        -2   /* a size is negative, zero where it must not be,
+                                  or sizes disagree (e.g. Hq % Hkv != 0)          */
+#define SWA_E_UNSUPPORTED -3   /* dtype / head_dim / block_size not built         */
+#define SWA_E_ALIGN       -4   /* a pointer is not 16-byte aligned               */
+#define SWA_E_CUDA        -5   /* the CUDA runtime or driver reported an error    */
+
+/* ---- device-side error bits (atomicOr into *err) ------------------------ */
+#define SWA_ERR_BLOCK_ID   0x01  /* block_table entry outside [0, num_blocks)      */
+#define SWA_ERR_POSITION   0x02  /* position < 0 or its page beyond the table row  */
+#define SWA_ERR_QSL        0x04  /* query_start_loc not monotone / past num_tokens */
+#define SWA_ERR_LENS       0x08  /* seq_lens / context_lens inconsistent           */
+#define SWA_ERR_TIMEOUT    0x10  /* a bounded pipeline wait gave up                */
+#define SWA_ERR_SPLITS     0x20  /* splits_per_seq entry outside [1, num_splits]   */
+
+/* ---- element types ------------------------------------------------------ */
+#define SWA_DTYPE_BF16 0
+#define SWA_DTYPE_FP32 1
+
+/* Split-KV partitions start on multiples of this many keys (see below). */
+#define SWA_SPLIT_ALIGN 128
+
+/*
+ * swa_slot_mapping -- logical token position -> physical KV-cache slot.
+ *
+ * Defined by the vllm-ascend article on _compute_slot_mapping_kernel,
+ * section 2 ("non-CP path") and section 1 (the padded tail): for token t of
+ * request r, with pos = positions[t],
+ *     slot_mapping[t] = block_table[r][pos / block_size] * block_size
+ *                       + pos % block_size,
+ * and slot_mapping[t] = pad_id for t in [num_tokens, max_num_tokens), which
+ * keeps the output shape fixed for graph capture.
+ *
+ *   query_start_loc  int32[num_reqs + 1], CSR offsets of each request's tokens
+ *   positions        int64[num_tokens]
+ *   block_table      int32[num_reqs, block_table_stride]
+ *   slot_mapping     int32[max_num_tokens] (output)
+ * Host errors: NULL pointers (except err), num_reqs < 0, num_tokens < 0,
+ *   max_num_tokens < num_tokens, block_size <= 0, stride < 1.
+ * Device errors: a position < 0 or whose page index >= block_table_stride
+ *   sets SWA_ERR_POSITION and writes pad_id; query_start_loc that decreases or
+ *   passes num_tokens sets SWA_ERR_QSL (tokens outside every request get pad_id).
+ */
+int swa_slot_mapping(const int32_t *query_start_loc, const int64_t *positions,
+                     const int32_t *block_table, int64_t block_table_stride,
+                     int32_t block_size, int32_t num_reqs, int64_t num_tokens,
+                     int64_t max_num_tokens, int32_t pad_id, int32_t *slot_mapping,
+                     int32_t *err, void *stream);
+
+/*
+ * swa_tile_bounds -- per query block, the KV-tile loop range after pruning.
+ *
+ * Defined by the vLLM PR #53147 summary, the compute_tile_loop_bounds excerpt
+ * and its geometry tests.  Query block b of sequence s holds query rows
+ * qpos_lo = b*block_q .. qpos_hi = min(qpos_lo + block_q - 1, query_len - 1);
+ * q_lo = ctx + qpos_lo, q_hi = ctx + qpos_hi.
+ *   max_seq_prefix_len = seq_len if image ranges are enabled (mm_ranges != NULL
+ *     and max_mm_ranges > 0) or !causal, else min(q_hi + 1, seq_len);
+ *   num_tiles = ceil(max_seq_prefix_len / tile_size);
+ *   window <= 0: [lo, hi) = [0, num_tiles);
+ *   window  > 0: first = q_lo - window + 1; last = causal ? q_hi : q_hi+window-1;
+ *     every valid range [s, e] (s < e) with s <= q_hi and e >= q_lo gives
+ *     first = min(first, max(s, q_lo - window + 1)), last = max(last, e);
+ *     last = min(last, seq_len - 1);
+ *     lo = max(0, floor(first / tile_size)), hi = min(last / tile_size + 1, num_tiles).
+ * (The page takes the block's last row for the window's left edge; this
+ * library takes the first row, which keeps every visible key of the block's
+ * earlier rows inside [lo, hi) and gives the printed [3, 72) and [3, 68).)
+ *
+ *   context_lens  int32[num_seqs] or NULL (then seq_len - query_len)
+ *   out           int32[num_seqs, max_qblocks_per_seq, 3] = {lo, hi,
+ *                 max_seq_prefix_len}; blocks past the query length get {0,0,0}
+ * Host errors: NULL (except context_lens, mm_ranges, err), tile_size <= 0,
+ *   block_q <= 0, num_seqs < 0, max_qblocks_per_seq < 0, max_mm_ranges < 0.
+ * Device errors: context_lens[s] != seq_len - query_len or query_len > seq_len
+ *   sets SWA_ERR_LENS and writes {0, 0, 0} for the sequence.
+ */
+int swa_tile_bounds(const int32_t *query_start_loc, const int32_t *seq_lens,
+                    const int32_t *context_lens, const int32_t *mm_ranges,
+                    int32_t max_mm_ranges, int32_t num_seqs, int32_t window, int32_t causal,
+                    int32_t tile_size, int32_t block_q, int32_t max_qblocks_per_seq,
+                    int32_t *out, int32_t *err, void *stream);
+
+/*
+ * swa_mm_paged_attention -- paged attention with SWA and the clamped image mask.
+ *
+ * Key k of sequence s is visible to the query at absolute position q when
+ * (vLLM PR #53147 summary, implementation items 1-2, "OR semantics"):
+ *     base(q,k): window > 0: k >= q-window+1 and (causal ? k <= q : k <= q+window-1)
+ *                window <= 0: causal ? k <= q : true
+ *  OR mm(q,k):   some valid range [s0,e0] holds both q and k, and
+ *                (window > 0) k >= q - window + 1
+ *  AND 0 <= k < seq_lens[s].
+ * With sc = scale * dot(q, k) over the visible keys:
+ *     out = sum_k exp(sc - m) v_k / sum_k exp(sc - m),  lse = m + ln sum_k exp(sc - m)
+ * (m = max sc, natural log).  Tiles outside the pruned loop range of
+ * swa_tile_bounds are never read.
+ *
+ * Split-KV (num_splits > 1): sequence s uses P_s = splits_per_seq[s] (or
+ * num_splits when splits_per_seq is NULL) partitions.  Partition p covers the
+ * keys [p*L, min((p+1)*L, seq_len)), L = SWA_SPLIT_ALIGN *
+ * ceil(ceil(seq_len / P_s) / SWA_SPLIT_ALIGN).  Each (p, token, head) gets the
+ * normalised partial output over the visible keys of its partition and their
+ * LSE; when the partition holds no visible key for the row (including p >= P_s)
+ * partial_lse = -inf and that partial_out row is NOT written (lse_combine never
+ * reads it).  out / lse are not written in split mode; merge with lse_combine.
+ *
+ *   q, k_cache, v_cache   see layouts; dtype SWA_DTYPE_BF16 or SWA_DTYPE_FP32
+ *   num_blocks            first dimension of the caches (block ids are checked)
+ *   query_start_loc       int32[num_seqs + 1]
+ *   seq_lens              int32[num_seqs]
+ *   context_lens          int32[num_seqs] or NULL (derived)
+ *   mm_ranges             int32[num_seqs, max_mm_ranges, 2] or NULL
+ *   max_query_len         host-side upper bound of the query lengths (selects
+ *                         the decode or prefill kernel; any value >= 1 is safe)
+ *   head_dim              64, 128 or 256;  block_size 16, 32, 64 or 128
+ *   out                   [num_tokens, Hq, D] same dtype as q  (num_splits == 1)
+ *   lse                   fp32 [num_tokens, Hq] or NULL          (num_splits == 1)
+ *   partial_out/partial_lse  required when num_splits > 1, else ignored
+ * Host errors: NULL pointers, non-positive sizes, Hq % Hkv != 0, an unsupported
+ *   dtype/head_dim/block_size, misaligned (not 16-byte) q/k/v/out pointers.
+ * Device errors: SWA_ERR_BLOCK_ID (the page is treated as all-invisible),
+ *   SWA_ERR_LENS, SWA_ERR_SPLITS, SWA_ERR_TIMEOUT.
+ */
+int swa_mm_paged_attention(const void *q, const void *k_cache, const void *v_cache,
+                           int64_t num_blocks, const int32_t *block_table,
+                           int64_t block_table_stride, const int32_t *query_start_loc,
+                           const int32_t *seq_lens, const int32_t *context_lens,
+                           const int32_t *mm_ranges, int32_t max_mm_ranges, int32_t num_seqs,
+                           int64_t num_tokens, int32_t max_query_len, int32_t num_heads_q,
+                           int32_t num_heads_kv, int32_t head_dim, int32_t block_size,
+                           int32_t window, int32_t causal, float scale, int32_t dtype,
+                           int32_t num_splits, const int32_t *splits_per_seq, void *out,
+                           float *lse, void *partial_out, float *partial_lse, int32_t *err,
+                           void *stream);
+
+/*
+ * lse_combine -- merge split-KV partial outputs with their log-sum-exp.
+ *
+ * Defined by the MLA DCP decode study notes, section 1.1 and the LSE glossary
+ * entry (partial results merged by their LSE equal one softmax over the whole
+ * sequence).  Per (token, head):
+ *     L = max_p lse_p;  w_p = exp(lse_p - L);
+ *     out = sum_p w_p * o_p / sum_p w_p;   out_lse = L + ln(sum_p w_p).
+ * Partitions with lse_p = -inf have weight 0 and o_p is not read.  When every
+ * partition is -inf, out = 0 and out_lse = -inf.  Accumulation is fp32.
+ *
+ *   partial_out  [num_splits, num_tokens, num_heads, head_dim] (dtype)
+ *   partial_lse  fp32 [num_splits, num_tokens, num_heads]
+ *   out          [num_tokens, num_heads, head_dim] (dtype)
+ *   out_lse      fp32 [num_tokens, num_heads] or NULL
+ * Host errors: NULL pointers, num_splits < 1, num_tokens < 0, num_heads < 1,
+ *   head_dim not in {64, 128, 256}, unsupported dtype, misaligned pointers.
+ */
+int lse_combine(const void *partial_out, const float *partial_lse, int32_t num_splits,
+                int64_t num_tokens, int32_t num_heads, int32_t head_dim, int32_t dtype,
+                void *out, float *out_lse, void *stream);
+
+/* Library version string, e.g. "swa-gb300 0.1 sm_103a". */
+const char *swa_version(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* SWA_GB300_H */

@@ -1,0 +1,117 @@
+// The C ABI (include/swa.h): host-side argument checks, then one launch per
+// call on the caller's stream.  Nothing here allocates device memory.
+#include <cmath>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
+inline bool block_size_ok(int b) { return b == 16 || b == 32 || b == 64 || b == 128; }
+inline cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+inline int finish(cudaError_t e) { return e == cudaSuccess ? SWA_OK : SWA_E_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *swa_version(void) { return "swa-gb300 0.1 sm_103a"; }
+
+int swa_slot_mapping(const int32_t *query_start_loc, const int64_t *positions,
+                     const int32_t *block_table, int64_t block_table_stride, int32_t block_size,
+                     int32_t num_reqs, int64_t num_tokens, int64_t max_num_tokens, int32_t pad_id,
+                     int32_t *slot_mapping, int32_t *err, void *stream) {
+  if (num_reqs < 0 || num_tokens < 0 || max_num_tokens < num_tokens || block_size <= 0 ||
+      block_table_stride < 1)
+    return SWA_E_SIZE;
+  if (max_num_tokens == 0) return SWA_OK;
+  if (slot_mapping == nullptr || query_start_loc == nullptr) return SWA_E_NULL;
+  if (num_tokens > 0 && (positions == nullptr || block_table == nullptr)) return SWA_E_NULL;
+  if (max_num_tokens > INT32_MAX) return SWA_E_SIZE;
+  return finish(swa::launch_slot_mapping(query_start_loc, positions, block_table, block_table_stride,
+                                         block_size, num_reqs, num_tokens, max_num_tokens, pad_id,
+                                         slot_mapping, err, as_stream(stream)));
+}
+
+int swa_tile_bounds(const int32_t *query_start_loc, const int32_t *seq_lens,
+                    const int32_t *context_lens, const int32_t *mm_ranges, int32_t max_mm_ranges,
+                    int32_t num_seqs, int32_t window, int32_t causal, int32_t tile_size,
+                    int32_t block_q, int32_t max_qblocks_per_seq, int32_t *out, int32_t *err,
+                    void *stream) {
+  if (tile_size <= 0 || block_q <= 0 || num_seqs < 0 || max_qblocks_per_seq < 0 || max_mm_ranges < 0)
+    return SWA_E_SIZE;
+  if (num_seqs == 0 || max_qblocks_per_seq == 0) return SWA_OK;
+  if (query_start_loc == nullptr || seq_lens == nullptr || out == nullptr) return SWA_E_NULL;
+  if (num_seqs > 65535) return SWA_E_SIZE;
+  return finish(swa::launch_tile_bounds(query_start_loc, seq_lens, context_lens, mm_ranges,
+                                        max_mm_ranges, num_seqs, window, causal, tile_size, block_q,
+                                        max_qblocks_per_seq, out, err, as_stream(stream)));
+}
+
+int swa_mm_paged_attention(const void *q, const void *k_cache, const void *v_cache,
+                           int64_t num_blocks, const int32_t *block_table,
+                           int64_t block_table_stride, const int32_t *query_start_loc,
+                           const int32_t *seq_lens, const int32_t *context_lens,
+                           const int32_t *mm_ranges, int32_t max_mm_ranges, int32_t num_seqs,
+                           int64_t num_tokens, int32_t max_query_len, int32_t num_heads_q,
+                           int32_t num_heads_kv, int32_t head_dim, int32_t block_size,
+                           int32_t window, int32_t causal, float scale, int32_t dtype,
+                           int32_t num_splits, const int32_t *splits_per_seq, void *out,
+                           float *lse, void *partial_out, float *partial_lse, int32_t *err,
+                           void *stream) {
+  if (num_seqs < 0 || num_tokens < 0 || num_blocks < 0 || block_table_stride < 1 ||
+      max_mm_ranges < 0 || num_heads_q < 1 || num_heads_kv < 1 || num_splits < 1 ||
+      max_query_len < 0)
+    return SWA_E_SIZE;
+  if (num_heads_q % num_heads_kv != 0 || num_heads_q / num_heads_kv > 32) return SWA_E_SIZE;
+  if (num_heads_kv > 65535 || num_splits > 65535) return SWA_E_SIZE;
+  if (dtype != SWA_DTYPE_BF16 && dtype != SWA_DTYPE_FP32) return SWA_E_UNSUPPORTED;
+  if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return SWA_E_UNSUPPORTED;
+  if (!std::isfinite(scale)) return SWA_E_SIZE;
+  if (num_tokens == 0 || num_seqs == 0) return SWA_OK;
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
+      query_start_loc == nullptr || seq_lens == nullptr)
+    return SWA_E_NULL;
+  if (num_splits > 1) {
+    if (partial_out == nullptr || partial_lse == nullptr) return SWA_E_NULL;
+    if (!aligned16(partial_out)) return SWA_E_ALIGN;
+  } else {
+    if (out == nullptr) return SWA_E_NULL;
+    if (!aligned16(out)) return SWA_E_ALIGN;
+  }
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return SWA_E_ALIGN;
+
+  swa::AttnArgs a;
+  a.q = q; a.k_cache = k_cache; a.v_cache = v_cache; a.num_blocks = num_blocks;
+  a.block_table = block_table; a.bt_stride = block_table_stride;
+  a.qsl = query_start_loc; a.seq_lens = seq_lens; a.ctx_lens = context_lens;
+  a.mm_ranges = (max_mm_ranges > 0) ? mm_ranges : nullptr;
+  a.max_mm_ranges = (mm_ranges != nullptr) ? max_mm_ranges : 0;
+  a.num_seqs = num_seqs; a.num_tokens = num_tokens; a.max_query_len = max_query_len;
+  a.hq = num_heads_q; a.hkv = num_heads_kv; a.head_dim = head_dim; a.block_size = block_size;
+  a.window = window; a.causal = causal != 0; a.scale = scale; a.dtype = dtype;
+  a.num_splits = num_splits; a.splits_per_seq = (num_splits > 1) ? splits_per_seq : nullptr;
+  a.out = out; a.lse = lse; a.partial_out = partial_out; a.partial_lse = partial_lse; a.err = err;
+
+  cudaStream_t st = as_stream(stream);
+  if (swa::tc_supported(a)) return finish(swa::launch_attention_tc(a, st));
+  if (swa::decode_supported(a)) return finish(swa::launch_attention_decode(a, st));
+  return finish(swa::launch_attention_simt(a, st));
+}
+
+int lse_combine(const void *partial_out, const float *partial_lse, int32_t num_splits,
+                int64_t num_tokens, int32_t num_heads, int32_t head_dim, int32_t dtype, void *out,
+                float *out_lse, void *stream) {
+  if (num_splits < 1 || num_tokens < 0 || num_heads < 1) return SWA_E_SIZE;
+  if (!head_dim_ok(head_dim)) return SWA_E_UNSUPPORTED;
+  if (dtype != SWA_DTYPE_BF16 && dtype != SWA_DTYPE_FP32) return SWA_E_UNSUPPORTED;
+  if (num_tokens == 0) return SWA_OK;
+  if (partial_out == nullptr || partial_lse == nullptr || out == nullptr) return SWA_E_NULL;
+  if (!aligned16(partial_out) || !aligned16(out)) return SWA_E_ALIGN;
+  return finish(swa::launch_lse_combine(partial_out, partial_lse, num_splits, num_tokens, num_heads,
+                                        head_dim, dtype, out, out_lse, as_stream(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,54 @@
+// Internal launchers behind the C ABI (host side).  Arguments are validated
+// by the ABI layer before these are called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace swa {
+
+struct AttnArgs {
+  const void *q, *k_cache, *v_cache;
+  int64_t num_blocks;
+  const int32_t *block_table;
+  int64_t bt_stride;
+  const int32_t *qsl, *seq_lens, *ctx_lens, *mm_ranges;
+  int32_t max_mm_ranges, num_seqs;
+  int64_t num_tokens;
+  int32_t max_query_len, hq, hkv, head_dim, block_size, window, causal;
+  float scale;
+  int32_t dtype, num_splits;
+  const int32_t *splits_per_seq;
+  void *out;
+  float *lse;
+  void *partial_out;
+  float *partial_lse;
+  int32_t *err;
+};
+
+cudaError_t launch_slot_mapping(const int32_t *qsl, const int64_t *pos, const int32_t *bt,
+                                int64_t stride, int32_t block_size, int32_t num_reqs,
+                                int64_t num_tokens, int64_t max_num_tokens, int32_t pad_id,
+                                int32_t *out, int32_t *err, cudaStream_t st);
+
+cudaError_t launch_tile_bounds(const int32_t *qsl, const int32_t *seq_lens, const int32_t *ctx,
+                               const int32_t *mm, int32_t max_mm, int32_t num_seqs, int32_t window,
+                               int32_t causal, int32_t tile, int32_t bq, int32_t max_qblocks,
+                               int32_t *out, int32_t *err, cudaStream_t st);
+
+cudaError_t launch_lse_combine(const void *po, const float *pl, int32_t num_splits,
+                               int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                               int32_t dtype, void *out, float *out_lse, cudaStream_t st);
+
+// General CUDA-core attention: any supported dtype / head_dim, split or not.
+cudaError_t launch_attention_simt(const AttnArgs &a, cudaStream_t st);
+
+// Split-KV decode: bf16, few query tokens per sequence, TMA-staged K/V.
+bool decode_supported(const AttnArgs &a);
+cudaError_t launch_attention_decode(const AttnArgs &a, cudaStream_t st);
+
+// tcgen05 / TMEM / TMA prefill: bf16, head_dim 128 or 256, no split.
+bool tc_supported(const AttnArgs &a);
+cudaError_t launch_attention_tc(const AttnArgs &a, cudaStream_t st);
+
+}  // namespace swa

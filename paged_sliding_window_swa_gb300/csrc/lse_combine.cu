@@ -1,0 +1,137 @@
+// Merge of split-KV partial outputs by their log-sum-exp (MLA DCP decode study
+// notes, section 1.1: partials merged by LSE equal one softmax over the whole
+// sequence).
+//
+// A group of LPR lanes owns one (token, head) row; every lane moves 16-byte
+// vectors, so a row of D bf16 values is read with D*2/16 lanes in one
+// coalesced sweep per partition.  Partitions whose LSE is -inf are skipped
+// before their output is touched, so their (unwritten) rows are never read.
+#include "common.cuh"
+#include "launch.h"
+
+namespace swa {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename T, int D>
+struct CombineShape {
+  static constexpr int kVecElems = 16 / sizeof(T);            // elements per 16-byte vector
+  static constexpr int kVecs = D / kVecElems;                  // vectors per row
+  static constexpr int kLpr = kVecs < 32 ? kVecs : 32;         // lanes per row
+  static constexpr int kVpl = kVecs / kLpr;                    // vectors per lane
+  static constexpr int kRowsPerWarp = 32 / kLpr;
+};
+
+template <typename T>
+__device__ inline void accum(float *acc, const uint4 &v, float w) {
+  if constexpr (sizeof(T) == 2) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f = __bfloat1622float2(h[i]);
+      acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
+      acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+    }
+  } else {
+    const float *f = reinterpret_cast<const float *>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = fmaf(w, f[i], acc[i]);
+  }
+}
+
+template <typename T>
+__device__ inline uint4 pack(const float *x) {
+  uint4 r;
+  if constexpr (sizeof(T) == 2) {
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+  } else {
+    float *f = reinterpret_cast<float *>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = x[i];
+  }
+  return r;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads)
+lse_combine_kernel(const T *__restrict__ po, const float *__restrict__ pl, int32_t num_splits,
+                   int64_t rows, T *__restrict__ out, float *__restrict__ out_lse) {
+  using Sh = CombineShape<T, D>;
+  constexpr int E = Sh::kVecElems;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / Sh::kLpr;              // row within the warp
+  const int gl = lane % Sh::kLpr;               // lane within the row group
+  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int64_t row = warp * Sh::kRowsPerWarp + sub;
+  const bool live = row < rows;
+
+  // 1) L = max_p lse_p over the group's lanes
+  float L = -INFINITY;
+  if (live)
+    for (int p = gl; p < num_splits; p += Sh::kLpr) L = fmaxf(L, __ldg(pl + (int64_t)p * rows + row));
+#pragma unroll
+  for (int o = Sh::kLpr / 2; o > 0; o >>= 1) L = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, o));  // stays inside the group
+
+  float acc[Sh::kVpl * E];
+#pragma unroll
+  for (int i = 0; i < Sh::kVpl * E; ++i) acc[i] = 0.f;
+  float wsum = 0.f;
+  if (live && L != -INFINITY) {
+    for (int p = 0; p < num_splits; ++p) {
+      const float lp = __ldg(pl + (int64_t)p * rows + row);
+      if (lp == -INFINITY) continue;
+      const float w = expf(lp - L);
+      wsum += w;
+      const uint4 *src = reinterpret_cast<const uint4 *>(po + ((int64_t)p * rows + row) * D);
+#pragma unroll
+      for (int v = 0; v < Sh::kVpl; ++v) accum<T>(acc + v * E, __ldg(src + gl + v * Sh::kLpr), w);
+    }
+  }
+  if (!live) return;
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+  for (int i = 0; i < Sh::kVpl * E; ++i) acc[i] *= inv;
+  uint4 *dst = reinterpret_cast<uint4 *>(out + row * D);
+#pragma unroll
+  for (int v = 0; v < Sh::kVpl; ++v) dst[gl + v * Sh::kLpr] = pack<T>(acc + v * E);
+  if (out_lse != nullptr && gl == 0) out_lse[row] = (wsum > 0.f) ? L + logf(wsum) : -INFINITY;
+}
+
+template <typename T, int D>
+cudaError_t run(const void *po, const float *pl, int32_t P, int64_t rows, void *out, float *ol,
+                cudaStream_t st) {
+  using Sh = CombineShape<T, D>;
+  const int64_t rows_per_block = (kThreads / 32) * Sh::kRowsPerWarp;
+  const int64_t grid = ceil_div(rows, rows_per_block);
+  if (grid == 0) return cudaSuccess;
+  lse_combine_kernel<T, D><<<(unsigned)grid, kThreads, 0, st>>>(
+      static_cast<const T *>(po), pl, P, rows, static_cast<T *>(out), ol);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_lse_combine(const void *po, const float *pl, int32_t num_splits,
+                               int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                               int32_t dtype, void *out, float *out_lse, cudaStream_t st) {
+  const int64_t rows = num_tokens * num_heads;
+  if (dtype == SWA_DTYPE_BF16) {
+    switch (head_dim) {
+      case 64: return run<__nv_bfloat16, 64>(po, pl, num_splits, rows, out, out_lse, st);
+      case 128: return run<__nv_bfloat16, 128>(po, pl, num_splits, rows, out, out_lse, st);
+      case 256: return run<__nv_bfloat16, 256>(po, pl, num_splits, rows, out, out_lse, st);
+    }
+  } else {
+    switch (head_dim) {
+      case 64: return run<float, 64>(po, pl, num_splits, rows, out, out_lse, st);
+      case 128: return run<float, 128>(po, pl, num_splits, rows, out, out_lse, st);
+      case 256: return run<float, 256>(po, pl, num_splits, rows, out, out_lse, st);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace swa

@@ -1,0 +1,103 @@
+// Token position -> physical KV-cache slot
+// (vllm-ascend article on _compute_slot_mapping_kernel, sections 1-2).
+//
+// Token-flat grid: every thread maps 4 consecutive tokens, so positions are
+// read as two 16-byte vectors and slots written as one; the padded tail
+// [num_tokens, max_num_tokens) is filled by the same threads.  A thread finds
+// its request by binary search over query_start_loc once and walks forward.
+// Neighbouring tokens share block-table entries, so each entry is fetched from
+// DRAM once and served from L1/L2 afterwards -- the job of the page's bounded
+// block-table window, without staging it by hand.
+#include "common.cuh"
+#include "launch.h"
+
+namespace swa {
+namespace {
+
+constexpr int kTokPerThread = 4;
+constexpr int kThreads = 256;
+
+__device__ inline int find_req(const int32_t *qsl, int num_reqs, int64_t t) {
+  // largest r in [0, num_reqs) with qsl[r] <= t
+  int lo = 0, hi = num_reqs - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(qsl + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads)
+slot_mapping_kernel(const int32_t *__restrict__ qsl, const int64_t *__restrict__ pos,
+                    const int32_t *__restrict__ bt, int64_t stride, int32_t block_size,
+                    int32_t num_reqs, int64_t num_tokens, int64_t max_num_tokens, int32_t pad_id,
+                    int32_t *__restrict__ out, int32_t *__restrict__ err) {
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // query_start_loc sanity: monotone, starts >= 0, ends <= num_tokens
+  if (tid < num_reqs) {
+    int32_t a = __ldg(qsl + tid), b = __ldg(qsl + tid + 1);
+    if (a > b || a < 0 || b > num_tokens) report(err, SWA_ERR_QSL);
+  }
+  const int64_t t0 = tid * kTokPerThread;
+  if (t0 >= max_num_tokens) return;
+
+  int32_t res[kTokPerThread];
+  if (t0 >= num_tokens || num_reqs == 0) {
+#pragma unroll
+    for (int i = 0; i < kTokPerThread; ++i) res[i] = pad_id;
+  } else {
+    int64_t p[kTokPerThread];
+    if (kVec && t0 + kTokPerThread <= num_tokens) {
+      const longlong2 *src = reinterpret_cast<const longlong2 *>(pos + t0);
+      longlong2 a = __ldg(src), b = __ldg(src + 1);
+      p[0] = a.x; p[1] = a.y; p[2] = b.x; p[3] = b.y;
+    } else {
+#pragma unroll
+      for (int i = 0; i < kTokPerThread; ++i) p[i] = (t0 + i < num_tokens) ? __ldg(pos + t0 + i) : 0;
+    }
+    int r = find_req(qsl, num_reqs, t0);
+    int32_t r_end = __ldg(qsl + r + 1);
+#pragma unroll
+    for (int i = 0; i < kTokPerThread; ++i) {
+      const int64_t t = t0 + i;
+      res[i] = pad_id;
+      if (t >= num_tokens) continue;
+      while (r + 1 < num_reqs && t >= r_end) { ++r; r_end = __ldg(qsl + r + 1); }
+      if (t < __ldg(qsl + r) || t >= r_end) continue;        // outside every request
+      const int64_t ps = p[i];
+      const int64_t page = ps / block_size;
+      if (ps < 0 || page >= stride) { report(err, SWA_ERR_POSITION); continue; }
+      const int32_t blk = __ldg(bt + (int64_t)r * stride + page);
+      res[i] = (int32_t)((int64_t)blk * block_size + (ps - page * block_size));
+    }
+  }
+  if (kVec && t0 + kTokPerThread <= max_num_tokens) {
+    *reinterpret_cast<int4 *>(out + t0) = make_int4(res[0], res[1], res[2], res[3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < kTokPerThread; ++i)
+      if (t0 + i < max_num_tokens) out[t0 + i] = res[i];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_slot_mapping(const int32_t *qsl, const int64_t *pos, const int32_t *bt,
+                                int64_t stride, int32_t block_size, int32_t num_reqs,
+                                int64_t num_tokens, int64_t max_num_tokens, int32_t pad_id,
+                                int32_t *out, int32_t *err, cudaStream_t st) {
+  const int64_t work = max(ceil_div(max_num_tokens, kTokPerThread), (int64_t)num_reqs);
+  if (work == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)ceil_div(work, kThreads);
+  const bool vec = ((uintptr_t)pos % 16 == 0) && ((uintptr_t)out % 16 == 0);
+  if (vec)
+    slot_mapping_kernel<true><<<grid, kThreads, 0, st>>>(qsl, pos, bt, stride, block_size, num_reqs,
+                                                         num_tokens, max_num_tokens, pad_id, out, err);
+  else
+    slot_mapping_kernel<false><<<grid, kThreads, 0, st>>>(qsl, pos, bt, stride, block_size, num_reqs,
+                                                          num_tokens, max_num_tokens, pad_id, out, err);
+  return cudaGetLastError();
+}
+
+}  // namespace swa

@@ -1,0 +1,76 @@
+// Per-query-block KV-tile loop range after sliding-window pruning with the
+// window-clamped image union (vLLM PR #53147 summary, compute_tile_loop_bounds
+// excerpt).  One thread per (sequence, query block).
+#include "common.cuh"
+#include "launch.h"
+
+namespace swa {
+namespace {
+
+__device__ inline int floor_div(int a, int b) {
+  int q = a / b;
+  return (a % b != 0 && ((a < 0) != (b < 0))) ? q - 1 : q;
+}
+
+__global__ void tile_bounds_kernel(const int32_t *__restrict__ qsl, const int32_t *__restrict__ seq_lens,
+                                   const int32_t *__restrict__ ctx_lens, const int32_t *__restrict__ mm,
+                                   int32_t max_mm, int32_t num_seqs, int32_t window, int32_t causal,
+                                   int32_t tile, int32_t bq, int32_t max_qblocks,
+                                   int32_t *__restrict__ out, int32_t *__restrict__ err) {
+  const int s = blockIdx.y;
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= num_seqs || b >= max_qblocks) return;
+  int32_t *o = out + ((int64_t)s * max_qblocks + b) * 3;
+  const int qlen = __ldg(qsl + s + 1) - __ldg(qsl + s);
+  const int seq_len = __ldg(seq_lens + s);
+  int ctx = seq_len - qlen;
+  if (qlen < 0 || ctx < 0 || (ctx_lens != nullptr && __ldg(ctx_lens + s) != ctx)) {
+    if (b == 0) report(err, SWA_ERR_LENS);
+    o[0] = o[1] = o[2] = 0;
+    return;
+  }
+  const int qpos_lo = b * bq;
+  if (qpos_lo >= qlen) { o[0] = o[1] = o[2] = 0; return; }
+  const int qpos_hi = min(qpos_lo + bq - 1, qlen - 1);
+  const bool use_mm = (mm != nullptr) && (max_mm > 0);
+  const int q_lo = ctx + qpos_lo, q_hi = ctx + qpos_hi;
+  const int max_prefix = (use_mm || !causal) ? seq_len : min(q_hi + 1, seq_len);
+  const int num_tiles = (int)ceil_div(max_prefix, tile);
+  int lo = 0, hi = num_tiles;
+  if (window > 0) {
+    int first = q_lo - window + 1;
+    int last = causal ? q_hi : q_hi + window - 1;
+    if (use_mm) {
+      const int32_t *r = mm + (int64_t)s * max_mm * 2;
+      for (int i = 0; i < max_mm; ++i) {
+        const int rs = __ldg(r + 2 * i), re = __ldg(r + 2 * i + 1);
+        if (rs < re && rs <= q_hi && re >= q_lo) {
+          first = min(first, max(rs, q_lo - window + 1));
+          last = max(last, re);
+        }
+      }
+    }
+    last = min(last, seq_len - 1);
+    lo = max(0, floor_div(first, tile));
+    hi = min(floor_div(last, tile) + 1, num_tiles);
+  }
+  o[0] = lo;
+  o[1] = hi;
+  o[2] = max_prefix;
+}
+
+}  // namespace
+
+cudaError_t launch_tile_bounds(const int32_t *qsl, const int32_t *seq_lens, const int32_t *ctx,
+                               const int32_t *mm, int32_t max_mm, int32_t num_seqs, int32_t window,
+                               int32_t causal, int32_t tile, int32_t bq, int32_t max_qblocks,
+                               int32_t *out, int32_t *err, cudaStream_t st) {
+  if (num_seqs == 0 || max_qblocks == 0) return cudaSuccess;
+  const int threads = 128;
+  dim3 grid((unsigned)ceil_div(max_qblocks, threads), (unsigned)num_seqs);
+  tile_bounds_kernel<<<grid, threads, 0, st>>>(qsl, seq_lens, ctx, mm, max_mm, num_seqs, window,
+                                               causal, tile, bq, max_qblocks, out, err);
+  return cudaGetLastError();
+}
+
+}  // namespace swa

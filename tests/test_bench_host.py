@@ -1,0 +1,23 @@
+"""Host-side checks of bench.py: its visible-pair count (the FLOP numerator)
+equals the oracle's per-pair count."""
+import numpy as np
+import pytest
+
+import bench
+import workloads as W
+from oracle import swa_oracle as O
+
+
+@pytest.mark.parametrize("lay", [W.tiny(), W.geometry("causal"), W.geometry("noncausal")]
+                         + [W.random_small(s, max_seqs=3, max_ctx=200, max_q=150) for s in range(8)],
+                         ids=lambda l: l.name)
+def test_visible_pair_count_matches_oracle(lay):
+    ref = O.allowed_pair_count(lay.query_start_loc, lay.seq_lens, lay.mm_ranges, lay.window, lay.causal)
+    assert bench.visible_pairs_per_head(lay) == ref
+
+
+def test_gemma_like_count_is_stable():
+    lay = W.gemma_like()
+    n = bench.visible_pairs_per_head(lay)
+    # about W + half an image per query beyond the window
+    assert 60e6 < n < 90e6

@@ -1,0 +1,172 @@
+"""GPU parity of swa_mm_paged_attention against the fp64 oracle.
+
+Small layouts are compared on every (token, head) row; the full-size
+workloads on sampled rows (every sequence's first and last token, image
+boundaries, and random rows), each sequence cut out with its own pages so the
+oracle stays fast.  The bar is max-abs 2e-2 for bf16 inputs (fp32
+accumulation) and 2e-3 for fp32 inputs; LSE within 5e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from _gpu_helpers import (LSE_ATOL, atol_for, gpu_inputs, max_errors, oracle_rows, run_attention,
+                          sample_rows)
+from oracle import swa_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture
+def err():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def _all_rows(lay):
+    return [(t, h) for t in range(lay.num_tokens) for h in range(lay.num_heads_q)]
+
+
+def _check(lay, rows, poison=False, err=None, data_seed=1):
+    q, k, v, d = gpu_inputs(lay, data_seed=data_seed, poison=poison)
+    out, lse = run_attention(lay, q, k, v, d, err=err)
+    ro, rl = oracle_rows(lay, q, k, v, rows)
+    e_out, e_lse = max_errors(out, lse, ro, rl, rows)
+    assert e_out <= atol_for(lay), f"{lay.name}: max-abs {e_out}"
+    assert e_lse <= LSE_ATOL, f"{lay.name}: lse max-abs {e_lse}"
+    if err is not None:
+        torch.cuda.synchronize()
+        assert err.item() == 0, hex(err.item())
+    return out, lse, (q, k, v, d)
+
+
+def test_tiny_all_rows(err):
+    lay = W.tiny()
+    _check(lay, _all_rows(lay), err=err)
+
+
+@pytest.mark.parametrize("variant", ["causal", "noncausal", "noncausal-wide"])
+def test_geometry_rows(variant, err):
+    lay = W.geometry(variant)
+    rows = [(t, h) for t in range(0, lay.num_tokens, 3) for h in range(lay.num_heads_q)]
+    rows += [(t, h) for t in range(1100, 1300) for h in (0, 5)]
+    _check(lay, sorted(set(rows)), err=err)
+
+
+def test_gemma_like_sampled(err):
+    lay = W.gemma_like()
+    edges = []
+    qsl = lay.query_start_loc
+    for s in range(lay.num_seqs):
+        for (a, b) in lay.mm_ranges[s][:6]:
+            edges += [qsl[s] + a - 1, qsl[s] + a, qsl[s] + b, qsl[s] + b + 1]
+    rows = sample_rows(lay, 600, extra_tokens=edges)
+    _check(lay, rows, err=err)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_chunked_prefill_sampled(causal, err):
+    lay = W.chunked_prefill(causal)
+    qsl, ctx = lay.query_start_loc, lay.context_lens
+    edges = []
+    for s in range(lay.num_seqs):
+        edges += [qsl[s], qsl[s] + 1, qsl[s] + 127, qsl[s] + 128]      # the straddling image
+    _check(lay, sample_rows(lay, 500, extra_tokens=edges), err=err)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_small_all_rows(seed, err):
+    dtype = "fp32" if seed % 4 == 3 else "bf16"
+    lay = W.random_small(seed, dtype=dtype, max_seqs=3, max_ctx=500, max_q=260)
+    _check(lay, _all_rows(lay), err=err)
+
+
+@pytest.mark.parametrize("D,B,G", [(128, 16, 2), (256, 16, 2), (128, 16, 4), (256, 32, 1),
+                                   (128, 64, 8), (64, 128, 4), (128, 128, 16)])
+def test_shapes_all_rows(D, B, G, err):
+    lay = W.random_small(100 + D + B + G, head_dim=D, block_size=B, group=G, max_seqs=3, max_ctx=700,
+                         max_q=300, window=int(np.random.default_rng(D + B).choice([48, 300])),
+                         with_ranges=True)
+    _check(lay, _all_rows(lay), err=err)
+
+
+def test_unused_cache_rows_never_reach_the_output(err):
+    """Spare blocks and page tails hold NaN; the output must stay finite and exact."""
+    for seed in range(4):
+        lay = W.random_small(40 + seed, max_seqs=3, max_ctx=300, max_q=200, block_size=64,
+                             with_ranges=True)
+        out, _, _ = _check(lay, _all_rows(lay), poison=True, err=err)
+        assert torch.isfinite(out.float()).all()
+
+
+def test_removing_image_ranges_changes_output(err):
+    lay = W.geometry("causal")
+    q, k, v, d = gpu_inputs(lay)
+    with_mm, _ = run_attention(lay, q, k, v, d, err=err)
+    without, _ = run_attention(lay, q, k, v, d, err=err, mm=False)
+    rows = [(t, h) for t in range(1024, 2304, 16) for h in range(lay.num_heads_q)]
+    ro, rl = oracle_rows(lay, q, k, v, rows)
+    e_out, _ = max_errors(with_mm, None, ro, rl, rows)
+    change = (with_mm.float() - without.float()).abs()[1024:2304].max().item()
+    assert change >= max(4 * e_out, 1e-3), (change, e_out)
+
+
+def test_bad_block_id_is_reported(err):
+    lay = W.random_small(9, max_seqs=2, max_q=100, max_ctx=100)
+    q, k, v, d = gpu_inputs(lay)
+    d["block_table"][0, 0] = lay.num_blocks + 5
+    out, _ = run_attention(lay, q, k, v, d, err=err)
+    torch.cuda.synchronize()
+    assert err.item() & 0x01
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_split_partials_and_merge(seed, err):
+    from paged_sliding_window_swa_gb300 import lse_combine
+    P = [2, 3, 5, 8, 16, 4][seed]
+    lay = W.random_small(200 + seed, max_seqs=3, max_ctx=2000, max_q=40, num_splits=P,
+                         with_ranges=seed % 2 == 0, dtype="fp32" if seed == 5 else "bf16")
+    q, k, v, d = gpu_inputs(lay)
+    po, pl = run_attention(lay, q, k, v, d, err=err)
+    rows = _all_rows(lay)
+    ro, rl = oracle_rows(lay, q, k, v, rows, num_splits=P)
+    pof = po.float().cpu().numpy()
+    plc = pl.cpu().numpy()
+    for (p, t, h), val in ro.items():
+        if rl[(p, t, h)] == -np.inf:
+            assert plc[p, t, h] == -np.inf
+        else:
+            assert abs(plc[p, t, h] - rl[(p, t, h)]) <= LSE_ATOL
+            assert np.abs(pof[p, t, h] - val).max() <= atol_for(lay)
+    mo, ml = lse_combine(po, pl)
+    uo, ul = oracle_rows(lay, q, k, v, rows)
+    e_out, e_lse = max_errors(mo, ml, uo, ul, rows)
+    assert e_out <= atol_for(lay) and e_lse <= LSE_ATOL
+    torch.cuda.synchronize()
+    assert err.item() == 0
+
+
+def test_decode_split_kv_sampled(err):
+    """128 single-token queries over 4k-64k contexts, 8-32 partitions, merged."""
+    from paged_sliding_window_swa_gb300 import lse_combine
+    lay = W.decode()
+    q, k, v, d = gpu_inputs(lay)
+    po, pl = run_attention(lay, q, k, v, d, err=err)
+    mo, ml = lse_combine(po, pl)
+    rng = np.random.default_rng(0)
+    seqs = sorted(set(rng.integers(0, lay.num_seqs, 6).tolist()) | {int(np.argmax(lay.seq_lens))})
+    rows = [(int(s), int(h)) for s in seqs for h in rng.integers(0, lay.num_heads_q, 3)]
+    ro, rl = oracle_rows(lay, q, k, v, rows, num_splits=lay.num_splits)
+    pof, plc = po.float().cpu().numpy(), pl.cpu().numpy()
+    for (p, t, h), val in ro.items():
+        if rl[(p, t, h)] == -np.inf:
+            assert plc[p, t, h] == -np.inf
+        else:
+            assert abs(plc[p, t, h] - rl[(p, t, h)]) <= LSE_ATOL
+            assert np.abs(pof[p, t, h] - val).max() <= 2e-2
+    uo, ul = oracle_rows(lay, q, k, v, rows)
+    e_out, e_lse = max_errors(mo, ml, uo, ul, rows)
+    assert e_out <= 2e-2 and e_lse <= LSE_ATOL
+    torch.cuda.synchronize()
+    assert err.item() == 0
