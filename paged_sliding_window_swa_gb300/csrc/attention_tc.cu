@@ -1,10 +1,480 @@
-// tcgen05 prefill attention (placeholder until the tensor-core kernel lands).
+// Tensor-core (tcgen05 / TMEM / TMA) prefill attention over the paged KV
+// cache with the sliding window and the window-clamped image mask (vLLM PR
+// #53147 summary, implementation items 1-2 and the compute_tile_loop_bounds
+// excerpt).
+//
+// One CTA = one 128-row query tile: BQ = 128 / G query positions x the G query
+// heads of one kv head (GQA packing -- every K/V tile is staged once for the
+// whole group).  Six warps:
+//   warp 0     TMA producer: the Q tile once, then K and V tiles of N keys,
+//              gathered page by page through the block table into a
+//              STAGES-deep ring (128-byte swizzled, one box per page and
+//              64-column chunk; pages past the sequence or with a bad block id
+//              are read from outside the tensor, which the TMA fills with 0).
+//   warp 1     tcgen05 issuer and TMEM owner: S = Q K^T into one of two TMEM S
+//              buffers, then O += P V with P read from TMEM (where the
+//              softmax wrote it over S) and V from shared memory (MN-major).
+//   warps 2-5  softmax: thread i owns row i (TMEM lane i); masks only tiles
+//              not fully inside its visible interval, keeps a running max in
+//              the log2 domain and rescales O in TMEM only when the max grows
+//              by more than 2^8, writes P as bf16 into TMEM, and finally
+//              normalises O and stores out / lse.
+// The key loop covers only the union of the rows' visible intervals -- the
+// pruned tile range [lo, hi) of the union formula.  Every mbarrier wait is
+// bounded in time; on expiry the CTA sets SWA_ERR_TIMEOUT, drains its own
+// TMA loads and MMAs, frees TMEM and exits.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
+#include "tc_ptx.cuh"
 
 namespace swa {
+namespace {
 
-bool tc_supported(const AttnArgs &) { return false; }
-cudaError_t launch_attention_tc(const AttnArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+using namespace tc;
+
+constexpr uint64_t kWaitLimitNs = 200000000ull;    // 200 ms per wait: far above any real stall
+
+template <int D_, int N_, int ST_>
+struct Cfg {
+  static constexpr int D = D_;          // head dim
+  static constexpr int N = N_;          // keys per K/V tile
+  static constexpr int ST = ST_;        // K/V ring depth
+  static constexpr int M = 128;         // query rows per CTA
+  static constexpr int CH = D / 64;     // 128-byte column chunks per row
+  static constexpr int Q_CHUNK = M * 128;
+  static constexpr int Q_BYTES = M * D * 2;
+  static constexpr int KV_CHUNK = N * 128;
+  static constexpr int KV_BYTES = N * D * 2;
+  static constexpr int OFF_K = Q_BYTES;
+  static constexpr int OFF_V = OFF_K + ST * KV_BYTES;
+  static constexpr int SMEM = OFF_V + ST * KV_BYTES + 1024;      // + alignment slack
+  static constexpr int TM_O = 0;        // TMEM columns: O [0, D), S0 [D, D+N), S1 [D+N, D+2N)
+  static constexpr int TM_S = D;
+  static constexpr uint32_t TM_COLS = 512;
+  static constexpr uint32_t IDESC_QK = idesc_bf16(128, N, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
+  static_assert(D + 2 * N <= 512, "TMEM budget");
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+struct Ctrl {
+  uint64_t q_full;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_full, drain;
+  uint32_t tmem_base;
+  int abort;
+  int kmin, kmax;
+};
+
+template <class C>
+__global__ void __launch_bounds__(192, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const int G) {
+  extern __shared__ uint8_t dsm_raw[];
+  __shared__ Ctrl ctl;
+  const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
+  uint8_t *dsm_ptr = dsm_raw + (dsm - smem_u32(dsm_raw));
+  const uint32_t q_s = dsm;
+  const uint32_t k_s = dsm + C::OFF_K;
+  const uint32_t v_s = dsm + C::OFF_V;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bq = C::M / G;
+  const int hk = blockIdx.y;
+
+  // ---- which sequence / query block (uniform over the CTA) ----
+  const int s = find_seq(a.qsl, a.num_seqs, blockIdx.x, bq);
+  const int64_t first_blk = (int64_t)__ldg(a.qsl + s) / bq + s;
+  const int local = (int)(blockIdx.x - first_blk);
+  const int qstart = __ldg(a.qsl + s);
+  const int qlen = __ldg(a.qsl + s + 1) - qstart;
+  const int qpos_lo = local * bq;
+  if (local < 0 || qpos_lo >= qlen) return;
+  if (qstart < 0 || (int64_t)qstart + qlen > a.num_tokens) {
+    if (threadIdx.x == 0) report(a.err, SWA_ERR_QSL);
+    return;
+  }
+  const int seq_len = __ldg(a.seq_lens + s);
+  const int ctx = seq_len - qlen;
+  if (ctx < 0 || (a.ctx_lens != nullptr && __ldg(a.ctx_lens + s) != ctx)) {
+    if (threadIdx.x == 0) report(a.err, SWA_ERR_LENS);
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    ctl.abort = 0;
+    ctl.kmin = INT_MAX;
+    ctl.kmax = -1;
+    mbar_init(smem_u32(&ctl.q_full), 1);
+    for (int i = 0; i < C::ST; ++i) {
+      mbar_init(smem_u32(&ctl.k_full[i]), 1);
+      mbar_init(smem_u32(&ctl.k_empty[i]), 1);
+      mbar_init(smem_u32(&ctl.v_full[i]), 1);
+      mbar_init(smem_u32(&ctl.v_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&ctl.s_full[i]), 1);
+      mbar_init(smem_u32(&ctl.p_full[i]), 128);
+    }
+    mbar_init(smem_u32(&ctl.o_full), 1);
+    mbar_init(smem_u32(&ctl.drain), 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  // ---- each softmax thread: its row's visible interval; the CTA's union ----
+  const bool is_softmax = warp >= 2;
+  const int row = 32 * (warp & 3) + lane;            // TMEM lane of this thread
+  int klo = 1, khi = 0;
+  bool row_valid = false;
+  int64_t out_row = 0;
+  if (is_softmax) {
+    const int qpos = qpos_lo + row / G;
+    row_valid = qpos < qlen;
+    if (row_valid) {
+      const int32_t *ranges = a.mm_ranges ? a.mm_ranges + (int64_t)s * a.max_mm_ranges * 2 : nullptr;
+      const Span sp = visible_span(ctx + qpos, seq_len, a.window, a.causal != 0, ranges,
+                                   a.mm_ranges ? a.max_mm_ranges : 0);
+      klo = sp.lo;
+      khi = sp.hi;
+      out_row = (int64_t)(qstart + qpos) * a.hq + hk * G + row % G;
+      if (klo <= khi) {
+        atomicMin(&ctl.kmin, klo);
+        atomicMax(&ctl.kmax, khi);
+      }
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl.tmem_base), C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  const int kmin = ctl.kmin, kmax = ctl.kmax;
+  const int tile_lo = kmax >= kmin ? kmin / C::N : 0;
+  const int n_tiles = kmax >= kmin ? kmax / C::N - tile_lo + 1 : 0;
+  volatile int *abort_flag = &ctl.abort;
+  const volatile int32_t *gerr = a.err;
+
+  if (warp == 0) {
+    // =============================== TMA producer ===============================
+    if (lane == 0 && n_tiles > 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      const uint32_t bq_full = smem_u32(&ctl.q_full);
+      mbar_expect_tx(bq_full, C::Q_BYTES);
+      for (int c = 0; c < C::CH; ++c)
+        tma_load_3d(q_s + c * C::Q_CHUNK, &tm_q, c * 64, hk * G, qstart + qpos_lo, bq_full);
+
+      const int R = min(a.block_size, C::N);             // rows per box (one page or part of one)
+      const int oob = (int)(a.num_blocks * a.block_size); // first slot outside the cache
+      const int32_t *bt = a.block_table + (int64_t)s * a.bt_stride;
+      int issued = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j % C::ST;
+        const uint32_t ph = (j / C::ST) & 1;
+        const int kt0 = (tile_lo + j) * C::N;
+        if (!mbar_wait(smem_u32(&ctl.k_empty[st]), ph ^ 1, abort_flag, gerr, kWaitLimitNs)) break;
+        mbar_expect_tx(smem_u32(&ctl.k_full[st]), C::KV_BYTES);
+        int slots[C::N / 16];
+        for (int i = 0; i < C::N / R; ++i) {
+          const int k = kt0 + i * R;
+          int slot = oob;
+          if (k < seq_len) {
+            const int page = k / a.block_size;
+            const int32_t blk = page < a.bt_stride ? __ldg(bt + page) : -1;
+            if (blk >= 0 && blk < a.num_blocks) slot = blk * a.block_size + (k - page * a.block_size);
+            else report(a.err, SWA_ERR_BLOCK_ID);
+          }
+          slots[i] = slot;
+          for (int c = 0; c < C::CH; ++c)
+            tma_load_3d(k_s + st * C::KV_BYTES + c * C::KV_CHUNK + i * R * 128, &tm_k, c * 64, hk, slot,
+                        smem_u32(&ctl.k_full[st]));
+        }
+        if (!mbar_wait(smem_u32(&ctl.v_empty[st]), ph ^ 1, abort_flag, gerr, kWaitLimitNs)) {
+          issued = j * 2 + 1;
+          break;
+        }
+        mbar_expect_tx(smem_u32(&ctl.v_full[st]), C::KV_BYTES);
+        for (int i = 0; i < C::N / R; ++i)
+          for (int c = 0; c < C::CH; ++c)
+            tma_load_3d(v_s + st * C::KV_BYTES + c * C::KV_CHUNK + i * R * 128, &tm_v, c * 64, hk, slots[i],
+                        smem_u32(&ctl.v_full[st]));
+        issued = j * 2 + 2;
+      }
+      if (issued < 2 * n_tiles) {
+        *abort_flag = 1;
+        report(a.err, SWA_ERR_TIMEOUT);
+      }
+      // drain: every load this thread issued must have landed before the CTA exits
+      for (int t = (issued > 2 * C::ST ? issued - 2 * C::ST : 0); t < issued; ++t) {
+        const int j = t / 2, st = j % C::ST;
+        const uint32_t ph = (j / C::ST) & 1;
+        const uint32_t bar = smem_u32((t & 1) ? &ctl.v_full[st] : &ctl.k_full[st]);
+        mbar_wait(bar, ph, nullptr, nullptr, kWaitLimitNs);
+      }
+      mbar_wait(bq_full, 0, nullptr, nullptr, kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    // =============================== MMA issuer =================================
+    if (lane == 0 && n_tiles > 0) {
+      bool ok = mbar_wait(smem_u32(&ctl.q_full), 0, abort_flag, gerr, kWaitLimitNs);
+      tc_fence_after();
+      auto issue_qk = [&](int j) -> bool {
+        const int st = j % C::ST;
+        if (!mbar_wait(smem_u32(&ctl.k_full[st]), (j / C::ST) & 1, abort_flag, gerr, kWaitLimitNs)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + C::TM_S + (j & 1) * C::N;
+#pragma unroll
+        for (int kk = 0; kk < C::D / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;     // 16-column step inside the 128-byte swizzle row
+          const uint64_t ad = smem_desc_sw128(q_s + (kk >> 2) * C::Q_CHUNK + off, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(k_s + st * C::KV_BYTES + (kk >> 2) * C::KV_CHUNK + off, 16, 1024);
+          mma_ss(d, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&ctl.s_full[j & 1]));
+        mma_commit(smem_u32(&ctl.k_empty[st]));
+        return true;
+      };
+      if (ok) ok = issue_qk(0);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j + 1 < n_tiles && !issue_qk(j + 1)) { ok = false; break; }
+        const int st = j % C::ST;
+        if (!mbar_wait(smem_u32(&ctl.p_full[j & 1]), (j >> 1) & 1, abort_flag, gerr, kWaitLimitNs) ||
+            !mbar_wait(smem_u32(&ctl.v_full[st]), (j / C::ST) & 1, abort_flag, gerr, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t p_t = tmem + C::TM_S + (j & 1) * C::N;
+#pragma unroll
+        for (int kk = 0; kk < C::N / 16; ++kk) {
+          const uint64_t bd = smem_desc_sw128(v_s + st * C::KV_BYTES + kk * 16 * 128, C::KV_CHUNK, 1024);
+          mma_ts(tmem + C::TM_O, p_t + kk * 8, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&ctl.v_empty[st]));
+        mma_commit(smem_u32(&ctl.o_full));
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        report(a.err, SWA_ERR_TIMEOUT);
+      }
+      // every MMA issued so far must finish before TMEM is released
+      mma_commit(smem_u32(&ctl.drain));
+      mbar_wait(smem_u32(&ctl.drain), 0, nullptr, nullptr, kWaitLimitNs);
+    }
+  } else {
+    // =============================== softmax ====================================
+    const uint32_t lane_t = (uint32_t)(32 * (warp & 3)) << 16;
+    const float sl2 = a.scale * kLog2e;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int kt0 = (tile_lo + j) * C::N;
+      ok = mbar_wait(smem_u32(&ctl.s_full[j & 1]), (j >> 1) & 1, abort_flag, gerr, kWaitLimitNs);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t raw[C::N];
+#pragma unroll
+      for (int c = 0; c < C::N / 32; ++c)
+        tmem_ld32(tmem + lane_t + C::TM_S + (j & 1) * C::N + 32 * c,
+                  *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
+      tmem_wait_ld();
+      float x[C::N];
+#pragma unroll
+      for (int c = 0; c < C::N; ++c) x[c] = __uint_as_float(raw[c]);
+      const bool full = klo <= kt0 && khi >= kt0 + C::N - 1;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < C::N; ++c) {
+        const bool vis = full || (kt0 + c >= klo && kt0 + c <= khi);
+        x[c] = vis ? x[c] * sl2 : -INFINITY;
+        mx = fmaxf(mx, x[c]);
+      }
+      const float m_new = fmaxf(m_used, mx);
+      const bool need = m_new > m_used + 8.f;             // also true on the first visible tile
+      // PV_{j-1} is confirmed exactly once per tile (here if O must be
+      // rescaled, else before P_j is published), so this thread is never more
+      // than one o_full phase behind and every parity wait is unambiguous.
+      bool pv_prev_done = (j == 0);
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_next = need ? m_new : m_used;
+        const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_next);
+        if (j > 0) {
+          ok = mbar_wait(smem_u32(&ctl.o_full), (j - 1) & 1, abort_flag, gerr, kWaitLimitNs);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          pv_prev_done = true;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < C::D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_t + C::TM_O + 32 * c, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(tmem + lane_t + C::TM_O + 32 * c, r);
+          }
+          tmem_wait_st();
+        }
+        l *= alpha;
+        m_used = m_next;
+      }
+      const float ms = (m_used == -INFINITY) ? 0.f : m_used;
+      uint32_t pk[C::N / 2];
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < C::N / 2; ++c) {
+        const float p0 = ex2(x[2 * c] - ms), p1 = ex2(x[2 * c + 1] - ms);
+        sum += p0 + p1;
+        pk[c] = pack_bf16(p0, p1);
+      }
+      l += sum;
+      if (kt0 + C::N > seq_len) {
+        // keys past the sequence end: their V rows may hold anything; zero them
+        const int st = j % C::ST;
+        ok = mbar_wait(smem_u32(&ctl.v_full[st]), (j / C::ST) & 1, abort_flag, gerr, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const int r0 = max(0, seq_len - kt0);
+        const int n16 = (C::N - r0) * 8 * C::CH;
+        for (int i = threadIdx.x - 64; i < n16; i += 128) {
+          const int c = i / ((C::N - r0) * 8), rem = i % ((C::N - r0) * 8);
+          uint4 *dst = reinterpret_cast<uint4 *>(dsm_ptr + C::OFF_V + st * C::KV_BYTES + c * C::KV_CHUNK +
+                                                 (r0 + rem / 8) * 128 + (rem % 8) * 16);
+          *dst = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      if (!pv_prev_done) {
+        ok = mbar_wait(smem_u32(&ctl.o_full), (j - 1) & 1, abort_flag, gerr, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      }
+#pragma unroll
+      for (int c = 0; c < C::N / 64; ++c) {
+        uint32_t r[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) r[e] = pk[32 * c + e];
+        tmem_st32(tmem + lane_t + C::TM_S + (j & 1) * C::N + 32 * c, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&ctl.p_full[j & 1]));
+    }
+    if (ok && n_tiles > 0) {
+      ok = mbar_wait(smem_u32(&ctl.o_full), (n_tiles - 1) & 1, abort_flag, gerr, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      report(a.err, SWA_ERR_TIMEOUT);
+    } else {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + out_row * C::D;
+#pragma unroll 1
+      for (int c = 0; c < C::D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_t + C::TM_O + 32 * c, r);
+        tmem_wait_ld();
+        if (row_valid) {
+          uint4 v[4];
+          uint32_t *w = reinterpret_cast<uint32_t *>(v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+          uint4 *dst = reinterpret_cast<uint4 *>(o + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = v[e];
+        }
+      }
+      if (row_valid && a.lse != nullptr)
+        a.lse[out_row] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+  static EncodeTiled fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiled>(nullptr);
+    return reinterpret_cast<EncodeTiled>(p);
+  }();
+  return fn;
+}
+
+bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+              uint32_t b0, uint32_t b1, uint32_t b2) {
+  EncodeTiled enc = encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <class C>
+cudaError_t run(const AttnArgs &a, cudaStream_t st) {
+  const int G = a.hq / a.hkv;
+  const int bq = C::M / G;
+  const int R = a.block_size < C::N ? a.block_size : C::N;
+  CUtensorMap mq, mk, mv;
+  const uint64_t esz = 2;
+  if (!make_map(&mq, a.q, C::D, a.hq, a.num_tokens, C::D * esz, (uint64_t)a.hq * C::D * esz, 64, G, bq) ||
+      !make_map(&mk, a.k_cache, C::D, a.hkv, (uint64_t)a.num_blocks * a.block_size, C::D * esz,
+                (uint64_t)a.hkv * C::D * esz, 64, 1, R) ||
+      !make_map(&mv, a.v_cache, C::D, a.hkv, (uint64_t)a.num_blocks * a.block_size, C::D * esz,
+                (uint64_t)a.hkv * C::D * esz, 64, 1, R))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int64_t blocks = a.num_tokens / bq + a.num_seqs;
+  dim3 grid((unsigned)blocks, (unsigned)a.hkv);
+  attn_tc_kernel<C><<<grid, 192, C::SMEM, st>>>(mq, mk, mv, a, G);
+  return cudaGetLastError();
+}
+
+using Cfg256 = Cfg<256, 64, 2>;
+using Cfg128 = Cfg<128, 128, 2>;
+
+}  // namespace
+
+bool tc_supported(const AttnArgs &a) {
+  const int G = a.hq / a.hkv;
+  return a.dtype == SWA_DTYPE_BF16 && (a.head_dim == 128 || a.head_dim == 256) && a.num_splits == 1 &&
+         (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) && a.max_query_len > 1 &&
+         a.num_blocks * a.block_size < (int64_t)INT32_MAX && a.num_tokens < (int64_t)INT32_MAX &&
+         encoder() != nullptr;
+}
+
+cudaError_t launch_attention_tc(const AttnArgs &a, cudaStream_t st) {
+  return a.head_dim == 256 ? run<Cfg256>(a, st) : run<Cfg128>(a, st);
+}
 
 }  // namespace swa

@@ -38,15 +38,20 @@ __device__ inline bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete.  Gives up after
-// `limit_ns` or as soon as *abort is set by another warp; returns false then.
-__device__ inline bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, uint64_t limit_ns) {
+// Wait for the phase with the given parity to complete.  Gives up (returns
+// false) after `limit_ns`, or early when the CTA-local flag *abort is set or
+// the launch-wide error word already carries SWA_ERR_TIMEOUT (so one stalled
+// CTA makes the others quit quickly).  Either pointer may be null: drain
+// waits pass nulls so they only stop at the time limit.
+__device__ inline bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int *abort,
+                                 const volatile int32_t *err, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
-      if (*abort) return false;
+      if (abort != nullptr && *abort) return false;
+      if (err != nullptr && (*err & SWA_ERR_TIMEOUT)) return false;
       if (global_ns() - t0 > limit_ns) return false;
     }
   }

@@ -170,3 +170,16 @@ def test_decode_split_kv_sampled(err):
     assert e_out <= 2e-2 and e_lse <= LSE_ATOL
     torch.cuda.synchronize()
     assert err.item() == 0
+
+
+def test_repeated_calls_are_bit_identical(err):
+    """No atomics in the arithmetic: any run-to-run difference is a race."""
+    lay = W.gemma_like()
+    q, k, v, d = gpu_inputs(lay)
+    ref, ref_lse = run_attention(lay, q, k, v, d, err=err)
+    ref, ref_lse = ref.clone(), ref_lse.clone()
+    for _ in range(4):
+        out, lse = run_attention(lay, q, k, v, d, err=err)
+        assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
+    torch.cuda.synchronize()
+    assert err.item() == 0
