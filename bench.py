@@ -172,7 +172,7 @@ class PrefillStep:
 def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    lay = W.gemma_like()
+    lay = W.gemma_like(num_requests=args.requests)
     step = PrefillStep(lay, dev)
     pairs = visible_pairs_per_head(lay)
     flops = 4.0 * lay.head_dim * lay.num_heads_q * pairs
@@ -217,6 +217,15 @@ def run_gpu(args, rank, world, local_rank):
 
     # end to end through the public API: pinned host inputs -> device -> three
     # calls -> host, every step inside the timed region
+    e2e = run_e2e(args, step, flops, barrier, stream, world, dev) if not args.no_e2e else None
+    torch.cuda.synchronize(dev)
+    err = int(step.err.item())
+    if rank != 0:
+        return None
+    return report_line(args, lay, step, flops, pairs, ms_per_step, attn_ms, feed_ms, clk, e2e, err, world)
+
+
+def run_e2e(args, step, flops, barrier, stream, world, dev):
     host = {"q": step.q.cpu().pin_memory(), "k": step.k.cpu().pin_memory(), "v": step.v.cpu().pin_memory()}
     for key, t in step.d.items():
         if t is not None:
@@ -252,12 +261,11 @@ def run_gpu(args, rank, world, local_rank):
         t = torch.tensor([e2e_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(t.item())
+    return {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+            "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
-    torch.cuda.synchronize(dev)
-    err = int(step.err.item())
-    if rank != 0:
-        return None
 
+def report_line(args, lay, step, flops, pairs, ms_per_step, attn_ms, feed_ms, clk, e2e, err, world):
     pk = peaks()
     attn_avg = statistics.mean(attn_ms)
     achieved = flops / (attn_avg * 1e-3) / 1e12
@@ -277,9 +285,10 @@ def run_gpu(args, rank, world, local_rank):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": "gemma_like: 4 requests (16550/16294/16806/16550 tokens), 60 images x 256 "
+            "workload": f"{lay.name}: {lay.num_seqs} request(s) of "
+                        f"{'/'.join(str(int(x)) for x in lay.seq_lens)} tokens, 60 images x 256 "
                         "tokens each, causal SWA W=1024 with the window-clamped image mask, Hq=16, "
-                        "Hkv=8, D=256, bf16, paged KV block 16, slot mapping padded to 73728",
+                        f"Hkv=8, D=256, bf16, paged KV block 16, slot mapping padded to {lay.max_num_tokens}",
             "global_batch": lay.num_seqs * world,
             "seq_len": int(lay.seq_lens.mean()),
             "tokens_per_step": lay.num_tokens,
@@ -303,8 +312,7 @@ def run_gpu(args, rank, world, local_rank):
             "avg_launch_ms": round(attn_avg, 4),
         },
         "feeders_ms": round(statistics.mean(feed_ms), 4),
-        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
-                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "gpu_launches": args.steps * step.launches_per_step(),
         "clocks": clk,
         "device_errors": err,
@@ -393,6 +401,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--requests", type=int, default=4, choices=[1, 2, 3, 4],
+                    help="Gemma-like requests per step (4 = the benchmark; fewer = profiling case)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

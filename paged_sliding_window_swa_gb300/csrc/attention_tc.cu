@@ -38,11 +38,12 @@ using namespace tc;
 
 constexpr uint64_t kWaitLimitNs = 200000000ull;    // 200 ms per wait: far above any real stall
 
-template <int D_, int N_, int ST_>
+template <int D_, int N_, int KST_, int VST_>
 struct Cfg {
   static constexpr int D = D_;          // head dim
   static constexpr int N = N_;          // keys per K/V tile
-  static constexpr int ST = ST_;        // K/V ring depth
+  static constexpr int KST = KST_;      // K ring depth
+  static constexpr int VST = VST_;      // V ring depth
   static constexpr int M = 128;         // query rows per CTA
   static constexpr int CH = D / 64;     // 128-byte column chunks per row
   static constexpr int Q_CHUNK = M * 128;
@@ -50,14 +51,16 @@ struct Cfg {
   static constexpr int KV_CHUNK = N * 128;
   static constexpr int KV_BYTES = N * D * 2;
   static constexpr int OFF_K = Q_BYTES;
-  static constexpr int OFF_V = OFF_K + ST * KV_BYTES;
-  static constexpr int SMEM = OFF_V + ST * KV_BYTES + 1024;      // + alignment slack
+  static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
+  static constexpr int SMEM = OFF_V + VST * KV_BYTES + 1024;     // + alignment slack
   static constexpr int TM_O = 0;        // TMEM columns: O [0, D), S0 [D, D+N), S1 [D+N, D+2N)
   static constexpr int TM_S = D;
   static constexpr uint32_t TM_COLS = 512;
   static constexpr uint32_t IDESC_QK = idesc_bf16(128, N, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
   static_assert(D + 2 * N <= 512, "TMEM budget");
+  static_assert(KST <= 4 && VST <= 4 && VST <= KST, "ring depths");
+  static_assert((KST - VST + 1) * (N / 16) <= 32, "V lag must stay inside the previous slot batch");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
@@ -111,9 +114,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     ctl.kmin = INT_MAX;
     ctl.kmax = -1;
     mbar_init(smem_u32(&ctl.q_full), 1);
-    for (int i = 0; i < C::ST; ++i) {
+    for (int i = 0; i < C::KST; ++i) {
       mbar_init(smem_u32(&ctl.k_full[i]), 1);
       mbar_init(smem_u32(&ctl.k_empty[i]), 1);
+    }
+    for (int i = 0; i < C::VST; ++i) {
       mbar_init(smem_u32(&ctl.v_full[i]), 1);
       mbar_init(smem_u32(&ctl.v_empty[i]), 1);
     }
@@ -165,63 +170,95 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   if (warp == 0) {
     // =============================== TMA producer ===============================
-    if (lane == 0 && n_tiles > 0) {
-      tma_prefetch_map(&tm_q);
-      tma_prefetch_map(&tm_k);
-      tma_prefetch_map(&tm_v);
-      const uint32_t bq_full = smem_u32(&ctl.q_full);
-      mbar_expect_tx(bq_full, C::Q_BYTES);
-      for (int c = 0; c < C::CH; ++c)
-        tma_load_3d(q_s + c * C::Q_CHUNK, &tm_q, c * 64, hk * G, qstart + qpos_lo, bq_full);
-
-      const int R = min(a.block_size, C::N);             // rows per box (one page or part of one)
-      const int oob = (int)(a.num_blocks * a.block_size); // first slot outside the cache
-      const int32_t *bt = a.block_table + (int64_t)s * a.bt_stride;
-      int issued = 0;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % C::ST;
-        const uint32_t ph = (j / C::ST) & 1;
-        const int kt0 = (tile_lo + j) * C::N;
-        if (!mbar_wait(smem_u32(&ctl.k_empty[st]), ph ^ 1, abort_flag, gerr, kWaitLimitNs)) break;
-        mbar_expect_tx(smem_u32(&ctl.k_full[st]), C::KV_BYTES);
-        int slots[C::N / 16];
-        for (int i = 0; i < C::N / R; ++i) {
-          const int k = kt0 + i * R;
-          int slot = oob;
-          if (k < seq_len) {
-            const int page = k / a.block_size;
-            const int32_t blk = page < a.bt_stride ? __ldg(bt + page) : -1;
-            if (blk >= 0 && blk < a.num_blocks) slot = blk * a.block_size + (k - page * a.block_size);
-            else report(a.err, SWA_ERR_BLOCK_ID);
-          }
-          slots[i] = slot;
-          for (int c = 0; c < C::CH; ++c)
-            tma_load_3d(k_s + st * C::KV_BYTES + c * C::KV_CHUNK + i * R * 128, &tm_k, c * 64, hk, slot,
-                        smem_u32(&ctl.k_full[st]));
-        }
-        if (!mbar_wait(smem_u32(&ctl.v_empty[st]), ph ^ 1, abort_flag, gerr, kWaitLimitNs)) {
-          issued = j * 2 + 1;
-          break;
-        }
-        mbar_expect_tx(smem_u32(&ctl.v_full[st]), C::KV_BYTES);
-        for (int i = 0; i < C::N / R; ++i)
-          for (int c = 0; c < C::CH; ++c)
-            tma_load_3d(v_s + st * C::KV_BYTES + c * C::KV_CHUNK + i * R * 128, &tm_v, c * 64, hk, slots[i],
-                        smem_u32(&ctl.v_full[st]));
-        issued = j * 2 + 2;
+    // The whole warp runs this loop: each lane resolves the cache slot of one
+    // box (one page, or part of one) through the block table, 32 boxes per
+    // batch and one batch ahead, and lane 0 issues the copies with the slots
+    // fetched by shuffle -- no block-table load sits on the issue path.
+    if (n_tiles > 0) {
+      if (lane == 0) {
+        tma_prefetch_map(&tm_q);
+        tma_prefetch_map(&tm_k);
+        tma_prefetch_map(&tm_v);
+        mbar_expect_tx(smem_u32(&ctl.q_full), C::Q_BYTES);
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_3d(q_s + c * C::Q_CHUNK, &tm_q, c * 64, hk * G, qstart + qpos_lo, smem_u32(&ctl.q_full));
       }
-      if (issued < 2 * n_tiles) {
+      const int R = min(a.block_size, C::N);             // rows per box
+      const int boxes = C::N / R;                         // boxes per tile
+      const int total_boxes = n_tiles * boxes;
+      const int oob = (int)(a.num_blocks * a.block_size); // first slot outside the cache: zero fill
+      const int32_t *bt = a.block_table + (int64_t)s * a.bt_stride;
+      auto resolve = [&](int b) -> int {
+        const int k = tile_lo * C::N + b * R;
+        int slot = oob;
+        if (b < total_boxes && k < seq_len) {
+          const int page = k / a.block_size;
+          const int32_t blk = page < a.bt_stride ? __ldg(bt + page) : -1;
+          if (blk >= 0 && blk < a.num_blocks) slot = blk * a.block_size + (k - page * a.block_size);
+          else report(a.err, SWA_ERR_BLOCK_ID);
+        }
+        return slot;
+      };
+      // V tiles trail K tiles by at most KST - VST + 1 tiles (< 32 boxes), so
+      // the batch before the current one is all a lagging request can need.
+      int batch = 0;
+      int prv = oob, cur = resolve(lane), nxt = resolve(32 + lane);
+      auto slot_of = [&](int b) -> int {                  // warp-uniform b
+        while (b >= (batch + 1) * 32) {
+          prv = cur;
+          cur = nxt;
+          ++batch;
+          nxt = resolve((batch + 1) * 32 + lane);
+        }
+        if (b >= batch * 32) return __shfl_sync(0xffffffffu, cur, b - batch * 32);
+        return __shfl_sync(0xffffffffu, prv, b - (batch - 1) * 32);
+      };
+      auto issue = [&](int t, bool is_v) {
+        const int st = is_v ? t % C::VST : t % C::KST;
+        const uint32_t full = smem_u32(is_v ? &ctl.v_full[st] : &ctl.k_full[st]);
+        const uint32_t dst = (is_v ? v_s : k_s) + st * C::KV_BYTES;
+        if (lane == 0) mbar_expect_tx(full, C::KV_BYTES);
+        for (int i = 0; i < boxes; ++i) {
+          const int slot = slot_of(t * boxes + i);
+          if (lane == 0)
+            for (int c = 0; c < C::CH; ++c)
+              tma_load_3d(dst + c * C::KV_CHUNK + i * R * 128, is_v ? &tm_v : &tm_k, c * 64, hk, slot, full);
+        }
+      };
+      // fill both rings, then refill each stage as soon as its consumer frees it:
+      // K tile t+KST after QK_t, V tile t+VST after PV_t (the order those happen in)
+      int k_issued = min(C::KST, n_tiles), v_issued = min(C::VST, n_tiles);
+      for (int t = 0; t < n_tiles && (t < C::KST || t < C::VST); ++t) {
+        if (t < C::KST) issue(t, false);
+        if (t < C::VST) issue(t, true);
+      }
+      bool ok = true;
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j + C::KST < n_tiles) {
+          ok = mbar_wait(smem_u32(&ctl.k_empty[j % C::KST]), (j / C::KST) & 1, abort_flag, gerr, kWaitLimitNs);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          issue(j + C::KST, false);
+          k_issued = j + C::KST + 1;
+        }
+        if (j + C::VST < n_tiles) {
+          ok = mbar_wait(smem_u32(&ctl.v_empty[j % C::VST]), (j / C::VST) & 1, abort_flag, gerr, kWaitLimitNs);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          issue(j + C::VST, true);
+          v_issued = j + C::VST + 1;
+        }
+      }
+      if (!ok && lane == 0) {
         *abort_flag = 1;
         report(a.err, SWA_ERR_TIMEOUT);
       }
-      // drain: every load this thread issued must have landed before the CTA exits
-      for (int t = (issued > 2 * C::ST ? issued - 2 * C::ST : 0); t < issued; ++t) {
-        const int j = t / 2, st = j % C::ST;
-        const uint32_t ph = (j / C::ST) & 1;
-        const uint32_t bar = smem_u32((t & 1) ? &ctl.v_full[st] : &ctl.k_full[st]);
-        mbar_wait(bar, ph, nullptr, nullptr, kWaitLimitNs);
+      // drain: every load issued here must have landed before the CTA exits
+      if (lane == 0) {
+        for (int t = max(0, k_issued - C::KST); t < k_issued; ++t)
+          mbar_wait(smem_u32(&ctl.k_full[t % C::KST]), (t / C::KST) & 1, nullptr, nullptr, kWaitLimitNs);
+        for (int t = max(0, v_issued - C::VST); t < v_issued; ++t)
+          mbar_wait(smem_u32(&ctl.v_full[t % C::VST]), (t / C::VST) & 1, nullptr, nullptr, kWaitLimitNs);
+        mbar_wait(smem_u32(&ctl.q_full), 0, nullptr, nullptr, kWaitLimitNs);
       }
-      mbar_wait(bq_full, 0, nullptr, nullptr, kWaitLimitNs);
     }
   } else if (warp == 1) {
     // =============================== MMA issuer =================================
@@ -229,8 +266,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       bool ok = mbar_wait(smem_u32(&ctl.q_full), 0, abort_flag, gerr, kWaitLimitNs);
       tc_fence_after();
       auto issue_qk = [&](int j) -> bool {
-        const int st = j % C::ST;
-        if (!mbar_wait(smem_u32(&ctl.k_full[st]), (j / C::ST) & 1, abort_flag, gerr, kWaitLimitNs)) return false;
+        const int st = j % C::KST;
+        if (!mbar_wait(smem_u32(&ctl.k_full[st]), (j / C::KST) & 1, abort_flag, gerr, kWaitLimitNs)) return false;
         tc_fence_after();
         const uint32_t d = tmem + C::TM_S + (j & 1) * C::N;
 #pragma unroll
@@ -247,9 +284,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       if (ok) ok = issue_qk(0);
       for (int j = 0; ok && j < n_tiles; ++j) {
         if (j + 1 < n_tiles && !issue_qk(j + 1)) { ok = false; break; }
-        const int st = j % C::ST;
+        const int st = j % C::VST;
         if (!mbar_wait(smem_u32(&ctl.p_full[j & 1]), (j >> 1) & 1, abort_flag, gerr, kWaitLimitNs) ||
-            !mbar_wait(smem_u32(&ctl.v_full[st]), (j / C::ST) & 1, abort_flag, gerr, kWaitLimitNs)) {
+            !mbar_wait(smem_u32(&ctl.v_full[st]), (j / C::VST) & 1, abort_flag, gerr, kWaitLimitNs)) {
           ok = false;
           break;
         }
@@ -339,8 +376,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       l += sum;
       if (kt0 + C::N > seq_len) {
         // keys past the sequence end: their V rows may hold anything; zero them
-        const int st = j % C::ST;
-        ok = mbar_wait(smem_u32(&ctl.v_full[st]), (j / C::ST) & 1, abort_flag, gerr, kWaitLimitNs);
+        const int st = j % C::VST;
+        ok = mbar_wait(smem_u32(&ctl.v_full[st]), (j / C::VST) & 1, abort_flag, gerr, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         const int r0 = max(0, seq_len - kt0);
         const int n16 = (C::N - r0) * 8 * C::CH;
@@ -460,8 +497,8 @@ cudaError_t run(const AttnArgs &a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-using Cfg256 = Cfg<256, 64, 2>;
-using Cfg128 = Cfg<128, 128, 2>;
+using Cfg256 = Cfg<256, 64, 3, 2>;     // 64 KB Q + 3 x 32 KB K + 2 x 32 KB V
+using Cfg128 = Cfg<128, 128, 3, 3>;    // 32 KB Q + 3 x 32 KB K + 3 x 32 KB V
 
 }  // namespace
 

@@ -43,18 +43,24 @@ __device__ inline bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // the launch-wide error word already carries SWA_ERR_TIMEOUT (so one stalled
 // CTA makes the others quit quickly).  Either pointer may be null: drain
 // waits pass nulls so they only stop at the time limit.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const volatile int *abort,
+                                            const volatile int32_t *err, uint64_t limit_ns) {
+  uint64_t t0 = 0;     // the clock is read only once a wait has really stalled
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (err != nullptr && (*err & SWA_ERR_TIMEOUT)) return false;
+      const uint64_t now = global_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > limit_ns) return false;
+    }
+  }
+}
 __device__ inline bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int *abort,
                                  const volatile int32_t *err, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (abort != nullptr && *abort) return false;
-      if (err != nullptr && (*err & SWA_ERR_TIMEOUT)) return false;
-      if (global_ns() - t0 > limit_ns) return false;
-    }
-  }
+  return mbar_wait_slow(bar, parity, abort, err, limit_ns);
 }
 
 // ---------------------------------------------------------------- TMA

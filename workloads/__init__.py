@@ -186,16 +186,17 @@ def geometry(variant: str = "causal", structure_seed: int = 0) -> Layout:
                   notes={"tile_size": 32, "block_q": 8})
 
 
-def gemma_like(structure_seed: int = 0) -> Layout:
+def gemma_like(structure_seed: int = 0, num_requests: int = 4) -> Layout:
     """4 requests (16550, 16294, 16806, 16550 tokens), 60 images of 256 tokens each.
 
     Text spans between images are a seeded random composition of the remaining
     text tokens into 61 gaps of at least one token.  Causal, W=1024, 16 q heads
     / 8 kv heads, D=256, bf16, block size 16; slot mapping pads to a multiple of
-    8192 tokens.
+    8192 tokens.  ``num_requests < 4`` keeps the first requests only (a smaller
+    case of the same structure, for profiling).
     """
     rng = np.random.default_rng(structure_seed)
-    lens = np.array([16550, 16294, 16806, 16550], dtype=np.int32)
+    lens = np.array([16550, 16294, 16806, 16550], dtype=np.int32)[:num_requests]
     n_img, img = 60, 256
     per_seq = []
     for n in lens:
@@ -210,7 +211,8 @@ def gemma_like(structure_seed: int = 0) -> Layout:
         per_seq.append(ranges)
     bt, nb = _block_table(rng, lens, 16)
     t = int(lens.sum())
-    return Layout("gemma_like", query_lens=lens.copy(), seq_lens=lens, mm_ranges=_pad_ranges(per_seq),
+    name = "gemma_like" if num_requests == 4 else f"gemma_like_{num_requests}req"
+    return Layout(name, query_lens=lens.copy(), seq_lens=lens, mm_ranges=_pad_ranges(per_seq),
                   block_table=bt, num_blocks=nb, num_heads_q=16, num_heads_kv=8, head_dim=256,
                   block_size=16, window=1024, causal=True, dtype="bf16",
                   max_num_tokens=-(-t // 8192) * 8192)
