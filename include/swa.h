@@ -60,6 +60,8 @@ extern "C" {
 #define SWA_ERR_LENS       0x08  /* seq_lens / context_lens inconsistent           */
 #define SWA_ERR_TIMEOUT    0x10  /* a bounded pipeline wait gave up                */
 #define SWA_ERR_SPLITS     0x20  /* splits_per_seq entry outside [1, num_splits]   */
+#define SWA_ERR_INTERNAL   0x40  /* a kernel could not set up its pipeline (its
+                                    outputs are not written)                      */
 
 /* ---- element types ------------------------------------------------------ */
 #define SWA_DTYPE_BF16 0

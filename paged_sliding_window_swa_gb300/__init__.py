@@ -29,7 +29,8 @@ DTYPE_BF16 = 0
 DTYPE_FP32 = 1
 SPLIT_ALIGN = 128
 _RC = {-1: "SWA_E_NULL", -2: "SWA_E_SIZE", -3: "SWA_E_UNSUPPORTED", -4: "SWA_E_ALIGN", -5: "SWA_E_CUDA"}
-ERR_BITS = {0x01: "BLOCK_ID", 0x02: "POSITION", 0x04: "QSL", 0x08: "LENS", 0x10: "TIMEOUT", 0x20: "SPLITS"}
+ERR_BITS = {0x01: "BLOCK_ID", 0x02: "POSITION", 0x04: "QSL", 0x08: "LENS", 0x10: "TIMEOUT", 0x20: "SPLITS",
+            0x40: "INTERNAL"}
 
 _c_i32, _c_i64, _c_f, _c_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 _SIGS = {

@@ -5,7 +5,7 @@
 //
 // One CTA = one 128-row query tile: BQ = 128 / G query positions x the G query
 // heads of one kv head (GQA packing -- every K/V tile is staged once for the
-// whole group).  Six warps:
+// whole group).  Ten warps:
 //   warp 0     TMA producer: the Q tile once, then K and V tiles of N keys,
 //              gathered page by page through the block table into a
 //              STAGES-deep ring (128-byte swizzled, one box per page and
@@ -14,11 +14,12 @@
 //   warp 1     tcgen05 issuer and TMEM owner: S = Q K^T into one of two TMEM S
 //              buffers, then O += P V with P read from TMEM (where the
 //              softmax wrote it over S) and V from shared memory (MN-major).
-//   warps 2-5  softmax: thread i owns row i (TMEM lane i); masks only tiles
+//   warps 2-9  softmax, two warpgroups: thread i of each owns row i (TMEM
+//              lane i) and one half of the tile's columns; masks only tiles
 //              not fully inside its visible interval, keeps a running max in
 //              the log2 domain and rescales O in TMEM only when the max grows
 //              by more than 2^8, writes P as bf16 into TMEM, and finally
-//              normalises O and stores out / lse.
+//              normalises its half of O and stores out / lse.
 // The key loop covers only the union of the rows' visible intervals -- the
 // pruned tile range [lo, hi) of the union formula.  Every mbarrier wait is
 // bounded in time; on expiry the CTA sets SWA_ERR_TIMEOUT, drains its own
@@ -52,7 +53,7 @@ struct Cfg {
   static constexpr int KV_BYTES = N * D * 2;
   static constexpr int OFF_K = Q_BYTES;
   static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
-  static constexpr int SMEM = OFF_V + VST * KV_BYTES + 1024;     // + alignment slack
+  static constexpr int OFF_CTRL = OFF_V + VST * KV_BYTES;         // control block (barriers, exchange)
   static constexpr int TM_O = 0;        // TMEM columns: O [0, D), S0 [D, D+N), S1 [D+N, D+2N)
   static constexpr int TM_S = D;
   static constexpr uint32_t TM_COLS = 512;
@@ -61,27 +62,34 @@ struct Cfg {
   static_assert(D + 2 * N <= 512, "TMEM budget");
   static_assert(KST <= 4 && VST <= 4 && VST <= KST, "ring depths");
   static_assert((KST - VST + 1) * (N / 16) <= 32, "V lag must stay inside the previous slot batch");
-  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert((N / 16) * CH <= 32, "one warp instruction must cover a tile's boxes");
 };
 
 struct Ctrl {
+  float red[2][2][128];                  // half-row max (and, at the end, sum) exchange buffers
   uint64_t q_full;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2];
   uint64_t o_full, drain;
+  uint64_t xch[2], xl;                   // exchange barriers of the two softmax warpgroups
   uint32_t tmem_base;
   int abort;
   int kmin, kmax;
 };
 
 template <class C>
-__global__ void __launch_bounds__(192, 1)
+constexpr int smem_bytes() { return C::OFF_CTRL + (int)sizeof(Ctrl); }
+
+template <class C>
+__global__ void __launch_bounds__(320, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const int G) {
-  extern __shared__ uint8_t dsm_raw[];
-  __shared__ Ctrl ctl;
-  const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
-  uint8_t *dsm_ptr = dsm_raw + (dsm - smem_u32(dsm_raw));
+  // Everything lives in dynamic shared memory, which starts 1024-byte aligned
+  // when a kernel has no static shared data (checked below): the 128-byte
+  // swizzled tiles need that alignment and there is no room for slack.
+  extern __shared__ __align__(1024) uint8_t dsm_ptr[];
+  const uint32_t dsm = smem_u32(dsm_ptr);
+  Ctrl &ctl = *reinterpret_cast<Ctrl *>(dsm_ptr + C::OFF_CTRL);
   const uint32_t q_s = dsm;
   const uint32_t k_s = dsm + C::OFF_K;
   const uint32_t v_s = dsm + C::OFF_V;
@@ -108,6 +116,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (threadIdx.x == 0) report(a.err, SWA_ERR_LENS);
     return;
   }
+  if ((dsm & 1023u) != 0) {
+    if (threadIdx.x == 0) report(a.err, SWA_ERR_INTERNAL);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     ctl.abort = 0;
@@ -124,8 +136,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctl.s_full[i]), 1);
-      mbar_init(smem_u32(&ctl.p_full[i]), 128);
+      mbar_init(smem_u32(&ctl.p_full[i]), 256);
+      mbar_init(smem_u32(&ctl.xch[i]), 256);
     }
+    mbar_init(smem_u32(&ctl.xl), 256);
     mbar_init(smem_u32(&ctl.o_full), 1);
     mbar_init(smem_u32(&ctl.drain), 1);
     mbar_fence_init();
@@ -203,27 +217,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       // the batch before the current one is all a lagging request can need.
       int batch = 0;
       int prv = oob, cur = resolve(lane), nxt = resolve(32 + lane);
-      auto slot_of = [&](int b) -> int {                  // warp-uniform b
-        while (b >= (batch + 1) * 32) {
+      auto advance = [&](int b_max) {                     // warp-uniform
+        while (b_max >= (batch + 1) * 32) {
           prv = cur;
           cur = nxt;
           ++batch;
           nxt = resolve((batch + 1) * 32 + lane);
         }
-        if (b >= batch * 32) return __shfl_sync(0xffffffffu, cur, b - batch * 32);
-        return __shfl_sync(0xffffffffu, prv, b - (batch - 1) * 32);
       };
+      auto slot_lane = [&](int b) -> int {                // per-lane b, inside the current or previous batch
+        const int from_cur = __shfl_sync(0xffffffffu, cur, (b - batch * 32) & 31);
+        const int from_prv = __shfl_sync(0xffffffffu, prv, (b - (batch - 1) * 32) & 31);
+        return b >= batch * 32 ? from_cur : from_prv;
+      };
+      // one warp instruction issues a whole tile: lane i*CH + c copies box i, chunk c
       auto issue = [&](int t, bool is_v) {
         const int st = is_v ? t % C::VST : t % C::KST;
         const uint32_t full = smem_u32(is_v ? &ctl.v_full[st] : &ctl.k_full[st]);
         const uint32_t dst = (is_v ? v_s : k_s) + st * C::KV_BYTES;
         if (lane == 0) mbar_expect_tx(full, C::KV_BYTES);
-        for (int i = 0; i < boxes; ++i) {
-          const int slot = slot_of(t * boxes + i);
-          if (lane == 0)
-            for (int c = 0; c < C::CH; ++c)
-              tma_load_3d(dst + c * C::KV_CHUNK + i * R * 128, is_v ? &tm_v : &tm_k, c * 64, hk, slot, full);
-        }
+        __syncwarp();
+        advance(t * boxes + boxes - 1);
+        const int i = min(lane / C::CH, boxes - 1), c = lane % C::CH;
+        const int slot = slot_lane(t * boxes + i);
+        if (lane < boxes * C::CH)
+          tma_load_3d(dst + c * C::KV_CHUNK + i * R * 128, is_v ? &tm_v : &tm_k, c * 64, hk, slot, full);
       };
       // fill both rings, then refill each stage as soon as its consumer frees it:
       // K tile t+KST after QK_t, V tile t+VST after PV_t (the order those happen in)
@@ -310,39 +328,55 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
   } else {
     // =============================== softmax ====================================
+    // Two warpgroups share every row: warpgroup h owns S columns
+    // [h*N/2, (h+1)*N/2) and O columns [h*D/2, (h+1)*D/2).  Both keep the
+    // same running max (half-row maxima are exchanged through shared memory
+    // once per tile, ordered by a bounded mbarrier) and a partial row sum.
+    constexpr int NH = C::N / 2;
+    constexpr int DH = C::D / 2;
+    const int h = (warp - 2) >> 2;
+    const int sid = threadIdx.x - 64;                    // 0..255 over both warpgroups
     const uint32_t lane_t = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = a.scale * kLog2e;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      const int kt0 = (tile_lo + j) * C::N;
+      const int kc0 = (tile_lo + j) * C::N + h * NH;     // key of this warpgroup's first column
       ok = mbar_wait(smem_u32(&ctl.s_full[j & 1]), (j >> 1) & 1, abort_flag, gerr, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      uint32_t raw[C::N];
+      uint32_t raw[NH];
 #pragma unroll
-      for (int c = 0; c < C::N / 32; ++c)
-        tmem_ld32(tmem + lane_t + C::TM_S + (j & 1) * C::N + 32 * c,
+      for (int c = 0; c < NH / 32; ++c)
+        tmem_ld32(tmem + lane_t + C::TM_S + (j & 1) * C::N + h * NH + 32 * c,
                   *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
       tmem_wait_ld();
-      float x[C::N];
+      float x[NH];
+      const bool full = klo <= kc0 && khi >= kc0 + NH - 1;
+      if (__all_sync(0xffffffffu, full)) {
 #pragma unroll
-      for (int c = 0; c < C::N; ++c) x[c] = __uint_as_float(raw[c]);
-      const bool full = klo <= kt0 && khi >= kt0 + C::N - 1;
-      float mx = -INFINITY;
+        for (int c = 0; c < NH; ++c) x[c] = __uint_as_float(raw[c]) * sl2;
+      } else {
 #pragma unroll
-      for (int c = 0; c < C::N; ++c) {
-        const bool vis = full || (kt0 + c >= klo && kt0 + c <= khi);
-        x[c] = vis ? x[c] * sl2 : -INFINITY;
-        mx = fmaxf(mx, x[c]);
+        for (int c = 0; c < NH; ++c)
+          x[c] = (kc0 + c >= klo && kc0 + c <= khi) ? __uint_as_float(raw[c]) * sl2 : -INFINITY;
       }
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < NH; ++c) m4[c & 3] = fmaxf(m4[c & 3], x[c]);
+      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      ctl.red[j & 1][h][row] = mx;
+      mbar_arrive(smem_u32(&ctl.xch[j & 1]));
+      ok = mbar_wait(smem_u32(&ctl.xch[j & 1]), (j >> 1) & 1, abort_flag, gerr, kWaitLimitNs);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      mx = fmaxf(mx, ctl.red[j & 1][h ^ 1][row]);
       const float m_new = fmaxf(m_used, mx);
       const bool need = m_new > m_used + 8.f;             // also true on the first visible tile
       // PV_{j-1} is confirmed exactly once per tile (here if O must be
       // rescaled, else before P_j is published), so this thread is never more
       // than one o_full phase behind and every parity wait is unambiguous.
       bool pv_prev_done = (j == 0);
-      if (__any_sync(0xffffffffu, need)) {
+      if (__any_sync(0xffffffffu, need)) {               // same decision in both warpgroups
         const float m_next = need ? m_new : m_used;
         const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_next);
         if (j > 0) {
@@ -351,13 +385,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           pv_prev_done = true;
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < C::D / 32; ++c) {
+          for (int c = 0; c < DH / 32; ++c) {
             uint32_t r[32];
-            tmem_ld32(tmem + lane_t + C::TM_O + 32 * c, r);
+            tmem_ld32(tmem + lane_t + C::TM_O + h * DH + 32 * c, r);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(tmem + lane_t + C::TM_O + 32 * c, r);
+            tmem_st32(tmem + lane_t + C::TM_O + h * DH + 32 * c, r);
           }
           tmem_wait_st();
         }
@@ -365,15 +399,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         m_used = m_next;
       }
       const float ms = (m_used == -INFINITY) ? 0.f : m_used;
-      uint32_t pk[C::N / 2];
-      float sum = 0.f;
+      uint32_t pk[NH / 2];
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < C::N / 2; ++c) {
+      for (int c = 0; c < NH / 2; ++c) {
         const float p0 = ex2(x[2 * c] - ms), p1 = ex2(x[2 * c + 1] - ms);
-        sum += p0 + p1;
+        s4[c & 3] += p0 + p1;
         pk[c] = pack_bf16(p0, p1);
       }
-      l += sum;
+      l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      const int kt0 = (tile_lo + j) * C::N;
       if (kt0 + C::N > seq_len) {
         // keys past the sequence end: their V rows may hold anything; zero them
         const int st = j % C::VST;
@@ -381,7 +416,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         const int r0 = max(0, seq_len - kt0);
         const int n16 = (C::N - r0) * 8 * C::CH;
-        for (int i = threadIdx.x - 64; i < n16; i += 128) {
+        for (int i = sid; i < n16; i += 256) {
           const int c = i / ((C::N - r0) * 8), rem = i % ((C::N - r0) * 8);
           uint4 *dst = reinterpret_cast<uint4 *>(dsm_ptr + C::OFF_V + st * C::KV_BYTES + c * C::KV_CHUNK +
                                                  (r0 + rem / 8) * 128 + (rem % 8) * 16);
@@ -394,12 +429,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       }
 #pragma unroll
-      for (int c = 0; c < C::N / 64; ++c) {
-        uint32_t r[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) r[e] = pk[32 * c + e];
-        tmem_st32(tmem + lane_t + C::TM_S + (j & 1) * C::N + 32 * c, r);
-      }
+      for (int c = 0; c < NH / 2; c += 16)
+        tmem_st16(tmem + lane_t + C::TM_S + (j & 1) * C::N + h * (NH / 2) + c, pk + c);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(&ctl.p_full[j & 1]));
@@ -408,17 +439,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       ok = mbar_wait(smem_u32(&ctl.o_full), (n_tiles - 1) & 1, abort_flag, gerr, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
     }
+    if (ok) {
+      // full row sum = both halves; buffer n_tiles & 1 was last read at tile
+      // n_tiles - 2, before every thread passed the exchange of tile n_tiles - 1
+      ctl.red[n_tiles & 1][h][row] = l;
+      mbar_arrive(smem_u32(&ctl.xl));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.xl), 0, abort_flag, gerr, kWaitLimitNs));
+      l += ctl.red[n_tiles & 1][h ^ 1][row];
+    }
     if (!ok) {
       *abort_flag = 1;
       report(a.err, SWA_ERR_TIMEOUT);
     } else {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + out_row * C::D;
+      __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + out_row * C::D + h * DH;
 #pragma unroll 1
-      for (int c = 0; c < C::D / 32; ++c) {
+      for (int c = 0; c < DH / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_t + C::TM_O + 32 * c, r);
+        tmem_ld32(tmem + lane_t + C::TM_O + h * DH + 32 * c, r);
         tmem_wait_ld();
         if (row_valid) {
           uint4 v[4];
@@ -431,7 +470,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           for (int e = 0; e < 4; ++e) dst[e] = v[e];
         }
       }
-      if (row_valid && a.lse != nullptr)
+      if (row_valid && h == 0 && a.lse != nullptr)
         a.lse[out_row] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
@@ -489,11 +528,13 @@ cudaError_t run(const AttnArgs &a, cudaStream_t st) {
       !make_map(&mv, a.v_cache, C::D, a.hkv, (uint64_t)a.num_blocks * a.block_size, C::D * esz,
                 (uint64_t)a.hkv * C::D * esz, 64, 1, R))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  constexpr int smem = smem_bytes<C>();
+  static_assert(smem <= 227 * 1024, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t blocks = a.num_tokens / bq + a.num_seqs;
   dim3 grid((unsigned)blocks, (unsigned)a.hkv);
-  attn_tc_kernel<C><<<grid, 192, C::SMEM, st>>>(mq, mk, mv, a, G);
+  attn_tc_kernel<C><<<grid, 320, smem, st>>>(mq, mk, mv, a, G);
   return cudaGetLastError();
 }
 
