@@ -5,12 +5,13 @@
 //
 // One CTA = one 128-row query tile: BQ = 128 / G query positions x the G query
 // heads of one kv head (GQA packing -- every K/V tile is staged once for the
-// whole group).  Ten warps:
-//   warp 0     TMA producer: the Q tile once, then K and V tiles of N keys,
-//              gathered page by page through the block table into a
-//              STAGES-deep ring (128-byte swizzled, one box per page and
-//              64-column chunk; pages past the sequence or with a bad block id
-//              are read from outside the tensor, which the TMA fills with 0).
+// whole group).  Eleven warps:
+//   warps 0,10 TMA producers of K and V: K and V tiles of N keys, gathered
+//              page by page through the block table into their own rings
+//              (128-byte swizzled, one box per page and 64-column chunk; pages
+//              past the sequence or with a bad block id are read from outside
+//              the tensor, which the TMA fills with 0).  The Q tile is copied
+//              once, as soon as the block's barriers exist.
 //   warp 1     tcgen05 issuer and TMEM owner: S = Q K^T into one of two TMEM S
 //              buffers, then O += P V with P read from TMEM (where the
 //              softmax wrote it over S) and V from shared memory (MN-major).
@@ -61,12 +62,14 @@ struct Cfg {
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
   static_assert(D + 2 * N <= 512, "TMEM budget");
   static_assert(KST <= 4 && VST <= 4 && VST <= KST, "ring depths");
-  static_assert((KST - VST + 1) * (N / 16) <= 32, "V lag must stay inside the previous slot batch");
   static_assert((N / 16) * CH <= 32, "one warp instruction must cover a tile's boxes");
 };
 
+constexpr int kMaxSmemRanges = 64;      // image ranges staged in shared memory (more: read from L1)
+
 struct Ctrl {
   float red[2][2][128];                  // half-row max (and, at the end, sum) exchange buffers
+  int32_t ranges[2 * kMaxSmemRanges];
   uint64_t q_full;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2];
@@ -81,7 +84,7 @@ template <class C>
 constexpr int smem_bytes() { return C::OFF_CTRL + (int)sizeof(Ctrl); }
 
 template <class C>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const int G) {
   // Everything lives in dynamic shared memory, which starts 1024-byte aligned
@@ -143,11 +146,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     mbar_init(smem_u32(&ctl.o_full), 1);
     mbar_init(smem_u32(&ctl.drain), 1);
     mbar_fence_init();
+    // the Q copy depends only on the block's first token: start it right away
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+    mbar_expect_tx(smem_u32(&ctl.q_full), C::Q_BYTES);
+    for (int c = 0; c < C::CH; ++c)
+      tma_load_3d(q_s + c * C::Q_CHUNK, &tm_q, c * 64, hk * G, qstart + qpos_lo, smem_u32(&ctl.q_full));
   }
+  // this sequence's image ranges, staged once for the 256 interval evaluations
+  const int nr = a.mm_ranges ? a.max_mm_ranges : 0;
+  const bool ranges_in_smem = nr <= kMaxSmemRanges;
+  const int32_t *ranges_g = a.mm_ranges ? a.mm_ranges + (int64_t)s * a.max_mm_ranges * 2 : nullptr;
+  if (warp == 1 && ranges_in_smem)
+    for (int i = lane; i < 2 * nr; i += 32) ctl.ranges[i] = __ldg(ranges_g + i);
   __syncthreads();
 
   // ---- each softmax thread: its row's visible interval; the CTA's union ----
-  const bool is_softmax = warp >= 2;
+  const bool is_softmax = warp >= 2 && warp < 10;
   const int row = 32 * (warp & 3) + lane;            // TMEM lane of this thread
   int klo = 1, khi = 0;
   bool row_valid = false;
@@ -155,17 +171,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (is_softmax) {
     const int qpos = qpos_lo + row / G;
     row_valid = qpos < qlen;
+    int red_lo = INT_MAX, red_hi = -1;
     if (row_valid) {
-      const int32_t *ranges = a.mm_ranges ? a.mm_ranges + (int64_t)s * a.max_mm_ranges * 2 : nullptr;
-      const Span sp = visible_span(ctx + qpos, seq_len, a.window, a.causal != 0, ranges,
-                                   a.mm_ranges ? a.max_mm_ranges : 0);
+      const Span sp = visible_span(ctx + qpos, seq_len, a.window, a.causal != 0,
+                                   ranges_in_smem ? ctl.ranges : ranges_g, nr);
       klo = sp.lo;
       khi = sp.hi;
       out_row = (int64_t)(qstart + qpos) * a.hq + hk * G + row % G;
-      if (klo <= khi) {
-        atomicMin(&ctl.kmin, klo);
-        atomicMax(&ctl.kmax, khi);
-      }
+      if (klo <= khi) { red_lo = klo; red_hi = khi; }
+    }
+    red_lo = __reduce_min_sync(0xffffffffu, red_lo);
+    red_hi = __reduce_max_sync(0xffffffffu, red_hi);
+    if (lane == 0) {
+      atomicMin(&ctl.kmin, red_lo);
+      atomicMax(&ctl.kmax, red_hi);
     }
   }
   if (warp == 1) {
@@ -182,21 +201,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   volatile int *abort_flag = &ctl.abort;
   const volatile int32_t *gerr = a.err;
 
-  if (warp == 0) {
-    // =============================== TMA producer ===============================
-    // The whole warp runs this loop: each lane resolves the cache slot of one
-    // box (one page, or part of one) through the block table, 32 boxes per
-    // batch and one batch ahead, and lane 0 issues the copies with the slots
-    // fetched by shuffle -- no block-table load sits on the issue path.
+  if (warp == 0 || warp == 10) {
+    // =============================== TMA producers ==============================
+    // Warp 0 streams K tiles, warp 10 streams V tiles, each through its own
+    // ring.  The whole warp runs the loop: each lane resolves the cache slot of
+    // one box (one page, or part of one) through the block table, 32 boxes per
+    // batch and one batch ahead, and one warp instruction then issues every
+    // box of a tile (lane i*CH + c copies box i, 64-column chunk c).
+    const bool is_v = warp == 10;
+    const int ST = is_v ? C::VST : C::KST;
+    int issued = 0;
+    bool ok = true;
     if (n_tiles > 0) {
-      if (lane == 0) {
-        tma_prefetch_map(&tm_q);
-        tma_prefetch_map(&tm_k);
-        tma_prefetch_map(&tm_v);
-        mbar_expect_tx(smem_u32(&ctl.q_full), C::Q_BYTES);
-        for (int c = 0; c < C::CH; ++c)
-          tma_load_3d(q_s + c * C::Q_CHUNK, &tm_q, c * 64, hk * G, qstart + qpos_lo, smem_u32(&ctl.q_full));
-      }
       const int R = min(a.block_size, C::N);             // rows per box
       const int boxes = C::N / R;                         // boxes per tile
       const int total_boxes = n_tiles * boxes;
@@ -209,12 +225,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           const int page = k / a.block_size;
           const int32_t blk = page < a.bt_stride ? __ldg(bt + page) : -1;
           if (blk >= 0 && blk < a.num_blocks) slot = blk * a.block_size + (k - page * a.block_size);
-          else report(a.err, SWA_ERR_BLOCK_ID);
+          else if (!is_v) report(a.err, SWA_ERR_BLOCK_ID);
         }
         return slot;
       };
-      // V tiles trail K tiles by at most KST - VST + 1 tiles (< 32 boxes), so
-      // the batch before the current one is all a lagging request can need.
       int batch = 0;
       int prv = oob, cur = resolve(lane), nxt = resolve(32 + lane);
       auto advance = [&](int b_max) {                     // warp-uniform
@@ -225,14 +239,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           nxt = resolve((batch + 1) * 32 + lane);
         }
       };
-      auto slot_lane = [&](int b) -> int {                // per-lane b, inside the current or previous batch
+      auto slot_lane = [&](int b) -> int {                // per-lane b: current batch, or the one before
         const int from_cur = __shfl_sync(0xffffffffu, cur, (b - batch * 32) & 31);
         const int from_prv = __shfl_sync(0xffffffffu, prv, (b - (batch - 1) * 32) & 31);
         return b >= batch * 32 ? from_cur : from_prv;
       };
-      // one warp instruction issues a whole tile: lane i*CH + c copies box i, chunk c
-      auto issue = [&](int t, bool is_v) {
-        const int st = is_v ? t % C::VST : t % C::KST;
+      const CUtensorMap *map = is_v ? &tm_v : &tm_k;
+      auto issue = [&](int t) {
+        const int st = t % ST;
         const uint32_t full = smem_u32(is_v ? &ctl.v_full[st] : &ctl.k_full[st]);
         const uint32_t dst = (is_v ? v_s : k_s) + st * C::KV_BYTES;
         if (lane == 0) mbar_expect_tx(full, C::KV_BYTES);
@@ -240,43 +254,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         advance(t * boxes + boxes - 1);
         const int i = min(lane / C::CH, boxes - 1), c = lane % C::CH;
         const int slot = slot_lane(t * boxes + i);
-        if (lane < boxes * C::CH)
-          tma_load_3d(dst + c * C::KV_CHUNK + i * R * 128, is_v ? &tm_v : &tm_k, c * 64, hk, slot, full);
+        if (lane < boxes * C::CH) tma_load_3d(dst + c * C::KV_CHUNK + i * R * 128, map, c * 64, hk, slot, full);
       };
-      // fill both rings, then refill each stage as soon as its consumer frees it:
-      // K tile t+KST after QK_t, V tile t+VST after PV_t (the order those happen in)
-      int k_issued = min(C::KST, n_tiles), v_issued = min(C::VST, n_tiles);
-      for (int t = 0; t < n_tiles && (t < C::KST || t < C::VST); ++t) {
-        if (t < C::KST) issue(t, false);
-        if (t < C::VST) issue(t, true);
-      }
-      bool ok = true;
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j + C::KST < n_tiles) {
-          ok = mbar_wait(smem_u32(&ctl.k_empty[j % C::KST]), (j / C::KST) & 1, abort_flag, gerr, kWaitLimitNs);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          issue(j + C::KST, false);
-          k_issued = j + C::KST + 1;
-        }
-        if (j + C::VST < n_tiles) {
-          ok = mbar_wait(smem_u32(&ctl.v_empty[j % C::VST]), (j / C::VST) & 1, abort_flag, gerr, kWaitLimitNs);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          issue(j + C::VST, true);
-          v_issued = j + C::VST + 1;
-        }
+      // fill the ring, then refill each stage as soon as its consumer (QK_j
+      // for K, PV_j for V) has released it
+      issued = min(ST, n_tiles);
+      for (int t = 0; t < issued; ++t) issue(t);
+      for (int j = 0; j + ST < n_tiles; ++j) {
+        const uint32_t empty = smem_u32(is_v ? &ctl.v_empty[j % ST] : &ctl.k_empty[j % ST]);
+        ok = __all_sync(0xffffffffu, mbar_wait(empty, (j / ST) & 1, abort_flag, gerr, kWaitLimitNs));
+        if (!ok) break;
+        issue(j + ST);
+        issued = j + ST + 1;
       }
       if (!ok && lane == 0) {
         *abort_flag = 1;
         report(a.err, SWA_ERR_TIMEOUT);
       }
-      // drain: every load issued here must have landed before the CTA exits
-      if (lane == 0) {
-        for (int t = max(0, k_issued - C::KST); t < k_issued; ++t)
-          mbar_wait(smem_u32(&ctl.k_full[t % C::KST]), (t / C::KST) & 1, nullptr, nullptr, kWaitLimitNs);
-        for (int t = max(0, v_issued - C::VST); t < v_issued; ++t)
-          mbar_wait(smem_u32(&ctl.v_full[t % C::VST]), (t / C::VST) & 1, nullptr, nullptr, kWaitLimitNs);
-        mbar_wait(smem_u32(&ctl.q_full), 0, nullptr, nullptr, kWaitLimitNs);
-      }
+    }
+    // drain: every load issued by this warp must have landed before the CTA exits
+    if (lane == 0) {
+      for (int t = max(0, issued - ST); t < issued; ++t)
+        mbar_wait(smem_u32(is_v ? &ctl.v_full[t % ST] : &ctl.k_full[t % ST]), (t / ST) & 1, nullptr, nullptr,
+                  kWaitLimitNs);
+      if (!is_v) mbar_wait(smem_u32(&ctl.q_full), 0, nullptr, nullptr, kWaitLimitNs);
     }
   } else if (warp == 1) {
     // =============================== MMA issuer =================================
@@ -326,7 +327,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mma_commit(smem_u32(&ctl.drain));
       mbar_wait(smem_u32(&ctl.drain), 0, nullptr, nullptr, kWaitLimitNs);
     }
-  } else {
+  } else if (is_softmax) {
     // =============================== softmax ====================================
     // Two warpgroups share every row: warpgroup h owns S columns
     // [h*N/2, (h+1)*N/2) and O columns [h*D/2, (h+1)*D/2).  Both keep the
@@ -534,7 +535,7 @@ cudaError_t run(const AttnArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int64_t blocks = a.num_tokens / bq + a.num_seqs;
   dim3 grid((unsigned)blocks, (unsigned)a.hkv);
-  attn_tc_kernel<C><<<grid, 320, smem, st>>>(mq, mk, mv, a, G);
+  attn_tc_kernel<C><<<grid, 352, smem, st>>>(mq, mk, mv, a, G);
   return cudaGetLastError();
 }
 

@@ -54,7 +54,8 @@ __device__ inline int find_seq(const int32_t *qsl, int num_seqs, int64_t block, 
 // (right(q) = q causal, q+W-1 non-causal; with W <= 0 the left edge is 0 and a
 // non-causal right edge is the sequence end).  Every range holding q starts at
 // or before q, so its clamped part [max(s, q-W+1), e] joins the base window
-// without a gap.  Returns lo > hi when nothing is visible.
+// without a gap.  Returns lo > hi when nothing is visible.  `ranges` may point
+// to global or shared memory (plain generic loads).
 struct Span { int lo, hi; };
 
 __device__ inline Span visible_span(int q, int seq_len, int window, bool causal,
@@ -68,7 +69,7 @@ __device__ inline Span visible_span(int q, int seq_len, int window, bool causal,
     sp.hi = causal ? q : seq_len - 1;
   }
   for (int i = 0; i < num_ranges; ++i) {
-    int s = __ldg(ranges + 2 * i), e = __ldg(ranges + 2 * i + 1);
+    const int s = ranges[2 * i], e = ranges[2 * i + 1];
     if (s < e && s <= q && q <= e) sp.hi = max(sp.hi, e);
   }
   sp.hi = min(sp.hi, seq_len - 1);
