@@ -5,29 +5,37 @@
 //
 // One CTA = one 128-row query tile: BQ = 128 / G query positions x the G query
 // heads of one kv head (GQA packing -- every K/V tile is staged once for the
-// whole group).  Eleven warps:
-//   warps 0,10 TMA producers of K and V: K and V tiles of N keys, gathered
-//              page by page through the block table into their own rings
-//              (128-byte swizzled, one box per page and 64-column chunk; pages
-//              past the sequence or with a bad block id are read from outside
-//              the tensor, which the TMA fills with 0).  The Q tile is copied
-//              once, as soon as the block's barriers exist.
-//   warp 1     tcgen05 issuer and TMEM owner: S = Q K^T into one of two TMEM S
-//              buffers, then O += P V with P read from TMEM (where the
-//              softmax wrote it over S) and V from shared memory (MN-major).
-//   warps 2-9  softmax, two warpgroups: thread i of each owns row i (TMEM
-//              lane i) and one half of the tile's columns; masks only tiles
-//              not fully inside its visible interval, keeps a running max in
-//              the log2 domain and rescales O in TMEM only when the max grows
-//              by more than 2^8, writes P as bf16 into TMEM, and finally
-//              normalises its half of O and stores out / lse.
-// The key loop covers only the union of the rows' visible intervals -- the
-// pruned tile range [lo, hi) of the union formula.  Every mbarrier wait is
-// bounded in time; on expiry the CTA sets SWA_ERR_TIMEOUT, drains its own
-// TMA loads and MMAs, frees TMEM and exits.
+// whole group).  The key loop walks 128-key tiles over the union of the rows'
+// visible intervals (the pruned tile range of the union formula).
+//
+// Shared memory: the Q tile (TMA, 128-byte swizzled, K-major) and two rings of
+// 32 KB units (for head_dim 256; 16 KB for 128): a K unit holds one half of
+// head_dim for all 128 keys of a tile, a V unit holds all of head_dim for one
+// 64-key half of a tile.  So QK_j consumes two K units and PV_j two V units,
+// and each unit is recycled as soon as its half of the MMA work is done.
+// TMEM (512 columns): O [0, D), S buffers [D, D+128) and [D+128, D+256) in
+// fp32; the softmax overwrites the front half of S_j with P_j as bf16 pairs,
+// which the PV MMA reads as its A operand.
+//
+// Eleven warps:
+//   warp 0     K producer, warp 10 V producer: every lane resolves the cache
+//              slot of one page box through the block table (32 boxes per
+//              batch, one batch ahead) and one warp instruction issues a whole
+//              unit's boxes (one per page and 64-column chunk); pages past the
+//              sequence or with a bad block id are read from outside the
+//              tensor, which the TMA fills with 0.  Thread 0 copies Q as soon
+//              as the barriers exist.
+//   warp 1     tcgen05 issuer and TMEM owner: QK_0, QK_1, then per tile
+//              PV_j (once P_j is written) and QK_{j+2}.
+//   warps 2-9  softmax, two warpgroups: thread i of each owns row i (TMEM lane
+//              i) and one half of the tile's columns; the half-row maxima are
+//              exchanged through shared memory once per tile.  Masks only tiles
+//              not fully inside the row's visible interval, keeps the running
+//              max in the log2 domain and rescales O in TMEM only when the max
+//              grows by more than 2^8, and at the end normalises its half of O.
+// Every mbarrier wait is bounded in time; on expiry the CTA sets
+// SWA_ERR_TIMEOUT, drains its own TMA loads and MMAs, frees TMEM and exits.
 #include <cuda.h>
-
-#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -39,39 +47,43 @@ namespace {
 using namespace tc;
 
 constexpr uint64_t kWaitLimitNs = 200000000ull;    // 200 ms per wait: far above any real stall
+constexpr int kMaxSmemRanges = 64;                 // image ranges staged in shared memory
+constexpr int kMaxUnits = 8;                       // ring slots per operand
 
-template <int D_, int N_, int KST_, int VST_>
+template <int D_, int KSU_, int VSU_>
 struct Cfg {
   static constexpr int D = D_;          // head dim
-  static constexpr int N = N_;          // keys per K/V tile
-  static constexpr int KST = KST_;      // K ring depth
-  static constexpr int VST = VST_;      // V ring depth
+  static constexpr int N = 128;         // keys per tile
   static constexpr int M = 128;         // query rows per CTA
   static constexpr int CH = D / 64;     // 128-byte column chunks per row
+  static constexpr int KSU = KSU_;      // K ring slots (units)
+  static constexpr int VSU = VSU_;      // V ring slots (units)
   static constexpr int Q_CHUNK = M * 128;
   static constexpr int Q_BYTES = M * D * 2;
-  static constexpr int KV_CHUNK = N * 128;
-  static constexpr int KV_BYTES = N * D * 2;
+  static constexpr int UNIT = N * D;                 // bytes of a K or V unit (= 64 keys x D x 2)
+  static constexpr int KU_CH = CH / 2;               // chunks per K unit (half of head_dim)
+  static constexpr int KU_CHUNK = N * 128;           // bytes per chunk in a K unit (128 keys)
+  static constexpr int VU_KEYS = N / 2;              // keys per V unit
+  static constexpr int VU_CHUNK = VU_KEYS * 128;     // bytes per chunk in a V unit
+  static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = Q_BYTES;
-  static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
-  static constexpr int OFF_CTRL = OFF_V + VST * KV_BYTES;         // control block (barriers, exchange)
-  static constexpr int TM_O = 0;        // TMEM columns: O [0, D), S0 [D, D+N), S1 [D+N, D+2N)
+  static constexpr int OFF_V = OFF_K + KSU * UNIT;
+  static constexpr int OFF_CTRL = OFF_V + VSU * UNIT;
+  static constexpr int TM_O = 0;        // TMEM columns: O [0, D), S buffer b at [D + b*N, D + (b+1)*N)
   static constexpr int TM_S = D;
   static constexpr uint32_t TM_COLS = 512;
   static constexpr uint32_t IDESC_QK = idesc_bf16(128, N, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
   static_assert(D + 2 * N <= 512, "TMEM budget");
-  static_assert(KST <= 4 && VST <= 4 && VST <= KST, "ring depths");
-  static_assert((N / 16) * CH <= 32, "one warp instruction must cover a tile's boxes");
+  static_assert(KSU <= kMaxUnits && VSU <= kMaxUnits && KSU >= 2 && VSU >= 2, "ring sizes");
+  static_assert((N / 16) * KU_CH <= 32 && (VU_KEYS / 16) * CH <= 32, "one warp instruction per unit");
 };
-
-constexpr int kMaxSmemRanges = 64;      // image ranges staged in shared memory (more: read from L1)
 
 struct Ctrl {
   float red[2][2][128];                  // half-row max (and, at the end, sum) exchange buffers
   int32_t ranges[2 * kMaxSmemRanges];
   uint64_t q_full;
-  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t k_full[kMaxUnits], k_empty[kMaxUnits], v_full[kMaxUnits], v_empty[kMaxUnits];
   uint64_t s_full[2], p_full[2];
   uint64_t o_full, drain;
   uint64_t xch[2], xl;                   // exchange barriers of the two softmax warpgroups
@@ -93,7 +105,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   extern __shared__ __align__(1024) uint8_t dsm_ptr[];
   const uint32_t dsm = smem_u32(dsm_ptr);
   Ctrl &ctl = *reinterpret_cast<Ctrl *>(dsm_ptr + C::OFF_CTRL);
-  const uint32_t q_s = dsm;
+  const uint32_t q_s = dsm + C::OFF_Q;
   const uint32_t k_s = dsm + C::OFF_K;
   const uint32_t v_s = dsm + C::OFF_V;
 
@@ -129,11 +141,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     ctl.kmin = INT_MAX;
     ctl.kmax = -1;
     mbar_init(smem_u32(&ctl.q_full), 1);
-    for (int i = 0; i < C::KST; ++i) {
+    for (int i = 0; i < C::KSU; ++i) {
       mbar_init(smem_u32(&ctl.k_full[i]), 1);
       mbar_init(smem_u32(&ctl.k_empty[i]), 1);
     }
-    for (int i = 0; i < C::VST; ++i) {
+    for (int i = 0; i < C::VSU; ++i) {
       mbar_init(smem_u32(&ctl.v_full[i]), 1);
       mbar_init(smem_u32(&ctl.v_empty[i]), 1);
     }
@@ -203,22 +215,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   if (warp == 0 || warp == 10) {
     // =============================== TMA producers ==============================
-    // Warp 0 streams K tiles, warp 10 streams V tiles, each through its own
-    // ring.  The whole warp runs the loop: each lane resolves the cache slot of
-    // one box (one page, or part of one) through the block table, 32 boxes per
-    // batch and one batch ahead, and one warp instruction then issues every
-    // box of a tile (lane i*CH + c copies box i, 64-column chunk c).
     const bool is_v = warp == 10;
-    const int ST = is_v ? C::VST : C::KST;
+    const int SU = is_v ? C::VSU : C::KSU;
+    const int n_units = 2 * n_tiles;               // unit u = 2*tile + half
     int issued = 0;
     bool ok = true;
     if (n_tiles > 0) {
-      const int R = min(a.block_size, C::N);             // rows per box
-      const int boxes = C::N / R;                         // boxes per tile
-      const int total_boxes = n_tiles * boxes;
-      const int oob = (int)(a.num_blocks * a.block_size); // first slot outside the cache: zero fill
+      // K units cover 128 keys, V units 64 keys; a box is one page (or a
+      // 128-key part of a bigger page)
+      const int unit_keys = is_v ? C::VU_KEYS : C::N;
+      const int R = min(a.block_size, unit_keys);    // rows per box
+      const int boxes = unit_keys / R;               // boxes per unit (per chunk)
+      const int uch = is_v ? C::CH : C::KU_CH;       // chunks per unit
+      const int total_boxes = (n_tiles * C::N) / R;
+      const int oob = (int)(a.num_blocks * a.block_size);
       const int32_t *bt = a.block_table + (int64_t)s * a.bt_stride;
-      auto resolve = [&](int b) -> int {
+      auto resolve = [&](int b) -> int {           // slot of the first key of box b
         const int k = tile_lo * C::N + b * R;
         int slot = oob;
         if (b < total_boxes && k < seq_len) {
@@ -231,7 +243,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       };
       int batch = 0;
       int prv = oob, cur = resolve(lane), nxt = resolve(32 + lane);
-      auto advance = [&](int b_max) {                     // warp-uniform
+      auto advance = [&](int b_max) {               // warp-uniform
         while (b_max >= (batch + 1) * 32) {
           prv = cur;
           cur = nxt;
@@ -239,33 +251,37 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           nxt = resolve((batch + 1) * 32 + lane);
         }
       };
-      auto slot_lane = [&](int b) -> int {                // per-lane b: current batch, or the one before
+      auto slot_lane = [&](int b) -> int {          // per-lane b: current batch, or the one before
         const int from_cur = __shfl_sync(0xffffffffu, cur, (b - batch * 32) & 31);
         const int from_prv = __shfl_sync(0xffffffffu, prv, (b - (batch - 1) * 32) & 31);
         return b >= batch * 32 ? from_cur : from_prv;
       };
       const CUtensorMap *map = is_v ? &tm_v : &tm_k;
-      auto issue = [&](int t) {
-        const int st = t % ST;
-        const uint32_t full = smem_u32(is_v ? &ctl.v_full[st] : &ctl.k_full[st]);
-        const uint32_t dst = (is_v ? v_s : k_s) + st * C::KV_BYTES;
-        if (lane == 0) mbar_expect_tx(full, C::KV_BYTES);
+      auto issue = [&](int u) {
+        const int t = u >> 1, half = u & 1, slot_i = u % SU;
+        const uint32_t full = smem_u32(is_v ? &ctl.v_full[slot_i] : &ctl.k_full[slot_i]);
+        const uint32_t dst = (is_v ? v_s : k_s) + slot_i * C::UNIT;
+        if (lane == 0) mbar_expect_tx(full, C::UNIT);
         __syncwarp();
-        advance(t * boxes + boxes - 1);
-        const int i = min(lane / C::CH, boxes - 1), c = lane % C::CH;
-        const int slot = slot_lane(t * boxes + i);
-        if (lane < boxes * C::CH) tma_load_3d(dst + c * C::KV_CHUNK + i * R * 128, map, c * 64, hk, slot, full);
+        // K: unit = head_dim half `half` of tile t's 128 keys; V: key half `half`
+        const int b0 = is_v ? (2 * t + half) * boxes : t * boxes;
+        advance(b0 + boxes - 1);
+        const int i = min(lane / uch, boxes - 1), c = lane % uch;
+        const int slot = slot_lane(b0 + i);
+        const int x = (is_v ? c : half * C::KU_CH + c) * 64;
+        const uint32_t d = dst + c * (is_v ? C::VU_CHUNK : C::KU_CHUNK) + i * R * 128;
+        if (lane < boxes * uch) tma_load_3d(d, map, x, hk, slot, full);
       };
-      // fill the ring, then refill each stage as soon as its consumer (QK_j
-      // for K, PV_j for V) has released it
-      issued = min(ST, n_tiles);
-      for (int t = 0; t < issued; ++t) issue(t);
-      for (int j = 0; j + ST < n_tiles; ++j) {
-        const uint32_t empty = smem_u32(is_v ? &ctl.v_empty[j % ST] : &ctl.k_empty[j % ST]);
-        ok = __all_sync(0xffffffffu, mbar_wait(empty, (j / ST) & 1, abort_flag, gerr, kWaitLimitNs));
+      // fill the ring, then refill a slot as soon as its half of QK (for K) or
+      // of PV (for V) has finished with it
+      issued = min(SU, n_units);
+      for (int u = 0; u < issued; ++u) issue(u);
+      for (int u = SU; u < n_units; ++u) {
+        const uint32_t empty = smem_u32(is_v ? &ctl.v_empty[u % SU] : &ctl.k_empty[u % SU]);
+        ok = __all_sync(0xffffffffu, mbar_wait(empty, ((u / SU) - 1) & 1, abort_flag, gerr, kWaitLimitNs));
         if (!ok) break;
-        issue(j + ST);
-        issued = j + ST + 1;
+        issue(u);
+        issued = u + 1;
       }
       if (!ok && lane == 0) {
         *abort_flag = 1;
@@ -274,8 +290,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     // drain: every load issued by this warp must have landed before the CTA exits
     if (lane == 0) {
-      for (int t = max(0, issued - ST); t < issued; ++t)
-        mbar_wait(smem_u32(is_v ? &ctl.v_full[t % ST] : &ctl.k_full[t % ST]), (t / ST) & 1, nullptr, nullptr,
+      for (int u = max(0, issued - SU); u < issued; ++u)
+        mbar_wait(smem_u32(is_v ? &ctl.v_full[u % SU] : &ctl.k_full[u % SU]), (u / SU) & 1, nullptr, nullptr,
                   kWaitLimitNs);
       if (!is_v) mbar_wait(smem_u32(&ctl.q_full), 0, nullptr, nullptr, kWaitLimitNs);
     }
@@ -285,39 +301,53 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       bool ok = mbar_wait(smem_u32(&ctl.q_full), 0, abort_flag, gerr, kWaitLimitNs);
       tc_fence_after();
       auto issue_qk = [&](int j) -> bool {
-        const int st = j % C::KST;
-        if (!mbar_wait(smem_u32(&ctl.k_full[st]), (j / C::KST) & 1, abort_flag, gerr, kWaitLimitNs)) return false;
-        tc_fence_after();
         const uint32_t d = tmem + C::TM_S + (j & 1) * C::N;
+        for (int half = 0; half < 2; ++half) {
+          const int u = 2 * j + half, slot = u % C::KSU;
+          if (!mbar_wait(smem_u32(&ctl.k_full[slot]), (u / C::KSU) & 1, abort_flag, gerr, kWaitLimitNs))
+            return false;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < C::D / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;     // 16-column step inside the 128-byte swizzle row
-          const uint64_t ad = smem_desc_sw128(q_s + (kk >> 2) * C::Q_CHUNK + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(k_s + st * C::KV_BYTES + (kk >> 2) * C::KV_CHUNK + off, 16, 1024);
-          mma_ss(d, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < C::D / 32; ++kk) {     // 16-column steps over this half of head_dim
+            const uint32_t off = (kk & 3) * 32;         // inside the 128-byte swizzle row
+            const int cl = kk >> 2;                     // chunk within the unit
+            const uint64_t ad = smem_desc_sw128(q_s + (half * C::KU_CH + cl) * C::Q_CHUNK + off, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(k_s + slot * C::UNIT + cl * C::KU_CHUNK + off, 16, 1024);
+            mma_ss(d, ad, bd, C::IDESC_QK, (half > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&ctl.k_empty[slot]));
         }
         mma_commit(smem_u32(&ctl.s_full[j & 1]));
-        mma_commit(smem_u32(&ctl.k_empty[st]));
         return true;
       };
+      // S buffer j & 1 last held P_{j-2}, whose PV was issued before QK_j;
+      // tcgen05 ops from one thread run in issue order
       if (ok) ok = issue_qk(0);
+      if (ok && n_tiles > 1) ok = issue_qk(1);
       for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j + 1 < n_tiles && !issue_qk(j + 1)) { ok = false; break; }
-        const int st = j % C::VST;
-        if (!mbar_wait(smem_u32(&ctl.p_full[j & 1]), (j >> 1) & 1, abort_flag, gerr, kWaitLimitNs) ||
-            !mbar_wait(smem_u32(&ctl.v_full[st]), (j / C::VST) & 1, abort_flag, gerr, kWaitLimitNs)) {
+        if (!mbar_wait(smem_u32(&ctl.p_full[j & 1]), (j >> 1) & 1, abort_flag, gerr, kWaitLimitNs)) {
           ok = false;
           break;
         }
-        tc_fence_after();
         const uint32_t p_t = tmem + C::TM_S + (j & 1) * C::N;
+        for (int half = 0; half < 2 && ok; ++half) {
+          const int u = 2 * j + half, slot = u % C::VSU;
+          if (!mbar_wait(smem_u32(&ctl.v_full[slot]), (u / C::VSU) & 1, abort_flag, gerr, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < C::N / 16; ++kk) {
-          const uint64_t bd = smem_desc_sw128(v_s + st * C::KV_BYTES + kk * 16 * 128, C::KV_CHUNK, 1024);
-          mma_ts(tmem + C::TM_O, p_t + kk * 8, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < C::VU_KEYS / 16; ++kk) {
+            const uint64_t bd = smem_desc_sw128(v_s + slot * C::UNIT + kk * 16 * 128, C::VU_CHUNK, 1024);
+            mma_ts(tmem + C::TM_O, p_t + (half * (C::VU_KEYS / 16) + kk) * 8, bd, C::IDESC_PV,
+                   (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&ctl.v_empty[slot]));
         }
-        mma_commit(smem_u32(&ctl.v_empty[st]));
+        if (!ok) break;
         mma_commit(smem_u32(&ctl.o_full));
+        if (j + 2 < n_tiles && !issue_qk(j + 2)) { ok = false; break; }
       }
       if (!ok) {
         *abort_flag = 1;
@@ -342,7 +372,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      const int kc0 = (tile_lo + j) * C::N + h * NH;     // key of this warpgroup's first column
+      const int kt0 = (tile_lo + j) * C::N;
+      const int kc0 = kt0 + h * NH;                      // key of this warpgroup's first column
       ok = mbar_wait(smem_u32(&ctl.s_full[j & 1]), (j >> 1) & 1, abort_flag, gerr, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -409,29 +440,37 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         pk[c] = pack_bf16(p0, p1);
       }
       l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-      const int kt0 = (tile_lo + j) * C::N;
-      if (kt0 + C::N > seq_len) {
-        // keys past the sequence end: their V rows may hold anything; zero them
-        const int st = j % C::VST;
-        ok = mbar_wait(smem_u32(&ctl.v_full[st]), (j / C::VST) & 1, abort_flag, gerr, kWaitLimitNs);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        const int r0 = max(0, seq_len - kt0);
-        const int n16 = (C::N - r0) * 8 * C::CH;
-        for (int i = sid; i < n16; i += 256) {
-          const int c = i / ((C::N - r0) * 8), rem = i % ((C::N - r0) * 8);
-          uint4 *dst = reinterpret_cast<uint4 *>(dsm_ptr + C::OFF_V + st * C::KV_BYTES + c * C::KV_CHUNK +
-                                                 (r0 + rem / 8) * 128 + (rem % 8) * 16);
-          *dst = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-      }
       if (!pv_prev_done) {
         ok = mbar_wait(smem_u32(&ctl.o_full), (j - 1) & 1, abort_flag, gerr, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       }
+      if (kt0 + C::N > seq_len) {
+        // keys past the sequence end: their V rows may hold anything; zero
+        // them.  PV_{j-1} is done, so every earlier unit of each V slot has
+        // been consumed and the v_full parity below is unambiguous.
+        for (int half = 0; half < 2 && ok; ++half) {
+          const int k0 = kt0 + half * C::VU_KEYS;
+          if (k0 + C::VU_KEYS <= seq_len) continue;
+          const int u = 2 * j + half, slot = u % C::VSU;
+          ok = mbar_wait(smem_u32(&ctl.v_full[slot]), (u / C::VSU) & 1, abort_flag, gerr, kWaitLimitNs);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          const int r0 = max(0, seq_len - k0);
+          const int n16 = (C::VU_KEYS - r0) * 8 * C::CH;
+          for (int i = sid; i < n16; i += 256) {
+            const int c = i / ((C::VU_KEYS - r0) * 8), rem = i % ((C::VU_KEYS - r0) * 8);
+            uint4 *dst = reinterpret_cast<uint4 *>(dsm_ptr + C::OFF_V + slot * C::UNIT + c * C::VU_CHUNK +
+                                                   (r0 + rem / 8) * 128 + (rem % 8) * 16);
+            *dst = make_uint4(0, 0, 0, 0);
+          }
+        }
+        if (!ok) break;
+        fence_proxy_async_smem();
+      }
 #pragma unroll
-      for (int c = 0; c < NH / 2; c += 16)
-        tmem_st16(tmem + lane_t + C::TM_S + (j & 1) * C::N + h * (NH / 2) + c, pk + c);
+      for (int c = 0; c < NH / 2; c += 32)
+        tmem_st32(tmem + lane_t + C::TM_S + (j & 1) * C::N + h * (NH / 2) + c,
+                  *reinterpret_cast<const uint32_t(*)[32]>(pk + c));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(&ctl.p_full[j & 1]));
@@ -520,14 +559,14 @@ template <class C>
 cudaError_t run(const AttnArgs &a, cudaStream_t st) {
   const int G = a.hq / a.hkv;
   const int bq = C::M / G;
-  const int R = a.block_size < C::N ? a.block_size : C::N;
   CUtensorMap mq, mk, mv;
   const uint64_t esz = 2;
+  const uint64_t slots = (uint64_t)a.num_blocks * a.block_size;
   if (!make_map(&mq, a.q, C::D, a.hq, a.num_tokens, C::D * esz, (uint64_t)a.hq * C::D * esz, 64, G, bq) ||
-      !make_map(&mk, a.k_cache, C::D, a.hkv, (uint64_t)a.num_blocks * a.block_size, C::D * esz,
-                (uint64_t)a.hkv * C::D * esz, 64, 1, R) ||
-      !make_map(&mv, a.v_cache, C::D, a.hkv, (uint64_t)a.num_blocks * a.block_size, C::D * esz,
-                (uint64_t)a.hkv * C::D * esz, 64, 1, R))
+      !make_map(&mk, a.k_cache, C::D, a.hkv, slots, C::D * esz, (uint64_t)a.hkv * C::D * esz, 64, 1,
+                (uint32_t)min(a.block_size, C::N)) ||
+      !make_map(&mv, a.v_cache, C::D, a.hkv, slots, C::D * esz, (uint64_t)a.hkv * C::D * esz, 64, 1,
+                (uint32_t)min(a.block_size, C::VU_KEYS)))
     return cudaErrorInvalidValue;
   constexpr int smem = smem_bytes<C>();
   static_assert(smem <= 227 * 1024, "shared memory budget");
@@ -539,8 +578,8 @@ cudaError_t run(const AttnArgs &a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-using Cfg256 = Cfg<256, 64, 3, 2>;     // 64 KB Q + 3 x 32 KB K + 2 x 32 KB V
-using Cfg128 = Cfg<128, 128, 3, 3>;    // 32 KB Q + 3 x 32 KB K + 3 x 32 KB V
+using Cfg256 = Cfg<256, 2, 3>;    // 64 KB Q + 2 K + 3 V units of 32 KB
+using Cfg128 = Cfg<128, 6, 6>;    // 32 KB Q + 6 K + 6 V units of 16 KB
 
 }  // namespace
 
