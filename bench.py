@@ -72,6 +72,23 @@ def visible_pairs_per_head(lay) -> int:
     return total
 
 
+def kernel_traffic():
+    """DRAM bytes per attention launch on the 4-request workload from the committed ncu
+    launch list (profiles/attn_tc_gemma_like.md), or None when the kernel source has
+    changed since those counters were taken."""
+    import hashlib
+    src = os.path.join(ROOT, "paged_sliding_window_swa_gb300", "csrc", "attention_tc.cu")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return MEASURED_TRAFFIC["bytes"] if sha == MEASURED_TRAFFIC["kernel_sha"] else None
+
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one attention launch (ncu, 1 pass)
+MEASURED_TRAFFIC = {"kernel_sha": "bb739acea273b4a1", "bytes": (1101.6 + 527.4) * 1e6}
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -307,7 +324,7 @@ def report_line(args, lay, step, flops, pairs, ms_per_step, attn_ms, feed_ms, cl
             "peak": pk["bf16_tflops"],
             "unit": "TFLOP/s",
             "frac": round(achieved / pk["bf16_tflops"], 4),
-            "traffic": None,
+            "traffic": kernel_traffic(),
             "peak_source": f"{pk['source']} bf16 dense (burst)",
             "avg_launch_ms": round(attn_avg, 4),
         },
@@ -319,7 +336,112 @@ def report_line(args, lay, step, flops, pairs, ms_per_step, attn_ms, feed_ms, cl
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(lay, step, budget_s=args.cpu_seconds)
+    if not args.no_extras:
+        line["extras"] = run_extras(step.dev, pk)
     return line
+
+
+# ---------------------------------------------------------------------------
+# the other workloads and the bandwidth kernels (reported under "extras")
+# ---------------------------------------------------------------------------
+def _time_ms(fn, reps=5, flush=None):
+    """Median device time of fn() in ms over `reps` launches (events on the current stream)."""
+    out = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1))
+    return statistics.median(out)
+
+
+def run_extras(dev, pk):
+    import paged_sliding_window_swa_gb300 as swa
+    res = {}
+    scratch = torch.empty(512 << 20, dtype=torch.uint8, device=dev)     # 512 MB > L2: flush
+
+    def flush():
+        scratch.fill_(1)
+
+    # chunked prefill over cached context (head_dim 128, GQA 4), causal and non-causal
+    for causal in (True, False):
+        lay = W.chunked_prefill(causal)
+        q, k, v = W.make_tensors(lay, device=dev)
+        d = W.device_layout(lay, dev)
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+
+        def attn():
+            swa.swa_mm_paged_attention(q, k, v, d["block_table"], d["query_start_loc"], d["seq_lens"],
+                                       context_lens=d["context_lens"], mm_ranges=d["mm_ranges"],
+                                       max_query_len=lay.max_query_len, window=lay.window, causal=causal,
+                                       scale=lay.scale, out=out, lse=lse)
+        attn()
+        ms = _time_ms(attn)
+        fl = 4.0 * lay.head_dim * lay.num_heads_q * visible_pairs_per_head(lay)
+        res[lay.name] = {"ms": round(ms, 4), "tflops_visible": round(fl / ms / 1e9, 2),
+                         "frac_of_bf16_peak": round(fl / ms / 1e9 / pk["bf16_tflops"], 4),
+                         "tok_per_s": round(lay.num_tokens / ms * 1e3, 1)}
+        del q, k, v, out
+
+    # decode: 128 single-token queries over 4k-64k contexts, split-KV + LSE merge
+    lay = W.decode()
+    q, k, v = W.make_tensors(lay, device=dev)
+    d = W.device_layout(lay, dev)
+    P = lay.num_splits
+    po = torch.empty((P,) + tuple(q.shape), dtype=q.dtype, device=dev)
+    pl = torch.empty((P,) + tuple(q.shape[:2]), dtype=torch.float32, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+
+    def dec_attn():
+        swa.swa_mm_paged_attention(q, k, v, d["block_table"], d["query_start_loc"], d["seq_lens"],
+                                   context_lens=d["context_lens"], max_query_len=1, window=lay.window,
+                                   causal=True, scale=lay.scale, num_splits=P,
+                                   splits_per_seq=d["splits_per_seq"], partial_out=po, partial_lse=pl)
+
+    def dec_merge():
+        swa.lse_combine(po, pl, out=out, out_lse=lse)
+    dec_attn()
+    dec_merge()
+    ms_a = _time_ms(dec_attn)
+    ms_m = _time_ms(dec_merge, flush=flush)
+    kv_bytes = float(lay.seq_lens.sum()) * lay.num_heads_kv * lay.head_dim * 2 * 2
+    live = float(lay.splits_per_seq.sum()) * lay.num_heads_q
+    m_bytes = live * lay.head_dim * 2 + lay.num_tokens * lay.num_heads_q * (P * 4 + lay.head_dim * 2 + 4)
+    res["decode"] = {"attention_ms": round(ms_a, 4), "kv_gbs": round(kv_bytes / ms_a / 1e6, 1),
+                     "kv_frac_of_hbm": round(kv_bytes / ms_a / 1e6 / pk["hbm_gbs"], 4),
+                     "lse_combine_ms": round(ms_m, 4), "lse_combine_gbs": round(m_bytes / ms_m / 1e6, 1),
+                     "step_ms": round(ms_a + ms_m, 4)}
+    del q, k, v, po, pl
+
+    # bandwidth sweeps at sizes where HBM, not launch latency, sets the time (cold L2)
+    n_tok, B = 1 << 24, 16
+    lens = np.full(64, n_tok // 64, dtype=np.int64)
+    qsl = torch.as_tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev)
+    pos = torch.cat([torch.arange(int(x), device=dev, dtype=torch.int64) for x in lens])
+    pages = int(-(-lens.max() // B))
+    bt = torch.randperm(64 * pages, device=dev, dtype=torch.int64).to(torch.int32).view(64, pages)
+    maxn = n_tok + 8192
+    slots = torch.empty(maxn, dtype=torch.int32, device=dev)
+    sm_ms = _time_ms(lambda: swa.swa_slot_mapping(qsl, pos, bt, B, maxn, out=slots), flush=flush)
+    sm_bytes = n_tok * (8 + 4) + (maxn - n_tok) * 4 + 64 * pages * 4
+    res["slot_mapping_16M_tokens"] = {"ms": round(sm_ms, 4), "gbs": round(sm_bytes / sm_ms / 1e6, 1),
+                                      "frac_of_hbm": round(sm_bytes / sm_ms / 1e6 / pk["hbm_gbs"], 4)}
+    P, T, H, D = 8, 65536, 32, 128
+    po = torch.randn((P, T, H, D), device=dev).to(torch.bfloat16)
+    pl = torch.randn((P, T, H), device=dev)
+    out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    cm_ms = _time_ms(lambda: swa.lse_combine(po, pl, out=out, out_lse=lse), flush=flush)
+    cm_bytes = P * T * H * (D * 2 + 4) + T * H * (D * 2 + 4)
+    res["lse_combine_T65536_P8"] = {"ms": round(cm_ms, 4), "gbs": round(cm_bytes / cm_ms / 1e6, 1),
+                                    "frac_of_hbm": round(cm_bytes / cm_ms / 1e6 / pk["hbm_gbs"], 4)}
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -402,6 +524,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads and bandwidth sweeps")
     ap.add_argument("--requests", type=int, default=4, choices=[1, 2, 3, 4],
                     help="Gemma-like requests per step (4 = the benchmark; fewer = profiling case)")
     args = ap.parse_args()

@@ -169,8 +169,9 @@ int swa_tile_bounds(const int32_t *query_start_loc, const int32_t *seq_lens,
  *   partial_out/partial_lse  required when num_splits > 1, else ignored
  * Host errors: NULL pointers, non-positive sizes, Hq % Hkv != 0, an unsupported
  *   dtype/head_dim/block_size, misaligned (not 16-byte) q/k/v/out pointers.
- * Device errors: SWA_ERR_BLOCK_ID (the page is treated as all-invisible),
- *   SWA_ERR_LENS, SWA_ERR_SPLITS, SWA_ERR_TIMEOUT.
+ * Device errors: SWA_ERR_BLOCK_ID (rows that see such a page get unspecified
+ *   but finite outputs), SWA_ERR_LENS and SWA_ERR_QSL (the sequence's rows are
+ *   not written), SWA_ERR_SPLITS, SWA_ERR_TIMEOUT, SWA_ERR_INTERNAL.
  */
 int swa_mm_paged_attention(const void *q, const void *k_cache, const void *v_cache,
                            int64_t num_blocks, const int32_t *block_table,
