@@ -161,8 +161,10 @@ int swa_tile_bounds(const int32_t *query_start_loc, const int32_t *seq_lens,
  *   seq_lens              int32[num_seqs]
  *   context_lens          int32[num_seqs] or NULL (derived)
  *   mm_ranges             int32[num_seqs, max_mm_ranges, 2] or NULL
- *   max_query_len         host-side upper bound of the query lengths (selects
- *                         the decode or prefill kernel; any value >= 1 is safe)
+ *   max_query_len         host-side upper bound of every query length (it
+ *                         selects the decode or the prefill kernel; a value
+ *                         below a sequence's query length sets SWA_ERR_LENS
+ *                         for that sequence in the decode kernel)
  *   head_dim              64, 128 or 256;  block_size 16, 32, 64 or 128
  *   out                   [num_tokens, Hq, D] same dtype as q  (num_splits == 1)
  *   lse                   fp32 [num_tokens, Hq] or NULL          (num_splits == 1)

@@ -147,6 +147,38 @@ def test_split_partials_and_merge(seed, err):
     assert err.item() == 0
 
 
+@pytest.mark.parametrize("D,G,max_q,P,window,ranges", [
+    (128, 4, 1, 32, 0, False), (128, 4, 1, 1, 0, False), (64, 2, 2, 4, 100, True),
+    (256, 1, 4, 3, 0, True), (128, 2, 1, 8, 37, False), (256, 4, 1, 5, 300, True),
+    (64, 1, 3, 1, 0, True), (128, 4, 1, 16, 1, False)])
+def test_decode_kernel_cases(D, G, max_q, P, window, ranges, err):
+    """Few query tokens per sequence (the decode path), split or not, all rows."""
+    from paged_sliding_window_swa_gb300 import lse_combine
+    lay = W.random_small(300 + D + G + P, head_dim=D, group=G, max_seqs=4, max_ctx=3000, max_q=max_q,
+                         window=window, with_ranges=ranges, num_splits=P)
+    q, k, v, d = gpu_inputs(lay, poison=True)
+    rows = _all_rows(lay)
+    res = run_attention(lay, q, k, v, d, err=err)
+    if P > 1:
+        po, pl = res
+        ro, rl = oracle_rows(lay, q, k, v, rows, num_splits=P)
+        pof, plc = po.float().cpu().numpy(), pl.cpu().numpy()
+        for (p, t, h), val in ro.items():
+            if rl[(p, t, h)] == -np.inf:
+                assert plc[p, t, h] == -np.inf
+            else:
+                assert abs(plc[p, t, h] - rl[(p, t, h)]) <= LSE_ATOL
+                assert np.abs(pof[p, t, h] - val).max() <= atol_for(lay)
+        out, lse = lse_combine(po, pl)
+    else:
+        out, lse = res
+    uo, ul = oracle_rows(lay, q, k, v, rows)
+    e_out, e_lse = max_errors(out, lse, uo, ul, rows)
+    assert e_out <= atol_for(lay) and e_lse <= LSE_ATOL
+    torch.cuda.synchronize()
+    assert err.item() == 0
+
+
 def test_decode_split_kv_sampled(err):
     """128 single-token queries over 4k-64k contexts, 8-32 partitions, merged."""
     from paged_sliding_window_swa_gb300 import lse_combine
