@@ -3,36 +3,39 @@
 // #53147 summary, implementation items 1-2 and the compute_tile_loop_bounds
 // excerpt).
 //
-// One CTA = one 128-row query tile: BQ = 128 / G query positions x the G query
-// heads of one kv head (GQA packing -- every K/V tile is staged once for the
-// whole group).  The key loop walks 128-key tiles over the union of the rows'
-// visible intervals (the pruned tile range of the union formula).
+// Persistent: one CTA per SM walks its share of the work items.  An item is
+// one 128-row query tile -- 128 / G query positions x the G query heads of one
+// kv head (GQA packing: every K/V tile is staged once for the whole group) --
+// and its key loop covers the 128-key tiles of the union of its rows' visible
+// intervals (the pruned tile range of the union formula).  All roles walk the
+// same item sequence, compute each item's tile range themselves, and count
+// tiles, K/V units and exchanges globally, so the rings, the S buffers and
+// every barrier phase simply continue from one item to the next: the next
+// item's Q copy and first two QK MMAs overlap the current item's tail.
 //
-// Shared memory: the Q tile (TMA, 128-byte swizzled, K-major) and two rings of
-// 32 KB units (for head_dim 256; 16 KB for 128): a K unit holds one half of
-// head_dim for all 128 keys of a tile, a V unit holds all of head_dim for one
-// 64-key half of a tile.  So QK_j consumes two K units and PV_j two V units,
-// and each unit is recycled as soon as its half of the MMA work is done.
-// TMEM (512 columns): O [0, D), S buffers [D, D+128) and [D+128, D+256) in
-// fp32; the softmax overwrites the front half of S_j with P_j as bf16 pairs,
-// which the PV MMA reads as its A operand.
+// Shared memory: the Q tile (TMA, 128-byte swizzled, K-major) and two rings
+// of 32 KB units (for head_dim 256; 16 KB for 128): a K unit holds one half of
+// head_dim for all 128 keys of a tile, a V unit all of head_dim for one
+// 64-key half of a tile, so QK consumes two K units and PV two V units and
+// each is recycled as soon as its half of the MMA work is done.  TMEM (512
+// columns): O [0, D) and two S buffers of 128 fp32 columns; the softmax
+// overwrites the front of S with P as bf16 pairs, the A operand of PV.
 //
 // Eleven warps:
-//   warp 0     K producer, warp 10 V producer: every lane resolves the cache
-//              slot of one page box through the block table (32 boxes per
-//              batch, one batch ahead) and one warp instruction issues a whole
-//              unit's boxes (one per page and 64-column chunk); pages past the
-//              sequence or with a bad block id are read from outside the
-//              tensor, which the TMA fills with 0.  Thread 0 copies Q as soon
-//              as the barriers exist.
-//   warp 1     tcgen05 issuer and TMEM owner: QK_0, QK_1, then per tile
-//              PV_j (once P_j is written) and QK_{j+2}.
+//   warp 0     Q and K producer, warp 10 V producer: every lane resolves the
+//              cache slot of one page box through the block table (32 boxes
+//              per batch, one batch ahead) and one warp instruction issues a
+//              whole unit (one box per page and 64-column chunk); pages past
+//              the sequence or with a bad block id are read from outside the
+//              tensor, which the TMA fills with 0.
+//   warp 1     tcgen05 issuer and TMEM owner: QK runs two tiles ahead of PV
+//              along the CTA's flat tile stream.
 //   warps 2-9  softmax, two warpgroups: thread i of each owns row i (TMEM lane
-//              i) and one half of the tile's columns; the half-row maxima are
-//              exchanged through shared memory once per tile.  Masks only tiles
-//              not fully inside the row's visible interval, keeps the running
-//              max in the log2 domain and rescales O in TMEM only when the max
-//              grows by more than 2^8, and at the end normalises its half of O.
+//              i) and one half of the tile's columns; half-row maxima meet in
+//              shared memory once per tile.  Masks only tiles not fully inside
+//              the row's interval, keeps the running max in the log2 domain,
+//              rescales O in TMEM only when the max grows by more than 2^8, and
+//              at the end of an item normalises and stores its half of O.
 // Every mbarrier wait is bounded in time; on expiry the CTA sets
 // SWA_ERR_TIMEOUT, drains its own TMA loads and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -47,24 +50,23 @@ namespace {
 using namespace tc;
 
 constexpr uint64_t kWaitLimitNs = 200000000ull;    // 200 ms per wait: far above any real stall
-constexpr int kMaxSmemRanges = 64;                 // image ranges staged in shared memory
 constexpr int kMaxUnits = 8;                       // ring slots per operand
 
 template <int D_, int KSU_, int VSU_>
 struct Cfg {
   static constexpr int D = D_;          // head dim
   static constexpr int N = 128;         // keys per tile
-  static constexpr int M = 128;         // query rows per CTA
+  static constexpr int M = 128;         // query rows per item
   static constexpr int CH = D / 64;     // 128-byte column chunks per row
   static constexpr int KSU = KSU_;      // K ring slots (units)
   static constexpr int VSU = VSU_;      // V ring slots (units)
   static constexpr int Q_CHUNK = M * 128;
   static constexpr int Q_BYTES = M * D * 2;
-  static constexpr int UNIT = N * D;                 // bytes of a K or V unit (= 64 keys x D x 2)
+  static constexpr int UNIT = N * D;                 // bytes of a K or V unit
   static constexpr int KU_CH = CH / 2;               // chunks per K unit (half of head_dim)
-  static constexpr int KU_CHUNK = N * 128;           // bytes per chunk in a K unit (128 keys)
+  static constexpr int KU_CHUNK = N * 128;           // bytes per chunk of a K unit (128 keys)
   static constexpr int VU_KEYS = N / 2;              // keys per V unit
-  static constexpr int VU_CHUNK = VU_KEYS * 128;     // bytes per chunk in a V unit
+  static constexpr int VU_CHUNK = VU_KEYS * 128;     // bytes per chunk of a V unit
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = Q_BYTES;
   static constexpr int OFF_V = OFF_K + KSU * UNIT;
@@ -80,25 +82,167 @@ struct Cfg {
 };
 
 struct Ctrl {
-  float red[2][2][128];                  // half-row max (and, at the end, sum) exchange buffers
-  int32_t ranges[2 * kMaxSmemRanges];
-  uint64_t q_full;
+  float red[2][2][128];                  // half-row max / row-sum exchange buffers
+  uint64_t q_full, q_empty;
   uint64_t k_full[kMaxUnits], k_empty[kMaxUnits], v_full[kMaxUnits], v_empty[kMaxUnits];
   uint64_t s_full[2], p_full[2];
   uint64_t o_full, drain;
-  uint64_t xch[2], xl;                   // exchange barriers of the two softmax warpgroups
+  uint64_t xch[2];                       // exchanges between the two softmax warpgroups
   uint32_t tmem_base;
   int abort;
-  int kmin, kmax;
 };
 
 template <class C>
 constexpr int smem_bytes() { return C::OFF_CTRL + (int)sizeof(Ctrl); }
 
+struct Item {
+  int s, hk, qstart, qlen, qpos_lo, seq_len, ctx;
+  int q_lo, q_hi;                        // absolute positions of the block's first and last rows
+};
+
+// Item -> (query block, kv head).  False for blocks past their sequence's
+// query length (nothing to do) and for inconsistent metadata (err bits set).
+__device__ inline bool decode_item(const AttnArgs &a, int item, int bq, Item &it, int32_t &errbits) {
+  const int bx = item / a.hkv;
+  it.hk = item - bx * a.hkv;
+  it.s = find_seq(a.qsl, a.num_seqs, bx, bq);
+  const int64_t first = (int64_t)__ldg(a.qsl + it.s) / bq + it.s;
+  const int local = (int)(bx - first);
+  it.qstart = __ldg(a.qsl + it.s);
+  it.qlen = __ldg(a.qsl + it.s + 1) - it.qstart;
+  it.qpos_lo = local * bq;
+  errbits = 0;
+  if (local < 0 || it.qpos_lo >= it.qlen) return false;
+  if (it.qstart < 0 || (int64_t)it.qstart + it.qlen > a.num_tokens) {
+    errbits = SWA_ERR_QSL;
+    return false;
+  }
+  it.seq_len = __ldg(a.seq_lens + it.s);
+  it.ctx = it.seq_len - it.qlen;
+  if (it.ctx < 0 || (a.ctx_lens != nullptr && __ldg(a.ctx_lens + it.s) != it.ctx)) {
+    errbits = SWA_ERR_LENS;
+    return false;
+  }
+  it.q_lo = it.ctx + it.qpos_lo;
+  it.q_hi = it.ctx + min(it.qpos_lo + bq - 1, it.qlen - 1);
+  return true;
+}
+
+// The union of the block's rows' visible intervals: left edge of the first
+// row's window, right edge the larger of the last row's window and the end of
+// every valid image range that meets the block (largest such end: `emax`, -1
+// if none), clamped to the sequence.  A range meets the block exactly when it
+// holds one of its rows, so this equals the union of the per-row intervals.
+__device__ inline void union_keys(const AttnArgs &a, const Item &it, int emax, int &kmin, int &kmax) {
+  int lo, hi;
+  if (a.window > 0) {
+    lo = max(0, it.q_lo - a.window + 1);
+    hi = a.causal ? it.q_hi : it.q_hi + a.window - 1;
+  } else {
+    lo = 0;
+    hi = a.causal ? it.q_hi : it.seq_len - 1;
+  }
+  kmin = lo;
+  kmax = min(max(hi, emax), it.seq_len - 1);
+}
+
+// Ranges scanned by lanes `start`, `start + step`, ...; `warp_reduce`
+// combines the lanes.
+__device__ inline void block_keys(const AttnArgs &a, const Item &it, int start, int step, bool warp_reduce,
+                                  int &kmin, int &kmax) {
+  int emax = -1;
+  if (a.mm_ranges != nullptr) {
+    const int32_t *rg = a.mm_ranges + (int64_t)it.s * a.max_mm_ranges * 2;
+    for (int i = start; i < a.max_mm_ranges; i += step) {
+      const int s0 = __ldg(rg + 2 * i), e0 = __ldg(rg + 2 * i + 1);
+      if (s0 < e0 && s0 <= it.q_hi && e0 >= it.q_lo) emax = max(emax, e0);
+    }
+  }
+  if (warp_reduce) emax = __reduce_max_sync(0xffffffffu, emax);
+  union_keys(a, it, emax, kmin, kmax);
+}
+
+// Next valid item of this CTA's stream after `item` (false at the end).
+__device__ inline bool next_item(const AttnArgs &a, int &item, int stride, int n_items, int bq, Item &it) {
+  for (item += stride; item < n_items; item += stride) {
+    int32_t eb;
+    if (decode_item(a, item, bq, it, eb)) return true;
+  }
+  return false;
+}
+
+// What a softmax thread needs for one item: the item's tile range and its
+// row's visible interval [klo, khi] (empty for rows past the query length).
+struct RowSetup {
+  Item it;
+  int tile_lo, n_tiles;
+  int klo, khi;
+  int64_t out_row;
+  bool row_valid;
+};
+
+// One pass of the warp over the sequence's ranges yields both the block union
+// and every lane's own interval: a range is tested against the warp's 32 rows
+// only when it meets their span (ballot), which is rarely more than once.
+// Same rule as the visible interval of a single query: a valid range holding q
+// moves the right edge to its end.
+template <int N>
+__device__ inline void row_setup(const AttnArgs &a, const Item &it, int row, int G, int lane, RowSetup &rs) {
+  rs.it = it;
+  const int wrow0 = row - lane;
+  const int wq_lo = it.ctx + it.qpos_lo + wrow0 / G;
+  const int wq_hi = it.ctx + it.qpos_lo + (wrow0 + 31) / G;
+  const int qpos = it.qpos_lo + row / G;
+  const int q = it.ctx + qpos;
+  int emax = -1, rhi = -1;
+  if (a.mm_ranges != nullptr) {
+    const int32_t *rg = a.mm_ranges + (int64_t)it.s * a.max_mm_ranges * 2;
+    for (int b = 0; b < a.max_mm_ranges; b += 32) {
+      int s0 = 0, e0 = -1;
+      if (b + lane < a.max_mm_ranges) {
+        s0 = __ldg(rg + 2 * (b + lane));
+        e0 = __ldg(rg + 2 * (b + lane) + 1);
+      }
+      const bool valid = s0 < e0;
+      if (valid && s0 <= it.q_hi && e0 >= it.q_lo) emax = max(emax, e0);
+      uint32_t m = __ballot_sync(0xffffffffu, valid && s0 <= wq_hi && e0 >= wq_lo);
+      while (m != 0) {
+        const int src = __ffs(m) - 1;
+        m &= m - 1;
+        const int s1 = __shfl_sync(0xffffffffu, s0, src), e1 = __shfl_sync(0xffffffffu, e0, src);
+        if (s1 <= q && q <= e1) rhi = max(rhi, e1);
+      }
+    }
+    emax = __reduce_max_sync(0xffffffffu, emax);
+  }
+  int kmin, kmax;
+  union_keys(a, it, emax, kmin, kmax);
+  rs.tile_lo = kmin / N;
+  rs.n_tiles = kmax / N - rs.tile_lo + 1;
+  rs.row_valid = qpos < it.qlen;
+  if (rs.row_valid) {
+    int lo, hi;
+    if (a.window > 0) {
+      lo = max(0, q - a.window + 1);
+      hi = a.causal ? q : q + a.window - 1;
+    } else {
+      lo = 0;
+      hi = a.causal ? q : it.seq_len - 1;
+    }
+    rs.klo = lo;
+    rs.khi = min(max(hi, rhi), it.seq_len - 1);
+    rs.out_row = (int64_t)(it.qstart + qpos) * a.hq + it.hk * G + row % G;
+  } else {
+    rs.klo = 1;
+    rs.khi = 0;
+    rs.out_row = 0;
+  }
+}
+
 template <class C>
 __global__ void __launch_bounds__(352, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const int G) {
+               const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const int G, const int n_items) {
   // Everything lives in dynamic shared memory, which starts 1024-byte aligned
   // when a kernel has no static shared data (checked below): the 128-byte
   // swizzled tiles need that alignment and there is no room for slack.
@@ -111,36 +255,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bq = C::M / G;
-  const int hk = blockIdx.y;
-
-  // ---- which sequence / query block (uniform over the CTA) ----
-  const int s = find_seq(a.qsl, a.num_seqs, blockIdx.x, bq);
-  const int64_t first_blk = (int64_t)__ldg(a.qsl + s) / bq + s;
-  const int local = (int)(blockIdx.x - first_blk);
-  const int qstart = __ldg(a.qsl + s);
-  const int qlen = __ldg(a.qsl + s + 1) - qstart;
-  const int qpos_lo = local * bq;
-  if (local < 0 || qpos_lo >= qlen) return;
-  if (qstart < 0 || (int64_t)qstart + qlen > a.num_tokens) {
-    if (threadIdx.x == 0) report(a.err, SWA_ERR_QSL);
-    return;
-  }
-  const int seq_len = __ldg(a.seq_lens + s);
-  const int ctx = seq_len - qlen;
-  if (ctx < 0 || (a.ctx_lens != nullptr && __ldg(a.ctx_lens + s) != ctx)) {
-    if (threadIdx.x == 0) report(a.err, SWA_ERR_LENS);
-    return;
-  }
   if ((dsm & 1023u) != 0) {
     if (threadIdx.x == 0) report(a.err, SWA_ERR_INTERNAL);
     return;
   }
-
   if (threadIdx.x == 0) {
     ctl.abort = 0;
-    ctl.kmin = INT_MAX;
-    ctl.kmax = -1;
     mbar_init(smem_u32(&ctl.q_full), 1);
+    mbar_init(smem_u32(&ctl.q_empty), 1);
     for (int i = 0; i < C::KSU; ++i) {
       mbar_init(smem_u32(&ctl.k_full[i]), 1);
       mbar_init(smem_u32(&ctl.k_empty[i]), 1);
@@ -154,50 +276,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(smem_u32(&ctl.p_full[i]), 256);
       mbar_init(smem_u32(&ctl.xch[i]), 256);
     }
-    mbar_init(smem_u32(&ctl.xl), 256);
     mbar_init(smem_u32(&ctl.o_full), 1);
     mbar_init(smem_u32(&ctl.drain), 1);
     mbar_fence_init();
-    // the Q copy depends only on the block's first token: start it right away
     tma_prefetch_map(&tm_q);
     tma_prefetch_map(&tm_k);
     tma_prefetch_map(&tm_v);
-    mbar_expect_tx(smem_u32(&ctl.q_full), C::Q_BYTES);
-    for (int c = 0; c < C::CH; ++c)
-      tma_load_3d(q_s + c * C::Q_CHUNK, &tm_q, c * 64, hk * G, qstart + qpos_lo, smem_u32(&ctl.q_full));
-  }
-  // this sequence's image ranges, staged once for the 256 interval evaluations
-  const int nr = a.mm_ranges ? a.max_mm_ranges : 0;
-  const bool ranges_in_smem = nr <= kMaxSmemRanges;
-  const int32_t *ranges_g = a.mm_ranges ? a.mm_ranges + (int64_t)s * a.max_mm_ranges * 2 : nullptr;
-  if (warp == 1 && ranges_in_smem)
-    for (int i = lane; i < 2 * nr; i += 32) ctl.ranges[i] = __ldg(ranges_g + i);
-  __syncthreads();
-
-  // ---- each softmax thread: its row's visible interval; the CTA's union ----
-  const bool is_softmax = warp >= 2 && warp < 10;
-  const int row = 32 * (warp & 3) + lane;            // TMEM lane of this thread
-  int klo = 1, khi = 0;
-  bool row_valid = false;
-  int64_t out_row = 0;
-  if (is_softmax) {
-    const int qpos = qpos_lo + row / G;
-    row_valid = qpos < qlen;
-    int red_lo = INT_MAX, red_hi = -1;
-    if (row_valid) {
-      const Span sp = visible_span(ctx + qpos, seq_len, a.window, a.causal != 0,
-                                   ranges_in_smem ? ctl.ranges : ranges_g, nr);
-      klo = sp.lo;
-      khi = sp.hi;
-      out_row = (int64_t)(qstart + qpos) * a.hq + hk * G + row % G;
-      if (klo <= khi) { red_lo = klo; red_hi = khi; }
-    }
-    red_lo = __reduce_min_sync(0xffffffffu, red_lo);
-    red_hi = __reduce_max_sync(0xffffffffu, red_hi);
-    if (lane == 0) {
-      atomicMin(&ctl.kmin, red_lo);
-      atomicMax(&ctl.kmax, red_hi);
-    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl.tmem_base), C::TM_COLS);
@@ -207,33 +291,52 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
-  const int kmin = ctl.kmin, kmax = ctl.kmax;
-  const int tile_lo = kmax >= kmin ? kmin / C::N : 0;
-  const int n_tiles = kmax >= kmin ? kmax / C::N - tile_lo + 1 : 0;
   volatile int *abort_flag = &ctl.abort;
   const volatile int32_t *gerr = a.err;
+  const int stride = gridDim.x;
 
   if (warp == 0 || warp == 10) {
     // =============================== TMA producers ==============================
     const bool is_v = warp == 10;
     const int SU = is_v ? C::VSU : C::KSU;
-    const int n_units = 2 * n_tiles;               // unit u = 2*tile + half
-    int issued = 0;
+    const CUtensorMap *map = is_v ? &tm_v : &tm_k;
+    const int unit_keys = is_v ? C::VU_KEYS : C::N;     // K units: 128 keys, V units: 64 keys
+    const int R = min(a.block_size, unit_keys);         // rows per box
+    const int boxes = unit_keys / R;                    // boxes per unit (per chunk)
+    const int uch = is_v ? C::CH : C::KU_CH;            // chunks per unit
+    const int oob = (int)(a.num_blocks * a.block_size);
+    int64_t u_base = 0;                                 // units issued by this warp before this item
+    int ord = 0;                                        // valid items so far
     bool ok = true;
-    if (n_tiles > 0) {
-      // K units cover 128 keys, V units 64 keys; a box is one page (or a
-      // 128-key part of a bigger page)
-      const int unit_keys = is_v ? C::VU_KEYS : C::N;
-      const int R = min(a.block_size, unit_keys);    // rows per box
-      const int boxes = unit_keys / R;               // boxes per unit (per chunk)
-      const int uch = is_v ? C::CH : C::KU_CH;       // chunks per unit
+    for (int item = blockIdx.x; ok && item < n_items; item += stride) {
+      Item it;
+      int32_t eb;
+      if (!decode_item(a, item, bq, it, eb)) {
+        if (eb != 0 && !is_v && lane == 0) report(a.err, eb);
+        continue;
+      }
+      int kmin, kmax;
+      block_keys(a, it, lane, 32, true, kmin, kmax);
+      const int tile_lo = kmin / C::N;
+      const int n_tiles = kmax / C::N - tile_lo + 1;
+      if (!is_v && lane == 0) {
+        // Q: the previous item's last QK has to be done with the buffer
+        if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, gerr, kWaitLimitNs);
+        if (ok) {
+          mbar_expect_tx(smem_u32(&ctl.q_full), C::Q_BYTES);
+          for (int c = 0; c < C::CH; ++c)
+            tma_load_3d(q_s + c * C::Q_CHUNK, &tm_q, c * 64, it.hk * G, it.qstart + it.qpos_lo,
+                        smem_u32(&ctl.q_full));
+        }
+      }
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      ++ord;                                            // items whose Q copy was issued
       const int total_boxes = (n_tiles * C::N) / R;
-      const int oob = (int)(a.num_blocks * a.block_size);
-      const int32_t *bt = a.block_table + (int64_t)s * a.bt_stride;
-      auto resolve = [&](int b) -> int {           // slot of the first key of box b
+      const int32_t *bt = a.block_table + (int64_t)it.s * a.bt_stride;
+      auto resolve = [&](int b) -> int {                // slot of the first key of box b
         const int k = tile_lo * C::N + b * R;
         int slot = oob;
-        if (b < total_boxes && k < seq_len) {
+        if (b < total_boxes && k < it.seq_len) {
           const int page = k / a.block_size;
           const int32_t blk = page < a.bt_stride ? __ldg(bt + page) : -1;
           if (blk >= 0 && blk < a.num_blocks) slot = blk * a.block_size + (k - page * a.block_size);
@@ -243,111 +346,162 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       };
       int batch = 0;
       int prv = oob, cur = resolve(lane), nxt = resolve(32 + lane);
-      auto advance = [&](int b_max) {               // warp-uniform
-        while (b_max >= (batch + 1) * 32) {
-          prv = cur;
-          cur = nxt;
-          ++batch;
-          nxt = resolve((batch + 1) * 32 + lane);
+      int ul = 0;
+      for (; ul < 2 * n_tiles; ++ul) {                 // unit ul of this item: tile ul/2, half ul%2
+        const int64_t u = u_base + ul;
+        const int slot_i = (int)(u % SU);
+        if (u >= SU) {
+          const uint32_t empty = smem_u32(is_v ? &ctl.v_empty[slot_i] : &ctl.k_empty[slot_i]);
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(empty, (uint32_t)(((u / SU) - 1) & 1), abort_flag, gerr, kWaitLimitNs));
+          if (!ok) break;
         }
-      };
-      auto slot_lane = [&](int b) -> int {          // per-lane b: current batch, or the one before
-        const int from_cur = __shfl_sync(0xffffffffu, cur, (b - batch * 32) & 31);
-        const int from_prv = __shfl_sync(0xffffffffu, prv, (b - (batch - 1) * 32) & 31);
-        return b >= batch * 32 ? from_cur : from_prv;
-      };
-      const CUtensorMap *map = is_v ? &tm_v : &tm_k;
-      auto issue = [&](int u) {
-        const int t = u >> 1, half = u & 1, slot_i = u % SU;
+        const int t = ul >> 1, half = ul & 1;
         const uint32_t full = smem_u32(is_v ? &ctl.v_full[slot_i] : &ctl.k_full[slot_i]);
         const uint32_t dst = (is_v ? v_s : k_s) + slot_i * C::UNIT;
         if (lane == 0) mbar_expect_tx(full, C::UNIT);
         __syncwarp();
         // K: unit = head_dim half `half` of tile t's 128 keys; V: key half `half`
         const int b0 = is_v ? (2 * t + half) * boxes : t * boxes;
-        advance(b0 + boxes - 1);
+        while (b0 + boxes - 1 >= (batch + 1) * 32) {    // warp-uniform batch advance
+          prv = cur;
+          cur = nxt;
+          ++batch;
+          nxt = resolve((batch + 1) * 32 + lane);
+        }
         const int i = min(lane / uch, boxes - 1), c = lane % uch;
-        const int slot = slot_lane(b0 + i);
+        const int b = b0 + i;
+        const int from_cur = __shfl_sync(0xffffffffu, cur, (b - batch * 32) & 31);
+        const int from_prv = __shfl_sync(0xffffffffu, prv, (b - (batch - 1) * 32) & 31);
+        const int slot = b >= batch * 32 ? from_cur : from_prv;
         const int x = (is_v ? c : half * C::KU_CH + c) * 64;
         const uint32_t d = dst + c * (is_v ? C::VU_CHUNK : C::KU_CHUNK) + i * R * 128;
-        if (lane < boxes * uch) tma_load_3d(d, map, x, hk, slot, full);
-      };
-      // fill the ring, then refill a slot as soon as its half of QK (for K) or
-      // of PV (for V) has finished with it
-      issued = min(SU, n_units);
-      for (int u = 0; u < issued; ++u) issue(u);
-      for (int u = SU; u < n_units; ++u) {
-        const uint32_t empty = smem_u32(is_v ? &ctl.v_empty[u % SU] : &ctl.k_empty[u % SU]);
-        ok = __all_sync(0xffffffffu, mbar_wait(empty, ((u / SU) - 1) & 1, abort_flag, gerr, kWaitLimitNs));
-        if (!ok) break;
-        issue(u);
-        issued = u + 1;
+        if (lane < boxes * uch) tma_load_3d(d, map, x, it.hk, slot, full);
       }
-      if (!ok && lane == 0) {
-        *abort_flag = 1;
-        report(a.err, SWA_ERR_TIMEOUT);
-      }
+      u_base += ul;                                     // units issued (all of them unless aborted)
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      report(a.err, SWA_ERR_TIMEOUT);
     }
     // drain: every load issued by this warp must have landed before the CTA exits
     if (lane == 0) {
-      for (int u = max(0, issued - SU); u < issued; ++u)
-        mbar_wait(smem_u32(is_v ? &ctl.v_full[u % SU] : &ctl.k_full[u % SU]), (u / SU) & 1, nullptr, nullptr,
-                  kWaitLimitNs);
-      if (!is_v) mbar_wait(smem_u32(&ctl.q_full), 0, nullptr, nullptr, kWaitLimitNs);
+      for (int64_t u = max((int64_t)0, u_base - SU); u < u_base; ++u)
+        mbar_wait(smem_u32(is_v ? &ctl.v_full[u % SU] : &ctl.k_full[u % SU]), (uint32_t)((u / SU) & 1), nullptr,
+                  nullptr, kWaitLimitNs);
+      if (!is_v && ord > 0) mbar_wait(smem_u32(&ctl.q_full), (ord - 1) & 1, nullptr, nullptr, kWaitLimitNs);
     }
   } else if (warp == 1) {
     // =============================== MMA issuer =================================
-    if (lane == 0 && n_tiles > 0) {
-      bool ok = mbar_wait(smem_u32(&ctl.q_full), 0, abort_flag, gerr, kWaitLimitNs);
-      tc_fence_after();
-      auto issue_qk = [&](int j) -> bool {
-        const uint32_t d = tmem + C::TM_S + (j & 1) * C::N;
-        for (int half = 0; half < 2; ++half) {
-          const int u = 2 * j + half, slot = u % C::KSU;
-          if (!mbar_wait(smem_u32(&ctl.k_full[slot]), (u / C::KSU) & 1, abort_flag, gerr, kWaitLimitNs))
-            return false;
-          tc_fence_after();
+    if (lane == 0) {
+      // Event-driven issue: the tensor pipe queues only a few instructions, so
+      // any wait of this thread while work is ready elsewhere is lost MMA
+      // time.  Each pass polls the next PV half (needs P_t and its V unit) and
+      // the next QK half (needs its K unit, the item's Q, and S buffer t & 1
+      // free: PV_{t-2} issued -- tcgen05 ops from one thread run in issue
+      // order) and issues whichever is ready, PV first.
+      bool ok = true;
+      // QK cursor over the item stream; it records every item's tile count for PV
+      int qk_item = blockIdx.x - stride, qk_ord = -1, qk_j = 0, qk_n = 0, qk_half = 0;
+      bool qk_done = false, qk_q_ok = false;
+      int64_t qk_t = 0;                                  // tiles whose QK is fully issued
+      int ring_n[4];
+      int pushed = 0, popped = 0;
+      // PV cursor
+      int64_t pv_t = 0;
+      int pv_j = 0, pv_n = 0, pv_half = 0;
+      bool pv_p_ok = false;
+      uint64_t stall_t0 = 0;
+      uint32_t spins = 0;
+      while (true) {
+        bool progressed = false;
+        if (pv_n == 0 && popped < pushed) {
+          pv_n = ring_n[popped & 3];
+          pv_j = 0;
+        }
+        if (pv_n > 0 && pv_t < qk_t) {
+          if (!pv_p_ok) pv_p_ok = mbar_test_wait(smem_u32(&ctl.p_full[pv_t & 1]), (uint32_t)((pv_t >> 1) & 1));
+          const int64_t u = 2 * pv_t + pv_half;
+          const int slot = (int)(u % C::VSU);
+          if (pv_p_ok && mbar_test_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1))) {
+            tc_fence_after();
+            const uint32_t p_t = tmem + C::TM_S + (uint32_t)(pv_t & 1) * C::N;
 #pragma unroll
-          for (int kk = 0; kk < C::D / 32; ++kk) {     // 16-column steps over this half of head_dim
-            const uint32_t off = (kk & 3) * 32;         // inside the 128-byte swizzle row
-            const int cl = kk >> 2;                     // chunk within the unit
-            const uint64_t ad = smem_desc_sw128(q_s + (half * C::KU_CH + cl) * C::Q_CHUNK + off, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(k_s + slot * C::UNIT + cl * C::KU_CHUNK + off, 16, 1024);
-            mma_ss(d, ad, bd, C::IDESC_QK, (half > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < C::VU_KEYS / 16; ++kk) {
+              const uint64_t bd = smem_desc_sw128(v_s + slot * C::UNIT + kk * 16 * 128, C::VU_CHUNK, 1024);
+              mma_ts(tmem + C::TM_O, p_t + (pv_half * (C::VU_KEYS / 16) + kk) * 8, bd, C::IDESC_PV,
+                     (pv_j > 0 || pv_half > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&ctl.v_empty[slot]));
+            if (pv_half == 1) {
+              mma_commit(smem_u32(&ctl.o_full));
+              pv_half = 0;
+              pv_p_ok = false;
+              ++pv_t;
+              if (++pv_j == pv_n) {
+                ++popped;
+                pv_n = 0;
+              }
+            } else {
+              pv_half = 1;
+            }
+            progressed = true;
           }
-          mma_commit(smem_u32(&ctl.k_empty[slot]));
         }
-        mma_commit(smem_u32(&ctl.s_full[j & 1]));
-        return true;
-      };
-      // S buffer j & 1 last held P_{j-2}, whose PV was issued before QK_j;
-      // tcgen05 ops from one thread run in issue order
-      if (ok) ok = issue_qk(0);
-      if (ok && n_tiles > 1) ok = issue_qk(1);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (!mbar_wait(smem_u32(&ctl.p_full[j & 1]), (j >> 1) & 1, abort_flag, gerr, kWaitLimitNs)) {
-          ok = false;
-          break;
-        }
-        const uint32_t p_t = tmem + C::TM_S + (j & 1) * C::N;
-        for (int half = 0; half < 2 && ok; ++half) {
-          const int u = 2 * j + half, slot = u % C::VSU;
-          if (!mbar_wait(smem_u32(&ctl.v_full[slot]), (u / C::VSU) & 1, abort_flag, gerr, kWaitLimitNs)) {
-            ok = false;
-            break;
+        if (!qk_done && qk_t < pv_t + 2) {
+          if (qk_j == qk_n) {                            // enter the next valid item
+            Item it;
+            if (!next_item(a, qk_item, stride, n_items, bq, it)) {
+              qk_done = true;
+            } else {
+              int kmin, kmax;
+              block_keys(a, it, 0, 1, false, kmin, kmax);
+              qk_n = kmax / C::N - kmin / C::N + 1;
+              qk_j = 0;
+              ++qk_ord;
+              ring_n[pushed++ & 3] = qk_n;
+              qk_q_ok = false;
+            }
           }
-          tc_fence_after();
+          if (!qk_done) {
+            if (!qk_q_ok) qk_q_ok = mbar_test_wait(smem_u32(&ctl.q_full), qk_ord & 1);
+            const int64_t u = 2 * qk_t + qk_half;
+            const int slot = (int)(u % C::KSU);
+            if (qk_q_ok && mbar_test_wait(smem_u32(&ctl.k_full[slot]), (uint32_t)((u / C::KSU) & 1))) {
+              tc_fence_after();
+              const uint32_t d = tmem + C::TM_S + (uint32_t)(qk_t & 1) * C::N;
 #pragma unroll
-          for (int kk = 0; kk < C::VU_KEYS / 16; ++kk) {
-            const uint64_t bd = smem_desc_sw128(v_s + slot * C::UNIT + kk * 16 * 128, C::VU_CHUNK, 1024);
-            mma_ts(tmem + C::TM_O, p_t + (half * (C::VU_KEYS / 16) + kk) * 8, bd, C::IDESC_PV,
-                   (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < C::D / 32; ++kk) {  // 16-column steps over this half of head_dim
+                const uint32_t off = (kk & 3) * 32;      // inside the 128-byte swizzle row
+                const int cl = kk >> 2;                  // chunk within the unit
+                const uint64_t ad = smem_desc_sw128(q_s + (qk_half * C::KU_CH + cl) * C::Q_CHUNK + off, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(k_s + slot * C::UNIT + cl * C::KU_CHUNK + off, 16, 1024);
+                mma_ss(d, ad, bd, C::IDESC_QK, (qk_half > 0 || kk > 0) ? 1u : 0u);
+              }
+              mma_commit(smem_u32(&ctl.k_empty[slot]));
+              if (qk_half == 1) {
+                mma_commit(smem_u32(&ctl.s_full[qk_t & 1]));
+                if (qk_j == qk_n - 1) mma_commit(smem_u32(&ctl.q_empty));   // the item's Q is no longer read
+                qk_half = 0;
+                ++qk_t;
+                ++qk_j;
+              } else {
+                qk_half = 1;
+              }
+              progressed = true;
+            }
           }
-          mma_commit(smem_u32(&ctl.v_empty[slot]));
         }
-        if (!ok) break;
-        mma_commit(smem_u32(&ctl.o_full));
-        if (j + 2 < n_tiles && !issue_qk(j + 2)) { ok = false; break; }
+        if (qk_done && popped == pushed) break;          // every issued QK has had its PV
+        if (progressed) {
+          stall_t0 = 0;
+          spins = 0;
+        } else if ((++spins & 255u) == 0) {
+          if (*abort_flag || (*gerr & SWA_ERR_TIMEOUT)) { ok = false; break; }
+          const uint64_t now = global_ns();
+          if (stall_t0 == 0) stall_t0 = now;
+          else if (now - stall_t0 > kWaitLimitNs) { ok = false; break; }
+        }
       }
       if (!ok) {
         *abort_flag = 1;
@@ -357,7 +511,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mma_commit(smem_u32(&ctl.drain));
       mbar_wait(smem_u32(&ctl.drain), 0, nullptr, nullptr, kWaitLimitNs);
     }
-  } else if (is_softmax) {
+  } else {
     // =============================== softmax ====================================
     // Two warpgroups share every row: warpgroup h owns S columns
     // [h*N/2, (h+1)*N/2) and O columns [h*D/2, (h+1)*D/2).  Both keep the
@@ -367,151 +521,181 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     constexpr int DH = C::D / 2;
     const int h = (warp - 2) >> 2;
     const int sid = threadIdx.x - 64;                    // 0..255 over both warpgroups
+    const int row = 32 * (warp & 3) + lane;              // TMEM lane of this thread
     const uint32_t lane_t = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = a.scale * kLog2e;
-    float m_used = -INFINITY, l = 0.f;
+    int64_t t = 0;                                       // global tile index
+    int64_t xc = 0;                                      // exchanges so far (buffer xc & 1)
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int kt0 = (tile_lo + j) * C::N;
-      const int kc0 = kt0 + h * NH;                      // key of this warpgroup's first column
-      ok = mbar_wait(smem_u32(&ctl.s_full[j & 1]), (j >> 1) & 1, abort_flag, gerr, kWaitLimitNs);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t raw[NH];
-#pragma unroll
-      for (int c = 0; c < NH / 32; ++c)
-        tmem_ld32(tmem + lane_t + C::TM_S + (j & 1) * C::N + h * NH + 32 * c,
-                  *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
-      tmem_wait_ld();
-      float x[NH];
-      const bool full = klo <= kc0 && khi >= kc0 + NH - 1;
-      if (__all_sync(0xffffffffu, full)) {
-#pragma unroll
-        for (int c = 0; c < NH; ++c) x[c] = __uint_as_float(raw[c]) * sl2;
-      } else {
-#pragma unroll
-        for (int c = 0; c < NH; ++c)
-          x[c] = (kc0 + c >= klo && kc0 + c <= khi) ? __uint_as_float(raw[c]) * sl2 : -INFINITY;
-      }
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < NH; ++c) m4[c & 3] = fmaxf(m4[c & 3], x[c]);
-      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      ctl.red[j & 1][h][row] = mx;
-      mbar_arrive(smem_u32(&ctl.xch[j & 1]));
-      ok = mbar_wait(smem_u32(&ctl.xch[j & 1]), (j >> 1) & 1, abort_flag, gerr, kWaitLimitNs);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      mx = fmaxf(mx, ctl.red[j & 1][h ^ 1][row]);
-      const float m_new = fmaxf(m_used, mx);
-      const bool need = m_new > m_used + 8.f;             // also true on the first visible tile
-      // PV_{j-1} is confirmed exactly once per tile (here if O must be
-      // rescaled, else before P_j is published), so this thread is never more
-      // than one o_full phase behind and every parity wait is unambiguous.
-      bool pv_prev_done = (j == 0);
-      if (__any_sync(0xffffffffu, need)) {               // same decision in both warpgroups
-        const float m_next = need ? m_new : m_used;
-        const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_next);
-        if (j > 0) {
-          ok = mbar_wait(smem_u32(&ctl.o_full), (j - 1) & 1, abort_flag, gerr, kWaitLimitNs);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          pv_prev_done = true;
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < DH / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_t + C::TM_O + h * DH + 32 * c, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(tmem + lane_t + C::TM_O + h * DH + 32 * c, r);
-          }
-          tmem_wait_st();
-        }
-        l *= alpha;
-        m_used = m_next;
-      }
-      const float ms = (m_used == -INFINITY) ? 0.f : m_used;
-      uint32_t pk[NH / 2];
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < NH / 2; ++c) {
-        const float p0 = ex2(x[2 * c] - ms), p1 = ex2(x[2 * c + 1] - ms);
-        s4[c & 3] += p0 + p1;
-        pk[c] = pack_bf16(p0, p1);
-      }
-      l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-      if (!pv_prev_done) {
-        ok = mbar_wait(smem_u32(&ctl.o_full), (j - 1) & 1, abort_flag, gerr, kWaitLimitNs);
+    // The next item's setup (a few dependent global loads) is done while the
+    // current item's last PV runs.
+    int item = blockIdx.x - stride;
+    RowSetup cur;
+    bool have;
+    {
+      Item it;
+      have = next_item(a, item, stride, n_items, bq, it);
+      if (have) row_setup<C::N>(a, it, row, G, lane, cur);
+    }
+    while (ok && have) {
+      const Item &it = cur.it;
+      const int tile_lo = cur.tile_lo, n_tiles = cur.n_tiles;
+      const int klo = cur.klo, khi = cur.khi;
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < n_tiles; ++j, ++t) {
+        const int kt0 = (tile_lo + j) * C::N;
+        const int kc0 = kt0 + h * NH;                    // key of this warpgroup's first column
+        ok = mbar_wait(smem_u32(&ctl.s_full[t & 1]), (uint32_t)((t >> 1) & 1), abort_flag, gerr, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      }
-      if (kt0 + C::N > seq_len) {
-        // keys past the sequence end: their V rows may hold anything; zero
-        // them.  PV_{j-1} is done, so every earlier unit of each V slot has
-        // been consumed and the v_full parity below is unambiguous.
-        for (int half = 0; half < 2 && ok; ++half) {
-          const int k0 = kt0 + half * C::VU_KEYS;
-          if (k0 + C::VU_KEYS <= seq_len) continue;
-          const int u = 2 * j + half, slot = u % C::VSU;
-          ok = mbar_wait(smem_u32(&ctl.v_full[slot]), (u / C::VSU) & 1, abort_flag, gerr, kWaitLimitNs);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          const int r0 = max(0, seq_len - k0);
-          const int n16 = (C::VU_KEYS - r0) * 8 * C::CH;
-          for (int i = sid; i < n16; i += 256) {
-            const int c = i / ((C::VU_KEYS - r0) * 8), rem = i % ((C::VU_KEYS - r0) * 8);
-            uint4 *dst = reinterpret_cast<uint4 *>(dsm_ptr + C::OFF_V + slot * C::UNIT + c * C::VU_CHUNK +
-                                                   (r0 + rem / 8) * 128 + (rem % 8) * 16);
-            *dst = make_uint4(0, 0, 0, 0);
-          }
-        }
-        if (!ok) break;
-        fence_proxy_async_smem();
-      }
+        tc_fence_after();
+        uint32_t raw[NH];
 #pragma unroll
-      for (int c = 0; c < NH / 2; c += 32)
-        tmem_st32(tmem + lane_t + C::TM_S + (j & 1) * C::N + h * (NH / 2) + c,
-                  *reinterpret_cast<const uint32_t(*)[32]>(pk + c));
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&ctl.p_full[j & 1]));
-    }
-    if (ok && n_tiles > 0) {
-      ok = mbar_wait(smem_u32(&ctl.o_full), (n_tiles - 1) & 1, abort_flag, gerr, kWaitLimitNs);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      // full row sum = both halves; buffer n_tiles & 1 was last read at tile
-      // n_tiles - 2, before every thread passed the exchange of tile n_tiles - 1
-      ctl.red[n_tiles & 1][h][row] = l;
-      mbar_arrive(smem_u32(&ctl.xl));
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.xl), 0, abort_flag, gerr, kWaitLimitNs));
-      l += ctl.red[n_tiles & 1][h ^ 1][row];
-    }
-    if (!ok) {
-      *abort_flag = 1;
-      report(a.err, SWA_ERR_TIMEOUT);
-    } else {
+        for (int c = 0; c < NH / 32; ++c)
+          tmem_ld32(tmem + lane_t + C::TM_S + (uint32_t)(t & 1) * C::N + h * NH + 32 * c,
+                    *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
+        tmem_wait_ld();
+        float x[NH];
+        const bool full = klo <= kc0 && khi >= kc0 + NH - 1;
+        if (__all_sync(0xffffffffu, full)) {
+#pragma unroll
+          for (int c = 0; c < NH; ++c) x[c] = __uint_as_float(raw[c]) * sl2;
+        } else {
+#pragma unroll
+          for (int c = 0; c < NH; ++c)
+            x[c] = (kc0 + c >= klo && kc0 + c <= khi) ? __uint_as_float(raw[c]) * sl2 : -INFINITY;
+        }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < NH; ++c) m4[c & 3] = fmaxf(m4[c & 3], x[c]);
+        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        ctl.red[xc & 1][h][row] = mx;
+        mbar_arrive(smem_u32(&ctl.xch[xc & 1]));
+        ok = mbar_wait(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag, gerr, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        mx = fmaxf(mx, ctl.red[xc & 1][h ^ 1][row]);
+        ++xc;
+        const float m_new = fmaxf(m_used, mx);
+        const bool need = m_new > m_used + 8.f;           // also true on the first visible tile
+        // PV_{t-1} is confirmed exactly once per tile (here if O must be
+        // rescaled, else before P_t is published; for an item's first tile it
+        // was confirmed at the end of the previous item), so this thread is
+        // never more than one o_full phase behind.
+        bool pv_prev_done = (j == 0);
+        if (__any_sync(0xffffffffu, need)) {             // same decision in both warpgroups
+          const float m_next = need ? m_new : m_used;
+          const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_next);
+          if (j > 0) {
+            ok = mbar_wait(smem_u32(&ctl.o_full), (uint32_t)((t - 1) & 1), abort_flag, gerr, kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            pv_prev_done = true;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < DH / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(tmem + lane_t + C::TM_O + h * DH + 32 * c, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+              tmem_st32(tmem + lane_t + C::TM_O + h * DH + 32 * c, r);
+            }
+            tmem_wait_st();
+          }
+          l *= alpha;
+          m_used = m_next;
+        }
+        const float ms = (m_used == -INFINITY) ? 0.f : m_used;
+        uint32_t pk[NH / 2];
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < NH / 2; ++c) {
+          const float p0 = ex2(x[2 * c] - ms), p1 = ex2(x[2 * c + 1] - ms);
+          s4[c & 3] += p0 + p1;
+          pk[c] = pack_bf16(p0, p1);
+        }
+        l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        if (!pv_prev_done) {
+          ok = mbar_wait(smem_u32(&ctl.o_full), (uint32_t)((t - 1) & 1), abort_flag, gerr, kWaitLimitNs);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        }
+        if (kt0 + C::N > it.seq_len) {
+          // keys past the sequence end: their V rows may hold anything; zero
+          // them.  PV_{t-1} is done, so every earlier unit of each V slot has
+          // been consumed and the v_full parity below is unambiguous.
+          for (int half = 0; half < 2 && ok; ++half) {
+            const int k0 = kt0 + half * C::VU_KEYS;
+            if (k0 + C::VU_KEYS <= it.seq_len) continue;
+            const int64_t u = 2 * t + half;
+            const int slot = (int)(u % C::VSU);
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1),
+                                                   abort_flag, gerr, kWaitLimitNs));
+            if (!ok) break;
+            const int r0 = max(0, it.seq_len - k0);
+            const int n16 = (C::VU_KEYS - r0) * 8 * C::CH;
+            for (int i = sid; i < n16; i += 256) {
+              const int c = i / ((C::VU_KEYS - r0) * 8), rem = i % ((C::VU_KEYS - r0) * 8);
+              uint4 *dst = reinterpret_cast<uint4 *>(dsm_ptr + C::OFF_V + slot * C::UNIT + c * C::VU_CHUNK +
+                                                     (r0 + rem / 8) * 128 + (rem % 8) * 16);
+              *dst = make_uint4(0, 0, 0, 0);
+            }
+          }
+          if (!ok) break;
+          fence_proxy_async_smem();
+        }
+#pragma unroll
+        for (int c = 0; c < NH / 2; c += 32)
+          tmem_st32(tmem + lane_t + C::TM_S + (uint32_t)(t & 1) * C::N + h * (NH / 2) + c,
+                    *reinterpret_cast<const uint32_t(*)[32]>(pk + c));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&ctl.p_full[t & 1]));
+      }
+      if (!ok) break;
+      const bool row_valid = cur.row_valid;
+      const int64_t out_row = cur.out_row;
+      {
+        Item nit;
+        have = next_item(a, item, stride, n_items, bq, nit);
+        if (have) row_setup<C::N>(a, nit, row, G, lane, cur);
+      }
+      // the item's last PV, then the full row sum (both halves)
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_full), (uint32_t)((t - 1) & 1), abort_flag, gerr,
+                                             kWaitLimitNs));
+      if (!ok) break;
+      ctl.red[xc & 1][h][row] = l;
+      mbar_arrive(smem_u32(&ctl.xch[xc & 1]));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag,
+                                             gerr, kWaitLimitNs));
+      if (!ok) break;
+      l += ctl.red[xc & 1][h ^ 1][row];
+      ++xc;
+      // epilogue: O / l -> bf16, 64 columns per pass, 32-byte stores.  The
+      // next item's first PV overwrites O only after this thread's P for it
+      // (published after these loads completed).
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + out_row * C::D + h * DH;
 #pragma unroll 1
-      for (int c = 0; c < DH / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_t + C::TM_O + h * DH + 32 * c, r);
+      for (int c = 0; c < DH / 64; ++c) {
+        uint32_t r[64];
+        tmem_ld32(tmem + lane_t + C::TM_O + h * DH + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(r));
+        tmem_ld32(tmem + lane_t + C::TM_O + h * DH + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
         tmem_wait_ld();
         if (row_valid) {
-          uint4 v[4];
-          uint32_t *w = reinterpret_cast<uint32_t *>(v);
+          uint32_t w[32];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
+          for (int e = 0; e < 32; ++e)
             w[e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
-          uint4 *dst = reinterpret_cast<uint4 *>(o + 32 * c);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = v[e];
+          for (int e = 0; e < 4; ++e) st_global_v8(o + 64 * c + 16 * e, w + 8 * e);
         }
       }
       if (row_valid && h == 0 && a.lse != nullptr)
         a.lse[out_row] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      tc_fence_before();
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      report(a.err, SWA_ERR_TIMEOUT);
     }
   }
 
@@ -555,6 +739,14 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess)
+    return 0;
+  return n;
+}
+
 template <class C>
 cudaError_t run(const AttnArgs &a, cudaStream_t st) {
   const int G = a.hq / a.hkv;
@@ -572,9 +764,11 @@ cudaError_t run(const AttnArgs &a, cudaStream_t st) {
   static_assert(smem <= 227 * 1024, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int64_t blocks = a.num_tokens / bq + a.num_seqs;
-  dim3 grid((unsigned)blocks, (unsigned)a.hkv);
-  attn_tc_kernel<C><<<grid, 352, smem, st>>>(mq, mk, mv, a, G);
+  const int64_t items = (a.num_tokens / bq + a.num_seqs) * (int64_t)a.hkv;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int grid = (int)(items < sms ? items : (int64_t)sms);
+  attn_tc_kernel<C><<<grid, 352, smem, st>>>(mq, mk, mv, a, G, (int)items);
   return cudaGetLastError();
 }
 
@@ -585,10 +779,11 @@ using Cfg128 = Cfg<128, 6, 6>;    // 32 KB Q + 6 K + 6 V units of 16 KB
 
 bool tc_supported(const AttnArgs &a) {
   const int G = a.hq / a.hkv;
+  const int64_t items = (a.num_tokens / (128 / max(G, 1)) + a.num_seqs) * (int64_t)a.hkv;
   return a.dtype == SWA_DTYPE_BF16 && (a.head_dim == 128 || a.head_dim == 256) && a.num_splits == 1 &&
          (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) && a.max_query_len > 1 &&
          a.num_blocks * a.block_size < (int64_t)INT32_MAX && a.num_tokens < (int64_t)INT32_MAX &&
-         encoder() != nullptr;
+         items < (int64_t)INT32_MAX && encoder() != nullptr;
 }
 
 cudaError_t launch_attention_tc(const AttnArgs &a, cudaStream_t st) {
