@@ -86,8 +86,9 @@ struct Ctrl {
   uint64_t q_full, q_empty;
   uint64_t k_full[kMaxUnits], k_empty[kMaxUnits], v_full[kMaxUnits], v_empty[kMaxUnits];
   uint64_t s_full[2], p_full[2];
-  uint64_t o_full, drain;
+  uint64_t o_full, o_item, drain;
   uint64_t xch[2];                       // exchanges between the two softmax warpgroups
+  int32_t sched_n[4];                    // tile count of item ord at [ord & 3] (0: end of stream)
   uint32_t tmem_base;
   int abort;
 };
@@ -277,6 +278,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(smem_u32(&ctl.xch[i]), 256);
     }
     mbar_init(smem_u32(&ctl.o_full), 1);
+    mbar_init(smem_u32(&ctl.o_item), 1);
     mbar_init(smem_u32(&ctl.drain), 1);
     mbar_fence_init();
     tma_prefetch_map(&tm_q);
@@ -323,6 +325,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // Q: the previous item's last QK has to be done with the buffer
         if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, gerr, kWaitLimitNs);
         if (ok) {
+          // the MMA warp learns the item's tile count from here once q_full completes
+          ctl.sched_n[ord & 3] = n_tiles;
           mbar_expect_tx(smem_u32(&ctl.q_full), C::Q_BYTES);
           for (int c = 0; c < C::CH; ++c)
             tma_load_3d(q_s + c * C::Q_CHUNK, &tm_q, c * 64, it.hk * G, it.qstart + it.qpos_lo,
@@ -390,6 +394,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_wait(smem_u32(is_v ? &ctl.v_full[u % SU] : &ctl.k_full[u % SU]), (uint32_t)((u / SU) & 1), nullptr,
                   nullptr, kWaitLimitNs);
       if (!is_v && ord > 0) mbar_wait(smem_u32(&ctl.q_full), (ord - 1) & 1, nullptr, nullptr, kWaitLimitNs);
+      // end of stream for the MMA warp: one more q_full phase without data, once
+      // the MMA warp is past the last real one (its last QK released q_empty)
+      if (!is_v && ok &&
+          (ord == 0 || mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, gerr, kWaitLimitNs))) {
+        ctl.sched_n[ord & 3] = 0;
+        mbar_arrive(smem_u32(&ctl.q_full));
+      }
     }
   } else if (warp == 1) {
     // =============================== MMA issuer =================================
@@ -401,37 +412,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       // free: PV_{t-2} issued -- tcgen05 ops from one thread run in issue
       // order) and issues whichever is ready, PV first.
       bool ok = true;
-      // QK cursor over the item stream; it records every item's tile count for PV
-      int qk_item = blockIdx.x - stride, qk_ord = -1, qk_j = 0, qk_n = 0, qk_half = 0;
-      bool qk_done = false, qk_q_ok = false;
-      int64_t qk_t = 0;                                  // tiles whose QK is fully issued
-      int ring_n[4];
-      int pushed = 0, popped = 0;
+      // QK cursor: item ordinal, tile within the item, half; item tile counts
+      // come from the Q producer through ctl.sched_n with each q_full phase.
+      int qk_ord = -1, qk_j = 0, qk_n = 0, qk_half = 0;
+      bool qk_done = false;
+      int qk_t = 0;                                      // tiles whose QK is fully issued
       // PV cursor
-      int64_t pv_t = 0;
-      int pv_j = 0, pv_n = 0, pv_half = 0;
+      int pv_ord = 0, pv_t = 0, pv_j = 0, pv_n = 0, pv_half = 0;
       bool pv_p_ok = false;
       uint64_t stall_t0 = 0;
       uint32_t spins = 0;
       while (true) {
         bool progressed = false;
-        if (pv_n == 0 && popped < pushed) {
-          pv_n = ring_n[popped & 3];
+        if (pv_n == 0 && pv_ord <= qk_ord) {             // the PV cursor enters item pv_ord
+          pv_n = ctl.sched_n[pv_ord & 3];
           pv_j = 0;
         }
-        if (pv_n > 0 && pv_t < qk_t) {
+        if (pv_t < qk_t) {
           if (!pv_p_ok) pv_p_ok = mbar_test_wait(smem_u32(&ctl.p_full[pv_t & 1]), (uint32_t)((pv_t >> 1) & 1));
-          const int64_t u = 2 * pv_t + pv_half;
-          const int slot = (int)(u % C::VSU);
+          const int u = 2 * pv_t + pv_half;
+          const int slot = u % C::VSU;
           if (pv_p_ok && mbar_test_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1))) {
             tc_fence_after();
-            const uint32_t p_t = tmem + C::TM_S + (uint32_t)(pv_t & 1) * C::N;
+            const uint32_t p_t = tmem + C::TM_S + (uint32_t)(pv_t & 1) * C::N + pv_half * (C::VU_KEYS / 16) * 8;
+            const uint32_t vb = v_s + slot * C::UNIT;
 #pragma unroll
-            for (int kk = 0; kk < C::VU_KEYS / 16; ++kk) {
-              const uint64_t bd = smem_desc_sw128(v_s + slot * C::UNIT + kk * 16 * 128, C::VU_CHUNK, 1024);
-              mma_ts(tmem + C::TM_O, p_t + (pv_half * (C::VU_KEYS / 16) + kk) * 8, bd, C::IDESC_PV,
+            for (int kk = 0; kk < C::VU_KEYS / 16; ++kk)
+              mma_ts(tmem + C::TM_O, p_t + kk * 8, smem_desc_sw128(vb + kk * 16 * 128, C::VU_CHUNK, 1024), C::IDESC_PV,
                      (pv_j > 0 || pv_half > 0 || kk > 0) ? 1u : 0u);
-            }
             mma_commit(smem_u32(&ctl.v_empty[slot]));
             if (pv_half == 1) {
               mma_commit(smem_u32(&ctl.o_full));
@@ -439,7 +447,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
               pv_p_ok = false;
               ++pv_t;
               if (++pv_j == pv_n) {
-                ++popped;
+                mma_commit(smem_u32(&ctl.o_item));       // the item's O is final
+                ++pv_ord;
                 pv_n = 0;
               }
             } else {
@@ -449,50 +458,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           }
         }
         if (!qk_done && qk_t < pv_t + 2) {
-          if (qk_j == qk_n) {                            // enter the next valid item
-            Item it;
-            if (!next_item(a, qk_item, stride, n_items, bq, it)) {
+          if (qk_j == qk_n && mbar_test_wait(smem_u32(&ctl.q_full), (uint32_t)((qk_ord + 1) & 1))) {
+            // the next item's Q has landed (or the stream has ended)
+            const int n = ctl.sched_n[(qk_ord + 1) & 3];
+            if (n == 0) {
               qk_done = true;
             } else {
-              int kmin, kmax;
-              block_keys(a, it, 0, 1, false, kmin, kmax);
-              qk_n = kmax / C::N - kmin / C::N + 1;
-              qk_j = 0;
               ++qk_ord;
-              ring_n[pushed++ & 3] = qk_n;
-              qk_q_ok = false;
-            }
-          }
-          if (!qk_done) {
-            if (!qk_q_ok) qk_q_ok = mbar_test_wait(smem_u32(&ctl.q_full), qk_ord & 1);
-            const int64_t u = 2 * qk_t + qk_half;
-            const int slot = (int)(u % C::KSU);
-            if (qk_q_ok && mbar_test_wait(smem_u32(&ctl.k_full[slot]), (uint32_t)((u / C::KSU) & 1))) {
+              qk_n = n;
+              qk_j = 0;
               tc_fence_after();
-              const uint32_t d = tmem + C::TM_S + (uint32_t)(qk_t & 1) * C::N;
-#pragma unroll
-              for (int kk = 0; kk < C::D / 32; ++kk) {  // 16-column steps over this half of head_dim
-                const uint32_t off = (kk & 3) * 32;      // inside the 128-byte swizzle row
-                const int cl = kk >> 2;                  // chunk within the unit
-                const uint64_t ad = smem_desc_sw128(q_s + (qk_half * C::KU_CH + cl) * C::Q_CHUNK + off, 16, 1024);
-                const uint64_t bd = smem_desc_sw128(k_s + slot * C::UNIT + cl * C::KU_CHUNK + off, 16, 1024);
-                mma_ss(d, ad, bd, C::IDESC_QK, (qk_half > 0 || kk > 0) ? 1u : 0u);
-              }
-              mma_commit(smem_u32(&ctl.k_empty[slot]));
-              if (qk_half == 1) {
-                mma_commit(smem_u32(&ctl.s_full[qk_t & 1]));
-                if (qk_j == qk_n - 1) mma_commit(smem_u32(&ctl.q_empty));   // the item's Q is no longer read
-                qk_half = 0;
-                ++qk_t;
-                ++qk_j;
-              } else {
-                qk_half = 1;
-              }
-              progressed = true;
             }
+            progressed = true;
+          }
+          const int u = 2 * qk_t + qk_half;
+          const int slot = u % C::KSU;
+          if (qk_j < qk_n && mbar_test_wait(smem_u32(&ctl.k_full[slot]), (uint32_t)((u / C::KSU) & 1))) {
+            tc_fence_after();
+            const uint32_t d = tmem + C::TM_S + (uint32_t)(qk_t & 1) * C::N;
+            const uint32_t qa = q_s + qk_half * C::KU_CH * C::Q_CHUNK;
+            const uint32_t kb = k_s + slot * C::UNIT;
+#pragma unroll
+            for (int kk = 0; kk < C::D / 32; ++kk) {    // 16-column steps over this half of head_dim
+              const uint32_t off = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;   // chunk, then 32 B in the swizzle row
+              const uint32_t offk = (kk >> 2) * C::KU_CHUNK + (kk & 3) * 32;
+              mma_ss(d, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + offk, 16, 1024), C::IDESC_QK,
+                     (qk_half > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&ctl.k_empty[slot]));
+            if (qk_half == 1) {
+              mma_commit(smem_u32(&ctl.s_full[qk_t & 1]));
+              if (qk_j == qk_n - 1) mma_commit(smem_u32(&ctl.q_empty));   // the item's Q is no longer read
+              qk_half = 0;
+              ++qk_t;
+              ++qk_j;
+            } else {
+              qk_half = 1;
+            }
+            progressed = true;
           }
         }
-        if (qk_done && popped == pushed) break;          // every issued QK has had its PV
+        if (qk_done && pv_ord > qk_ord) break;           // every issued QK has had its PV
         if (progressed) {
           stall_t0 = 0;
           spins = 0;
@@ -526,6 +532,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const float sl2 = a.scale * kLog2e;
     int64_t t = 0;                                       // global tile index
     int64_t xc = 0;                                      // exchanges so far (buffer xc & 1)
+    int n_done = 0;                                      // items finished
     bool ok = true;
     // The next item's setup (a few dependent global loads) is done while the
     // current item's last PV runs.
@@ -576,18 +583,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         ++xc;
         const float m_new = fmaxf(m_used, mx);
         const bool need = m_new > m_used + 8.f;           // also true on the first visible tile
-        // PV_{t-1} is confirmed exactly once per tile (here if O must be
-        // rescaled, else before P_t is published; for an item's first tile it
-        // was confirmed at the end of the previous item), so this thread is
-        // never more than one o_full phase behind.
-        bool pv_prev_done = (j == 0);
+        // P_t does not wait for PV_{t-1}; only a rescale of O (and the V tail
+        // below) does.  PV_{t-2} has completed here (QK_t, seen complete, was
+        // issued after it and tcgen05 work completes in issue order), so the
+        // o_full phase of PV_{t-1} is the only one that can still be open and
+        // its parity is unambiguous.  An item's first tile needs no wait: the
+        // previous item's epilogue saw all of its PVs complete.
         if (__any_sync(0xffffffffu, need)) {             // same decision in both warpgroups
           const float m_next = need ? m_new : m_used;
           const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_next);
           if (j > 0) {
             ok = mbar_wait(smem_u32(&ctl.o_full), (uint32_t)((t - 1) & 1), abort_flag, gerr, kWaitLimitNs);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            pv_prev_done = true;
             tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < DH / 32; ++c) {
@@ -613,14 +620,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           pk[c] = pack_bf16(p0, p1);
         }
         l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-        if (!pv_prev_done) {
-          ok = mbar_wait(smem_u32(&ctl.o_full), (uint32_t)((t - 1) & 1), abort_flag, gerr, kWaitLimitNs);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        }
         if (kt0 + C::N > it.seq_len) {
           // keys past the sequence end: their V rows may hold anything; zero
-          // them.  PV_{t-1} is done, so every earlier unit of each V slot has
-          // been consumed and the v_full parity below is unambiguous.
+          // them.  Once PV_{t-1} is done every earlier unit of each V slot has
+          // been consumed, so the v_full parity below is unambiguous.
+          if (j > 0) {
+            ok = mbar_wait(smem_u32(&ctl.o_full), (uint32_t)((t - 1) & 1), abort_flag, gerr, kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          }
           for (int half = 0; half < 2 && ok; ++half) {
             const int k0 = kt0 + half * C::VU_KEYS;
             if (k0 + C::VU_KEYS <= it.seq_len) continue;
@@ -657,9 +664,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         have = next_item(a, item, stride, n_items, bq, nit);
         if (have) row_setup<C::N>(a, nit, row, G, lane, cur);
       }
-      // the item's last PV, then the full row sum (both halves)
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_full), (uint32_t)((t - 1) & 1), abort_flag, gerr,
+      // the item's last PV (one o_item phase per item), then the full row sum
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item), (uint32_t)(n_done & 1), abort_flag, gerr,
                                              kWaitLimitNs));
+      ++n_done;
       if (!ok) break;
       ctl.red[xc & 1][h][row] = l;
       mbar_arrive(smem_u32(&ctl.xch[xc & 1]));
