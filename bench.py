@@ -420,7 +420,7 @@ def run_extras(dev, pk):
     del q, k, v, po, pl
 
     # bandwidth sweeps at sizes where HBM, not launch latency, sets the time (cold L2)
-    n_tok, B = 1 << 24, 16
+    n_tok, B = 1 << 26, 16
     lens = np.full(64, n_tok // 64, dtype=np.int64)
     qsl = torch.as_tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev)
     pos = torch.cat([torch.arange(int(x), device=dev, dtype=torch.int64) for x in lens])
@@ -430,7 +430,7 @@ def run_extras(dev, pk):
     slots = torch.empty(maxn, dtype=torch.int32, device=dev)
     sm_ms = _time_ms(lambda: swa.swa_slot_mapping(qsl, pos, bt, B, maxn, out=slots), flush=flush)
     sm_bytes = n_tok * (8 + 4) + (maxn - n_tok) * 4 + 64 * pages * 4
-    res["slot_mapping_16M_tokens"] = {"ms": round(sm_ms, 4), "gbs": round(sm_bytes / sm_ms / 1e6, 1),
+    res["slot_mapping_64M_tokens"] = {"ms": round(sm_ms, 4), "gbs": round(sm_bytes / sm_ms / 1e6, 1),
                                       "frac_of_hbm": round(sm_bytes / sm_ms / 1e6 / pk["hbm_gbs"], 4)}
     P, T, H, D = 8, 65536, 32, 128
     po = torch.randn((P, T, H, D), device=dev).to(torch.bfloat16)
