@@ -19,6 +19,9 @@ Sources (page title, then the section):
 * "vllm-ascend Triton operator: _compute_slot_mapping_kernel"
   (0539edu.com) -- section 2 "non-CP path" (slot formula), section 1 (the
   PAD tail for graph-fixed shapes), section 5 (worked example).
+* the same slot-mapping article, section 3 "multi-CP domains" (the
+  interleaved context-parallel slot formula, steps 1-5, and the example of
+  section 3.3).
 * "MLA DCP decode two-stream overlap and V-up fusion (PR #16977)"
   (huashanblogllm.xyz) -- section 1.1 and the LSE glossary entry: partial
   outputs merged with their LSE are equal to one softmax over the whole
@@ -86,6 +89,89 @@ def slot_mapping(query_start_loc, positions, block_table, block_size, num_tokens
             out[t] = int(bt[r, index]) * block_size + offset
     del num_tokens  # the tail is everything after the last request's tokens
     return np.array(out, dtype=np.int64).astype(np.int32), bad
+
+
+def slot_mapping_cp(query_start_loc, positions, block_table, block_size, max_num_tokens,
+                    kv_cache_block_size, cp_world_size, cp_rank, cp_interleave, pad_id=-1):
+    """Slot of every token on one context-parallel rank (section 3.1, steps 1-5).
+
+    Token i of a sequence lives on rank (i // I) % W (I = interleave size, W =
+    world size).  A virtual block spans kv_cache_block_size * W positions;
+    the segments of it that this rank owns are concatenated into local
+    offsets, which index this rank's blocks:
+
+        v_idx, v_off = divmod(pos, kv_cache_block_size * W)
+        local        = (v_off // I) % W == rank
+        local_off    = (v_off // (W * I)) * I + v_off % I
+        block_index  = v_idx * (kv_cache_block_size // block_size) + local_off // block_size
+        slot         = block_table[r][block_index] * block_size + local_off % block_size
+
+    Tokens owned by another rank, the padded tail and unmapped tokens get
+    ``pad_id``; negative positions and block indices outside the row are
+    returned in ``bad``.  With W = 1, I = 1 this is ``slot_mapping``.
+    """
+    W, rank, I = int(cp_world_size), int(cp_rank), int(cp_interleave)
+    kvb, bs = int(kv_cache_block_size), int(block_size)
+    if not (W >= 1 and 0 <= rank < W and I >= 1 and bs >= 1 and kvb % bs == 0 and kvb % I == 0):
+        raise ValueError("cp geometry: need W >= 1, 0 <= rank < W, block_size | kv_cache_block_size, "
+                         "interleave | kv_cache_block_size")
+    qsl = np.asarray(query_start_loc, dtype=np.int64)
+    pos_arr = np.asarray(positions, dtype=np.int64)
+    bt = np.asarray(block_table, dtype=np.int64)
+    stride = bt.shape[1]
+    blocks_per_kv_block = kvb // bs
+    out = [pad_id] * int(max_num_tokens)
+    bad = []
+    for r in range(len(qsl) - 1):
+        for t in range(int(qsl[r]), int(qsl[r + 1])):
+            pos = int(pos_arr[t])
+            if pos < 0:
+                bad.append(t)
+                continue
+            v_idx, v_off = divmod(pos, kvb * W)
+            if (v_off // I) % W != rank:
+                continue                          # another rank's token
+            local_off = (v_off // (W * I)) * I + v_off % I
+            index = v_idx * blocks_per_kv_block + local_off // bs
+            if index >= stride:
+                bad.append(t)
+                continue
+            out[t] = int(bt[r, index]) * bs + local_off % bs
+    return np.array(out, dtype=np.int64).astype(np.int32), bad
+
+
+# ---------------------------------------------------------------------------
+# KV-cache write by slot id (vllm-ascend slot-mapping article, section 1 and
+# the closing summary: the cache-write and attention operators consume slots)
+# ---------------------------------------------------------------------------
+def kv_cache_write(k_new, v_new, slot_mapping, k_cache, v_cache):
+    """Copies of the two caches with token t's rows stored at slot
+    ``slot_mapping[t]``.
+
+    ``k_new``/``v_new``: [T, Hkv, D]; caches: [num_blocks, block_size, Hkv, D]
+    (or already slot-major [num_slots, Hkv, D]).  A negative slot (padding)
+    writes nothing; a slot >= num_slots writes nothing and is returned in
+    ``bad``.  Two tokens with the same slot: unspecified (the scheduler never
+    repeats a slot; here the later token wins).
+    """
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    shape = kc.shape
+    kc = kc.reshape(-1, shape[-2], shape[-1])
+    vc = vc.reshape(-1, shape[-2], shape[-1])
+    slots = np.asarray(slot_mapping, dtype=np.int64)
+    kn, vn = np.asarray(k_new), np.asarray(v_new)
+    bad = []
+    for t in range(kn.shape[0]):
+        s = int(slots[t])
+        if s < 0:
+            continue
+        if s >= kc.shape[0]:
+            bad.append(t)
+            continue
+        kc[s] = kn[t]
+        vc[s] = vn[t]
+    return kc.reshape(shape), vc.reshape(shape), bad
 
 
 # ---------------------------------------------------------------------------
