@@ -432,6 +432,24 @@ def run_extras(dev, pk):
     sm_bytes = n_tok * (8 + 4) + (maxn - n_tok) * 4 + 64 * pages * 4
     res["slot_mapping_64M_tokens"] = {"ms": round(sm_ms, 4), "gbs": round(sm_bytes / sm_ms / 1e6, 1),
                                       "frac_of_hbm": round(sm_bytes / sm_ms / 1e6 / pk["hbm_gbs"], 4)}
+    cp_ms = _time_ms(lambda: swa.swa_slot_mapping_cp(qsl, pos, bt, B, maxn, kv_cache_block_size=B, cp_world_size=4,
+                                                     cp_rank=1, cp_interleave=B, out=slots), flush=flush)
+    res["slot_mapping_cp4_64M_tokens"] = {"ms": round(cp_ms, 4), "gbs": round(sm_bytes / cp_ms / 1e6, 1),
+                                          "frac_of_hbm": round(sm_bytes / cp_ms / 1e6 / pk["hbm_gbs"], 4)}
+    del pos, slots
+    # the step's new K/V rows into the paged cache (Gemma-like sizes: 66,200 tokens x 8 kv heads x 256)
+    T_kv, hkv, D_kv = 66200, 8, 256
+    kn = torch.randn((T_kv, hkv, D_kv), device=dev).to(torch.bfloat16)
+    vn = torch.randn((T_kv, hkv, D_kv), device=dev).to(torch.bfloat16)
+    nblk = -(-T_kv // B) + 64
+    kc = torch.empty((nblk, B, hkv, D_kv), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    kv_slots = torch.randperm(nblk * B, device=dev)[:T_kv].to(torch.int32)
+    kv_ms = _time_ms(lambda: swa.swa_kv_cache_write(kn, vn, kv_slots, kc, vc), flush=flush)
+    kv_bytes = 2 * 2 * T_kv * hkv * D_kv * 2 + T_kv * 4
+    res["kv_cache_write_66200_tokens"] = {"ms": round(kv_ms, 4), "gbs": round(kv_bytes / kv_ms / 1e6, 1),
+                                          "frac_of_hbm": round(kv_bytes / kv_ms / 1e6 / pk["hbm_gbs"], 4)}
+    del kn, vn, kc, vc
     P, T, H, D = 8, 65536, 32, 128
     po = torch.randn((P, T, H, D), device=dev).to(torch.bfloat16)
     pl = torch.randn((P, T, H), device=dev)

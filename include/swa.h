@@ -62,6 +62,7 @@ extern "C" {
 #define SWA_ERR_SPLITS     0x20  /* splits_per_seq entry outside [1, num_splits]   */
 #define SWA_ERR_INTERNAL   0x40  /* a kernel could not set up its pipeline (its
                                     outputs are not written)                      */
+#define SWA_ERR_SLOT       0x80  /* a slot id at or past the end of the KV cache   */
 
 /* ---- element types ------------------------------------------------------ */
 #define SWA_DTYPE_BF16 0
@@ -96,6 +97,62 @@ int swa_slot_mapping(const int32_t *query_start_loc, const int64_t *positions,
                      int32_t block_size, int32_t num_reqs, int64_t num_tokens,
                      int64_t max_num_tokens, int32_t pad_id, int32_t *slot_mapping,
                      int32_t *err, void *stream);
+
+/*
+ * swa_slot_mapping_cp -- swa_slot_mapping on one rank of a context-parallel
+ * group whose KV cache is interleaved across the ranks.
+ *
+ * Defined by the same article, section 3 ("multi-CP domains", steps 1-5):
+ * token i of a sequence lives on rank (i / cp_interleave) % cp_world_size.
+ * With W = cp_world_size, I = cp_interleave, pos = positions[t]:
+ *     v_idx = pos / (kv_cache_block_size * W),  v_off = pos % (kv_cache_block_size * W)
+ *     token is local   iff (v_off / I) % W == cp_rank
+ *     local_off        = (v_off / (W * I)) * I + v_off % I
+ *     block_index      = v_idx * (kv_cache_block_size / block_size) + local_off / block_size
+ *     slot_mapping[t]  = block_table[r][block_index] * block_size + local_off % block_size
+ * and pad_id for tokens owned by another rank and for the padded tail.  A
+ * rank's segments are thus concatenated: its j-th token of a sequence sits at
+ * local offset j.  With W = 1 and I = 1 this is swa_slot_mapping.
+ *
+ *   arguments as for swa_slot_mapping, plus
+ *   kv_cache_block_size   a multiple of block_size and of cp_interleave
+ *   cp_world_size >= 1, 0 <= cp_rank < cp_world_size, cp_interleave >= 1
+ * Host errors: those of swa_slot_mapping, and a geometry that breaks the
+ *   rules above (SWA_E_SIZE).
+ * Device errors: as swa_slot_mapping (a block index >= block_table_stride sets
+ *   SWA_ERR_POSITION).
+ */
+int swa_slot_mapping_cp(const int32_t *query_start_loc, const int64_t *positions,
+                        const int32_t *block_table, int64_t block_table_stride,
+                        int32_t block_size, int32_t num_reqs, int64_t num_tokens,
+                        int64_t max_num_tokens, int32_t pad_id, int32_t kv_cache_block_size,
+                        int32_t cp_world_size, int32_t cp_rank, int32_t cp_interleave,
+                        int32_t *slot_mapping, int32_t *err, void *stream);
+
+/*
+ * swa_kv_cache_write -- store a step's new K and V rows in the paged cache.
+ *
+ * The slot ids of swa_slot_mapping are what the cache-write and attention
+ * operators consume (the slot-mapping article, section 1 and its closing
+ * summary): for every token t with 0 <= slot_mapping[t] < num_slots,
+ *     k_cache[slot_mapping[t]] = k_new[t],   v_cache[slot_mapping[t]] = v_new[t]
+ * (all num_heads_kv x head_dim elements of the row).  A negative slot is a
+ * padding token and writes nothing.  When two tokens carry the same slot, which
+ * one lands is unspecified.
+ *
+ *   k_new, v_new      [num_tokens, num_heads_kv, head_dim] (dtype), 16-byte aligned
+ *   slot_mapping      int32[num_tokens]
+ *   k_cache, v_cache  [num_slots, num_heads_kv, head_dim] (dtype) -- the
+ *                     [num_blocks, block_size, Hkv, D] caches with
+ *                     num_slots = num_blocks * block_size
+ * Host errors: NULL pointers (except err), num_tokens < 0, num_heads_kv < 1,
+ *   head_dim not a positive multiple of 8, unsupported dtype, misaligned pointers.
+ * Device errors: a slot >= num_slots sets SWA_ERR_SLOT and writes nothing.
+ */
+int swa_kv_cache_write(const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                       int64_t num_tokens, int32_t num_heads_kv, int32_t head_dim, int32_t dtype,
+                       void *k_cache, void *v_cache, int64_t num_slots, int32_t *err,
+                       void *stream);
 
 /*
  * swa_tile_bounds -- per query block, the KV-tile loop range after pruning.

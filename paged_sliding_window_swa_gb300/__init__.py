@@ -22,19 +22,22 @@ import torch
 
 from .build_lib import LIB_PATH
 
-__all__ = ["swa_slot_mapping", "swa_tile_bounds", "swa_mm_paged_attention", "lse_combine",
-           "lib", "SwaError", "DTYPE_BF16", "DTYPE_FP32", "ERR_BITS"]
+__all__ = ["swa_slot_mapping", "swa_slot_mapping_cp", "swa_kv_cache_write", "swa_tile_bounds",
+           "swa_mm_paged_attention", "lse_combine", "lib", "SwaError", "DTYPE_BF16", "DTYPE_FP32", "ERR_BITS"]
 
 DTYPE_BF16 = 0
 DTYPE_FP32 = 1
 SPLIT_ALIGN = 128
 _RC = {-1: "SWA_E_NULL", -2: "SWA_E_SIZE", -3: "SWA_E_UNSUPPORTED", -4: "SWA_E_ALIGN", -5: "SWA_E_CUDA"}
 ERR_BITS = {0x01: "BLOCK_ID", 0x02: "POSITION", 0x04: "QSL", 0x08: "LENS", 0x10: "TIMEOUT", 0x20: "SPLITS",
-            0x40: "INTERNAL"}
+            0x40: "INTERNAL", 0x80: "SLOT"}
 
 _c_i32, _c_i64, _c_f, _c_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 _SIGS = {
     "swa_slot_mapping": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i64, _c_i64, _c_i32, _c_p, _c_p, _c_p],
+    "swa_slot_mapping_cp": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i64, _c_i64, _c_i32, _c_i32, _c_i32,
+                            _c_i32, _c_i32, _c_p, _c_p, _c_p],
+    "swa_kv_cache_write": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i64, _c_p, _c_p],
     "swa_tile_bounds": [_c_p, _c_p, _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                         _c_p, _c_p, _c_p],
     "swa_mm_paged_attention": [_c_p, _c_p, _c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_i32,
@@ -120,6 +123,47 @@ def swa_slot_mapping(query_start_loc, positions, block_table, block_size: int, m
                                 _stream(stream))
     _check(rc, "swa_slot_mapping")
     return out
+
+
+def swa_slot_mapping_cp(query_start_loc, positions, block_table, block_size: int, max_num_tokens: int, *,
+                        kv_cache_block_size: int, cp_world_size: int, cp_rank: int, cp_interleave: int,
+                        pad_id: int = -1, out=None, err=None, stream=None):
+    """int32 slots [max_num_tokens] on one context-parallel rank; see ``swa_slot_mapping_cp``."""
+    _dev(query_start_loc, "query_start_loc", torch.int32)
+    _dev(positions, "positions", torch.int64)
+    _dev(block_table, "block_table", torch.int32)
+    if out is None:
+        out = torch.empty(max_num_tokens, dtype=torch.int32, device=positions.device)
+    _dev(out, "out", torch.int32)
+    _dev(err, "err", torch.int32)
+    rc = lib().swa_slot_mapping_cp(_ptr(query_start_loc), _ptr(positions), _ptr(block_table),
+                                   block_table.shape[1], block_size, query_start_loc.numel() - 1,
+                                   positions.numel(), max_num_tokens, pad_id, kv_cache_block_size,
+                                   cp_world_size, cp_rank, cp_interleave, _ptr(out), _ptr(err), _stream(stream))
+    _check(rc, "swa_slot_mapping_cp")
+    return out
+
+
+def swa_kv_cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, *, err=None, stream=None):
+    """Store rows t of ``k_new``/``v_new`` [T, Hkv, D] at slots ``slot_mapping[t]`` of the
+    [num_blocks, block_size, Hkv, D] caches (in place); see ``swa_kv_cache_write``."""
+    _dev(k_new, "k_new")
+    code = _dtype_code(k_new)
+    _dev(v_new, "v_new", k_new.dtype)
+    _dev(k_cache, "k_cache", k_new.dtype)
+    _dev(v_cache, "v_cache", k_new.dtype)
+    _dev(slot_mapping, "slot_mapping", torch.int32)
+    _dev(err, "err", torch.int32)
+    T, Hkv, D = k_new.shape
+    if tuple(v_new.shape) != (T, Hkv, D) or k_cache.shape[-2:] != (Hkv, D) or v_cache.shape != k_cache.shape:
+        raise SwaError("swa_kv_cache_write: shape mismatch")
+    if slot_mapping.numel() < T:
+        raise SwaError("swa_kv_cache_write: slot_mapping shorter than the token count")
+    num_slots = k_cache.numel() // (Hkv * D)
+    rc = lib().swa_kv_cache_write(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T, Hkv, D, code,
+                                  _ptr(k_cache), _ptr(v_cache), num_slots, _ptr(err), _stream(stream))
+    _check(rc, "swa_kv_cache_write")
+    return k_cache, v_cache
 
 
 def swa_tile_bounds(query_start_loc, seq_lens, *, context_lens=None, mm_ranges=None, window: int,

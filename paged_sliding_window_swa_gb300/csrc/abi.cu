@@ -35,6 +35,44 @@ int swa_slot_mapping(const int32_t *query_start_loc, const int64_t *positions,
                                          slot_mapping, err, as_stream(stream)));
 }
 
+int swa_slot_mapping_cp(const int32_t *query_start_loc, const int64_t *positions,
+                        const int32_t *block_table, int64_t block_table_stride, int32_t block_size,
+                        int32_t num_reqs, int64_t num_tokens, int64_t max_num_tokens, int32_t pad_id,
+                        int32_t kv_cache_block_size, int32_t cp_world_size, int32_t cp_rank,
+                        int32_t cp_interleave, int32_t *slot_mapping, int32_t *err, void *stream) {
+  if (num_reqs < 0 || num_tokens < 0 || max_num_tokens < num_tokens || block_size <= 0 ||
+      block_table_stride < 1)
+    return SWA_E_SIZE;
+  if (cp_world_size < 1 || cp_rank < 0 || cp_rank >= cp_world_size || cp_interleave < 1 ||
+      kv_cache_block_size < 1 || kv_cache_block_size % block_size != 0 ||
+      kv_cache_block_size % cp_interleave != 0 || (int64_t)kv_cache_block_size * cp_world_size > INT32_MAX)
+    return SWA_E_SIZE;
+  if (max_num_tokens == 0) return SWA_OK;
+  if (slot_mapping == nullptr || query_start_loc == nullptr) return SWA_E_NULL;
+  if (num_tokens > 0 && (positions == nullptr || block_table == nullptr)) return SWA_E_NULL;
+  if (max_num_tokens > INT32_MAX) return SWA_E_SIZE;
+  const swa::CpArgs cp{kv_cache_block_size, cp_world_size, cp_rank, cp_interleave};
+  return finish(swa::launch_slot_mapping(query_start_loc, positions, block_table, block_table_stride,
+                                         block_size, num_reqs, num_tokens, max_num_tokens, pad_id,
+                                         slot_mapping, err, as_stream(stream), &cp));
+}
+
+int swa_kv_cache_write(const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                       int64_t num_tokens, int32_t num_heads_kv, int32_t head_dim, int32_t dtype,
+                       void *k_cache, void *v_cache, int64_t num_slots, int32_t *err, void *stream) {
+  if (num_tokens < 0 || num_heads_kv < 1 || head_dim < 1 || head_dim % 8 != 0 || num_slots < 0)
+    return SWA_E_SIZE;
+  if (dtype != SWA_DTYPE_BF16 && dtype != SWA_DTYPE_FP32) return SWA_E_UNSUPPORTED;
+  if (num_tokens == 0) return SWA_OK;
+  if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr || k_cache == nullptr ||
+      v_cache == nullptr)
+    return SWA_E_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache)) return SWA_E_ALIGN;
+  const int64_t row_bytes = (int64_t)num_heads_kv * head_dim * (dtype == SWA_DTYPE_BF16 ? 2 : 4);
+  return finish(swa::launch_kv_cache_write(k_new, v_new, slot_mapping, num_tokens, row_bytes, k_cache, v_cache,
+                                           num_slots, err, as_stream(stream)));
+}
+
 int swa_tile_bounds(const int32_t *query_start_loc, const int32_t *seq_lens,
                     const int32_t *context_lens, const int32_t *mm_ranges, int32_t max_mm_ranges,
                     int32_t num_seqs, int32_t window, int32_t causal, int32_t tile_size,

@@ -26,10 +26,20 @@ struct AttnArgs {
   int32_t *err;
 };
 
+// Context-parallel geometry of swa_slot_mapping_cp (validated by the caller).
+struct CpArgs {
+  int32_t kv_cache_block_size, world, rank, interleave;
+};
+
 cudaError_t launch_slot_mapping(const int32_t *qsl, const int64_t *pos, const int32_t *bt,
                                 int64_t stride, int32_t block_size, int32_t num_reqs,
                                 int64_t num_tokens, int64_t max_num_tokens, int32_t pad_id,
-                                int32_t *out, int32_t *err, cudaStream_t st);
+                                int32_t *out, int32_t *err, cudaStream_t st, const CpArgs *cp = nullptr);
+
+// Scatter of new K/V rows into the paged cache by slot id.
+cudaError_t launch_kv_cache_write(const void *k_new, const void *v_new, const int32_t *slots,
+                                  int64_t num_tokens, int64_t row_bytes, void *k_cache, void *v_cache,
+                                  int64_t num_slots, int32_t *err, cudaStream_t st);
 
 cudaError_t launch_tile_bounds(const int32_t *qsl, const int32_t *seq_lens, const int32_t *ctx,
                                const int32_t *mm, int32_t max_mm, int32_t num_seqs, int32_t window,

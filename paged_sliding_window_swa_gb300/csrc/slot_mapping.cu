@@ -29,14 +29,27 @@ __device__ inline int find_req(const int32_t *qsl, int num_reqs, int64_t t) {
   return lo;
 }
 
-// kPow2: block_size == 1 << shift, the usual case -- a shift and a mask
-// instead of a 64-bit division, which the GPU does in software.
-template <bool kVec, bool kPow2>
+// How a position becomes (page, offset).  kPlainPow2: block_size == 1 << shift,
+// the usual case -- a shift and a mask instead of a 64-bit division, which the
+// GPU does in software.  kPlain: any block size.  kCp: one rank of an
+// interleaved context-parallel cache (the article's section 3.1, steps 1-5).
+// kCpPow2: the same with every CP size a power of two (shifts and masks).
+enum Mode { kPlainPow2 = 0, kPlain = 1, kCp = 2, kCpPow2 = 3 };
+
+struct Geom {
+  int32_t block_size, shift;
+  int64_t vbs;                          // CP: kv_cache_block_size * world size (< 2^31)
+  int32_t world, rank, interleave, blocks_per_kv_block;
+  int32_t vbs_shift, inter_shift, wi_shift;   // kCpPow2: log2 of vbs, interleave, world * interleave
+};
+
+template <bool kVec, int kMode>
 __global__ void __launch_bounds__(kThreads)
 slot_mapping_kernel(const int32_t *__restrict__ qsl, const int64_t *__restrict__ pos,
-                    const int32_t *__restrict__ bt, int64_t stride, int32_t block_size, int32_t shift,
+                    const int32_t *__restrict__ bt, int64_t stride, const Geom g,
                     int32_t num_reqs, int64_t num_tokens, int64_t max_num_tokens, int32_t pad_id,
                     int32_t *__restrict__ out, int32_t *__restrict__ err) {
+  const int32_t block_size = g.block_size;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   // query_start_loc sanity: monotone, starts >= 0, ends <= num_tokens
   if (tid < num_reqs) {
@@ -76,14 +89,44 @@ slot_mapping_kernel(const int32_t *__restrict__ qsl, const int64_t *__restrict__
       while (r + 1 < num_reqs && t >= r_end) { ++r; r_end = __ldg(qsl + r + 1); }
       if (t < __ldg(qsl + r) || t >= r_end) continue;        // outside every request
       const int64_t ps = p[i];
-      const int64_t page = kPow2 ? (ps >> shift) : ps / block_size;
-      if (ps < 0 || page >= stride) { report(err, SWA_ERR_POSITION); continue; }
+      if (ps < 0) { report(err, SWA_ERR_POSITION); continue; }
+      int64_t page, off;
+      if (kMode == kCpPow2) {
+        const int64_t v_idx = ps >> g.vbs_shift;
+        const int32_t v_off = (int32_t)(ps & (g.vbs - 1));
+        if (((v_off >> g.inter_shift) & (g.world - 1)) != g.rank) continue;   // another rank's token
+        const int32_t local = ((v_off >> g.wi_shift) << g.inter_shift) | (v_off & (g.interleave - 1));
+        page = v_idx * g.blocks_per_kv_block + (local >> g.shift);
+        off = local & (block_size - 1);
+      } else if (kMode == kCp) {
+        // 32-bit divisions whenever the position fits (the 64-bit ones are software routines)
+        int64_t v_idx;
+        uint32_t v_off;
+        if (ps <= INT32_MAX) {
+          v_idx = (uint32_t)ps / (uint32_t)g.vbs;
+          v_off = (uint32_t)ps - (uint32_t)v_idx * (uint32_t)g.vbs;
+        } else {
+          v_idx = ps / g.vbs;
+          v_off = (uint32_t)(ps - v_idx * g.vbs);
+        }
+        const uint32_t I = (uint32_t)g.interleave, Wd = (uint32_t)g.world;
+        if ((v_off / I) % Wd != (uint32_t)g.rank) continue;          // another rank's token
+        const uint32_t local = (v_off / (Wd * I)) * I + v_off % I;
+        page = v_idx * g.blocks_per_kv_block + local / (uint32_t)block_size;
+        off = local % (uint32_t)block_size;
+      } else if (kMode == kPlainPow2) {
+        page = ps >> g.shift;
+        off = ps & (block_size - 1);
+      } else {
+        page = ps / block_size;
+        off = ps - page * block_size;
+      }
+      if (page >= stride) { report(err, SWA_ERR_POSITION); continue; }
       const int64_t idx = (int64_t)r * stride + page;
       if (idx != last) {                                     // neighbouring tokens mostly share a page
         blk = __ldg(bt + idx);
         last = idx;
       }
-      const int64_t off = kPow2 ? (ps & (block_size - 1)) : ps - page * block_size;
       res[i] = (int32_t)((int64_t)blk * block_size + off);
     }
   }
@@ -104,18 +147,41 @@ slot_mapping_kernel(const int32_t *__restrict__ qsl, const int64_t *__restrict__
 cudaError_t launch_slot_mapping(const int32_t *qsl, const int64_t *pos, const int32_t *bt,
                                 int64_t stride, int32_t block_size, int32_t num_reqs,
                                 int64_t num_tokens, int64_t max_num_tokens, int32_t pad_id,
-                                int32_t *out, int32_t *err, cudaStream_t st) {
+                                int32_t *out, int32_t *err, cudaStream_t st, const CpArgs *cp) {
   const int64_t work = max(ceil_div(max_num_tokens, kTokPerThread), (int64_t)num_reqs);
   if (work == 0) return cudaSuccess;
   const unsigned grid = (unsigned)ceil_div(work, kThreads);
   const bool vec = ((uintptr_t)pos % 16 == 0) && ((uintptr_t)out % 16 == 0);   // t0 is a multiple of 8
-  int shift = 0;
-  while (shift < 30 && (1 << shift) < block_size) ++shift;
-  const bool pow2 = (1 << shift) == block_size;
-  auto k = vec ? (pow2 ? slot_mapping_kernel<true, true> : slot_mapping_kernel<true, false>)
-               : (pow2 ? slot_mapping_kernel<false, true> : slot_mapping_kernel<false, false>);
-  k<<<grid, kThreads, 0, st>>>(qsl, pos, bt, stride, block_size, shift, num_reqs, num_tokens, max_num_tokens,
-                               pad_id, out, err);
+  Geom g{};
+  g.block_size = block_size;
+  while (g.shift < 30 && (1 << g.shift) < block_size) ++g.shift;
+  int mode = (1 << g.shift) == block_size ? kPlainPow2 : kPlain;
+  if (cp != nullptr) {
+    g.vbs = (int64_t)cp->kv_cache_block_size * cp->world;
+    g.world = cp->world;
+    g.rank = cp->rank;
+    g.interleave = cp->interleave;
+    g.blocks_per_kv_block = cp->kv_cache_block_size / block_size;
+    auto log2_exact = [](int64_t x) -> int {       // -1 unless x is a power of two
+      int k = 0;
+      while (k < 62 && ((int64_t)1 << k) < x) ++k;
+      return ((int64_t)1 << k) == x ? k : -1;
+    };
+    g.vbs_shift = log2_exact(g.vbs);
+    g.inter_shift = log2_exact(g.interleave);
+    g.wi_shift = log2_exact((int64_t)g.world * g.interleave);
+    const bool pow2 = mode == kPlainPow2 && g.vbs_shift >= 0 && g.inter_shift >= 0 && g.wi_shift >= 0 &&
+                      log2_exact(g.world) >= 0;
+    mode = pow2 ? kCpPow2 : kCp;
+  }
+  using K = void (*)(const int32_t *, const int64_t *, const int32_t *, int64_t, const Geom, int32_t, int64_t,
+                     int64_t, int32_t, int32_t *, int32_t *);
+  const K table[2][4] = {{slot_mapping_kernel<false, kPlainPow2>, slot_mapping_kernel<false, kPlain>,
+                          slot_mapping_kernel<false, kCp>, slot_mapping_kernel<false, kCpPow2>},
+                         {slot_mapping_kernel<true, kPlainPow2>, slot_mapping_kernel<true, kPlain>,
+                          slot_mapping_kernel<true, kCp>, slot_mapping_kernel<true, kCpPow2>}};
+  table[vec ? 1 : 0][mode]<<<grid, kThreads, 0, st>>>(qsl, pos, bt, stride, g, num_reqs, num_tokens,
+                                                       max_num_tokens, pad_id, out, err);
   return cudaGetLastError();
 }
 

@@ -100,3 +100,29 @@ def test_product_path_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(swa, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(swa.SwaError):
         swa.lib()
+
+
+def test_binding_exposes_the_cache_write_and_cp_calls():
+    for n in ("swa_slot_mapping_cp", "swa_kv_cache_write"):
+        assert n in _declared() and callable(getattr(swa, n))
+
+
+def test_slot_mapping_cp_rejects_bad_geometry(lib):
+    def call(kvb=32, W=2, r=0, I=16, bs=16):
+        return lib.swa_slot_mapping_cp(NULL, NULL, NULL, 4, bs, 1, 10, 20, -1, kvb, W, r, I, NULL, NULL, NULL)
+    assert call(kvb=24) == -2                           # block size 16 does not divide 24
+    assert call(I=12) == -2                             # interleave does not divide 32
+    assert call(r=2) == -2                              # rank >= world size
+    assert call(W=0) == -2
+    assert call() == -1                                 # geometry fine, pointers missing
+    assert lib.swa_slot_mapping_cp(NULL, NULL, NULL, 4, 16, 0, 0, 0, -1, 32, 2, 0, 16, NULL, NULL, NULL) == 0
+
+
+def test_kv_cache_write_rejects_bad_arguments(lib):
+    def call(T=4, hkv=2, d=128, dtype=0, nslots=64):
+        return lib.swa_kv_cache_write(NULL, NULL, NULL, T, hkv, d, dtype, NULL, NULL, nslots, NULL, NULL)
+    assert call(d=100) == -2                            # rows of 16-byte vectors need D % 8 == 0
+    assert call(hkv=0) == -2
+    assert call(dtype=5) == -3
+    assert call() == -1
+    assert call(T=0) == 0
