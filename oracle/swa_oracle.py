@@ -38,9 +38,17 @@ design notes):
 * image ranges are inclusive ``[s, e]`` in absolute positions; ``s >= e`` is
   padding (the pages' test pads with [0, 0]);
 * tile bounds use the block's first row for the window's left edge
-  (``ctx + qpos_lo - W + 1``), the block's last row clamped to the query
-  length, and ``max_seq_prefix_len = seq_len`` whenever image ranges are
-  enabled or attention is non-causal;
+  (``ctx + qpos_lo - W + 1``, or its chunk's lookback start), the block's
+  last row clamped to the query length, and ``max_seq_prefix_len = seq_len``
+  whenever image ranges are enabled, attention is non-causal, or the
+  per-sequence causal mode is on;
+* chunked lookback (CHUNK_LOOKBACK >= 0) replaces only the base window's
+  left edge; the image mask keeps the ordinary window clamp; it needs
+  W > 0 and a positive chunk size (the excerpt applies it only inside the
+  sliding-window branch);
+* per-sequence causal: a flag per sequence replaces ``causal`` in the mask;
+  the tile bounds do not read the flags and bound every sequence with the
+  non-causal right edge, as the excerpt does;
 * split-KV: a sequence with P_s partitions gives partition p the keys
   ``[p*L, min((p+1)*L, seq_len))`` with ``L = 128 * ceil(ceil(seq_len/P_s)/128)``;
   a row with no allowed key in a partition has partial LSE = -inf;
@@ -177,19 +185,42 @@ def kv_cache_write(k_new, v_new, slot_mapping, k_cache, v_cache):
 # ---------------------------------------------------------------------------
 # the visibility rule (vLLM PR #53147 summary, implementation items 1-2)
 # ---------------------------------------------------------------------------
-def visible_keys(q_abs, seq_len, window, causal, ranges):
+def _check_chunk(window, chunk_size, chunk_lookback):
+    """Chunked lookback replaces the sliding window's left edge, so it needs a
+    window and a positive chunk size ("vLLM PR #53147 summary",
+    compute_tile_loop_bounds excerpt: the chunk branch sits inside the
+    SLIDING_WINDOW > 0 branch; CHUNK_LOOKBACK = -1 turns it off)."""
+    if chunk_lookback is None or chunk_lookback < 0:
+        return False
+    if window <= 0 or chunk_size is None or chunk_size <= 0:
+        raise ValueError("chunk_lookback >= 0 needs window > 0 and chunk_size > 0")
+    return True
+
+
+def visible_keys(q_abs, seq_len, window, causal, ranges, chunk_size=0, chunk_lookback=-1):
     """Boolean mask over every key k in [0, seq_len) for the query at q_abs.
 
-    base(q, k): for W > 0, k >= q-W+1 and (causal: k <= q; non-causal:
-    k <= q+W-1); for W <= 0, causal: k <= q, non-causal: every key.
-    mm(q, k): some valid range [s, e] holds both q and k, and (W > 0) k >= q-W+1.
+    base(q, k): for W > 0, k >= left(q) and (causal: k <= q; non-causal:
+    k <= q+W-1), where left(q) = q-W+1, or with chunked lookback
+    (chunk_lookback L >= 0, chunk size C) the start of the chunk L chunks
+    before q's chunk, ((q // C) - L) * C.  For W <= 0, causal: k <= q,
+    non-causal: every key.
+    mm(q, k): some valid range [s, e] holds both q and k, and (W > 0)
+    k >= q-W+1 -- the ordinary window's edge, also under chunking (the
+    reviewer's note on the same page: the image mask is OR-ed after the
+    chunk restriction and clamped by the ordinary window, so it can reach
+    keys before the chunk boundary).
     Visible = base OR mm, for 0 <= k < seq_len.
     """
     k = np.arange(int(seq_len), dtype=np.int64)
     q = int(q_abs)
+    chunked = _check_chunk(window, chunk_size, chunk_lookback)
     if window > 0:
         right = q if causal else q + window - 1
-        base = (k >= q - window + 1) & (k <= right)
+        left = q - window + 1
+        if chunked:
+            left = ((q // int(chunk_size)) - int(chunk_lookback)) * int(chunk_size)
+        base = (k >= left) & (k <= right)
     else:
         base = (k <= q) if causal else np.ones(k.shape, dtype=bool)
     mm = np.zeros(k.shape, dtype=bool)
@@ -236,8 +267,12 @@ def _as_f64(x):
 
 def attention(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, mm_ranges,
               window, causal, scale, context_lens=None, rows=None, splits_per_seq=None,
-              num_splits=1):
+              num_splits=1, seq_causal=None, chunk_size=0, chunk_lookback=-1):
     """Attention of every requested (token, head) row, fp64.
+
+    ``seq_causal``: None, or one flag per sequence that replaces ``causal``
+    for that sequence (the per-sequence causal mode).  ``chunk_size`` /
+    ``chunk_lookback``: chunked lookback, see ``visible_keys``.
 
     ``rows``: iterable of (token, head) pairs, or None for all rows.  Returns
     dicts keyed by (token, head): ``out`` (D-vector) and ``lse`` (float).  With
@@ -275,7 +310,8 @@ def attention(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, mm_ra
         key_ranges = split_key_ranges(seq_lens[s], parts)
         for t, h in lst:
             q_abs = int(ctx[s] + (t - qsl[s]))
-            vis = visible_keys(q_abs, seq_lens[s], window, causal, rng)
+            c_s = causal if seq_causal is None else bool(seq_causal[s])
+            vis = visible_keys(q_abs, seq_lens[s], window, c_s, rng, chunk_size, chunk_lookback)
             for p in range(num_splits if num_splits > 1 else 1):
                 sel = vis.copy()
                 if num_splits > 1:
@@ -299,7 +335,8 @@ def attention(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, mm_ra
     return out, lse
 
 
-def allowed_pair_count(query_start_loc, seq_lens, mm_ranges, window, causal, context_lens=None):
+def allowed_pair_count(query_start_loc, seq_lens, mm_ranges, window, causal, context_lens=None,
+                       seq_causal=None, chunk_size=0, chunk_lookback=-1):
     """Number of visible (query, key) pairs of one head, by the per-pair rule."""
     qsl = np.asarray(query_start_loc, dtype=np.int64)
     seq_lens = np.asarray(seq_lens, dtype=np.int64)
@@ -307,8 +344,10 @@ def allowed_pair_count(query_start_loc, seq_lens, mm_ranges, window, causal, con
     total = 0
     for s in range(len(seq_lens)):
         rng = None if mm_ranges is None else np.asarray(mm_ranges)[s]
+        c_s = causal if seq_causal is None else bool(seq_causal[s])
         for i in range(int(qsl[s + 1] - qsl[s])):
-            total += int(visible_keys(ctx[s] + i, seq_lens[s], window, causal, rng).sum())
+            total += int(visible_keys(ctx[s] + i, seq_lens[s], window, c_s, rng, chunk_size,
+                                      chunk_lookback).sum())
     return total
 
 
@@ -316,20 +355,28 @@ def allowed_pair_count(query_start_loc, seq_lens, mm_ranges, window, causal, con
 # tile bounds (vLLM PR #53147 summary, compute_tile_loop_bounds excerpt)
 # ---------------------------------------------------------------------------
 def tile_bounds(query_start_loc, seq_lens, mm_ranges, window, causal, tile_size, block_q,
-                max_qblocks, context_lens=None):
+                max_qblocks, context_lens=None, per_seq_causal=False, chunk_size=0,
+                chunk_lookback=-1):
     """[loop_lo, loop_hi, max_seq_prefix_len] for every (sequence, query block).
 
-    Blocks past the sequence's query length are left as [0, 0, 0].  With an
-    image-range array present (``mm_ranges`` not None), every range that
-    intersects the block's rows widens the window: the left edge to
-    max(start, q_lo - W + 1), the right edge to the range end; the right edge
-    is then clamped to seq_len - 1 and both edges are converted to tiles.
+    Blocks past the sequence's query length are left as [0, 0, 0].  The base
+    window's left edge is the block's first row's, q_lo - W + 1, or with
+    chunked lookback the start of the chunk L chunks before q_lo's chunk,
+    ((q_lo // C) - L) * C.  Its right edge is q_hi (causal) or q_hi + W - 1
+    (non-causal, and always in the per-sequence causal mode, which the
+    excerpt bounds as non-causal).  With an image-range array present
+    (``mm_ranges`` not None), every range that intersects the block's rows
+    widens it: the left edge to max(start, q_lo - W + 1), the right edge to
+    the range end; the right edge is then clamped to seq_len - 1 and both
+    edges are converted to tiles.
     """
     qsl = np.asarray(query_start_loc, dtype=np.int64)
     seq_lens = np.asarray(seq_lens, dtype=np.int64)
     S = len(seq_lens)
     ctx = (seq_lens - np.diff(qsl)) if context_lens is None else np.asarray(context_lens, np.int64)
     use_mm = mm_ranges is not None and np.asarray(mm_ranges).size > 0
+    chunked = _check_chunk(window, chunk_size, chunk_lookback)
+    right_causal = causal and not per_seq_causal
     out = np.zeros((S, max_qblocks, 3), dtype=np.int64)
     for s in range(S):
         qlen = int(qsl[s + 1] - qsl[s])
@@ -340,7 +387,7 @@ def tile_bounds(query_start_loc, seq_lens, mm_ranges, window, causal, tile_size,
             if qpos_lo >= qlen:
                 continue
             qpos_hi = min(qpos_lo + block_q - 1, qlen - 1)
-            if use_mm or not causal:
+            if use_mm or not right_causal:
                 max_prefix = seq_len
             else:
                 max_prefix = min(c + qpos_hi + 1, seq_len)
@@ -349,8 +396,11 @@ def tile_bounds(query_start_loc, seq_lens, mm_ranges, window, causal, tile_size,
                 lo, hi = 0, num_tiles
             else:
                 q_lo, q_hi = c + qpos_lo, c + qpos_hi
-                first = q_lo - window + 1
-                last = q_hi if causal else q_hi + window - 1
+                if chunked:
+                    first = ((q_lo // int(chunk_size)) - int(chunk_lookback)) * int(chunk_size)
+                else:
+                    first = q_lo - window + 1
+                last = q_hi if right_causal else q_hi + window - 1
                 if use_mm:
                     for rs, re_ in np.asarray(mm_ranges)[s].reshape(-1, 2):
                         rs, re_ = int(rs), int(re_)
@@ -364,8 +414,6 @@ def tile_bounds(query_start_loc, seq_lens, mm_ranges, window, causal, tile_size,
     return out.astype(np.int32)
 
 
-# ---------------------------------------------------------------------------
-# LSE merge (DCP decode study notes, section 1.1 and the LSE glossary entry)
 # ---------------------------------------------------------------------------
 def lse_combine(partial_out, partial_lse):
     """Merge P partial outputs [P, T, H, D] with their LSE [P, T, H].

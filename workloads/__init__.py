@@ -55,6 +55,9 @@ class Layout:
     num_splits: int = 1
     splits_per_seq: Optional[np.ndarray] = None   # int32 [S] or None
     max_num_tokens: int = 0
+    seq_causal: Optional[np.ndarray] = None       # int32 [S] per-sequence causal flags, or None
+    chunk_size: int = 0                           # chunked lookback: chunk size (0 = off)
+    chunk_lookback: int = -1                      # chunked lookback: chunks looked back (-1 = off)
     notes: dict = field(default_factory=dict)
 
     # ---- derived structure -------------------------------------------------
@@ -370,5 +373,6 @@ def device_layout(layout: Layout, device):
         "block_table": as_t(layout.block_table),
         "mm_ranges": None if layout.mm_ranges is None else as_t(layout.mm_ranges),
         "splits_per_seq": None if layout.splits_per_seq is None else as_t(layout.splits_per_seq),
+        "seq_causal": None if layout.seq_causal is None else as_t(layout.seq_causal),
     }
     return out
