@@ -158,33 +158,42 @@ int swa_kv_cache_write(const void *k_new, const void *v_new, const int32_t *slot
  * swa_tile_bounds -- per query block, the KV-tile loop range after pruning.
  *
  * Defined by the vLLM PR #53147 summary, the compute_tile_loop_bounds excerpt
- * and its geometry tests.  Query block b of sequence s holds query rows
+ * (with its CHUNK_LOOKBACK and USE_PER_SEQ_CAUSAL branches) and its geometry
+ * tests.  Query block b of sequence s holds query rows
  * qpos_lo = b*block_q .. qpos_hi = min(qpos_lo + block_q - 1, query_len - 1);
- * q_lo = ctx + qpos_lo, q_hi = ctx + qpos_hi.
+ * q_lo = ctx + qpos_lo, q_hi = ctx + qpos_hi;  rc = causal && !per_seq_causal.
  *   max_seq_prefix_len = seq_len if image ranges are enabled (mm_ranges != NULL
- *     and max_mm_ranges > 0) or !causal, else min(q_hi + 1, seq_len);
+ *     and max_mm_ranges > 0) or !rc, else min(q_hi + 1, seq_len);
  *   num_tiles = ceil(max_seq_prefix_len / tile_size);
  *   window <= 0: [lo, hi) = [0, num_tiles);
- *   window  > 0: first = q_lo - window + 1; last = causal ? q_hi : q_hi+window-1;
+ *   window  > 0: first = q_lo - window + 1, or with chunk_lookback >= 0
+ *       first = ((q_lo / chunk_size) - chunk_lookback) * chunk_size;
+ *     last = rc ? q_hi : q_hi + window - 1;
  *     every valid range [s, e] (s < e) with s <= q_hi and e >= q_lo gives
  *     first = min(first, max(s, q_lo - window + 1)), last = max(last, e);
  *     last = min(last, seq_len - 1);
  *     lo = max(0, floor(first / tile_size)), hi = min(last / tile_size + 1, num_tiles).
- * (The page takes the block's last row for the window's left edge; this
- * library takes the first row, which keeps every visible key of the block's
- * earlier rows inside [lo, hi) and gives the printed [3, 72) and [3, 68).)
+ * (The page takes the block's last row for the window's and the chunk's left
+ * edge; this library takes the first row, which keeps every visible key of the
+ * block's earlier rows inside [lo, hi) and gives the printed [3, 72) and
+ * [3, 68).)  per_seq_causal (0/1) is the per-sequence causal mode: the flags
+ * themselves are not read, every sequence is bounded with the non-causal
+ * right edge, as the excerpt does.  chunk_lookback < 0 turns chunking off
+ * (chunk_size is then ignored).
  *
  *   context_lens  int32[num_seqs] or NULL (then seq_len - query_len)
  *   out           int32[num_seqs, max_qblocks_per_seq, 3] = {lo, hi,
  *                 max_seq_prefix_len}; blocks past the query length get {0,0,0}
  * Host errors: NULL (except context_lens, mm_ranges, err), tile_size <= 0,
- *   block_q <= 0, num_seqs < 0, max_qblocks_per_seq < 0, max_mm_ranges < 0.
+ *   block_q <= 0, num_seqs < 0, max_qblocks_per_seq < 0, max_mm_ranges < 0,
+ *   chunk_lookback >= 0 with window <= 0 or chunk_size <= 0 (SWA_E_SIZE).
  * Device errors: context_lens[s] != seq_len - query_len or query_len > seq_len
  *   sets SWA_ERR_LENS and writes {0, 0, 0} for the sequence.
  */
 int swa_tile_bounds(const int32_t *query_start_loc, const int32_t *seq_lens,
                     const int32_t *context_lens, const int32_t *mm_ranges,
                     int32_t max_mm_ranges, int32_t num_seqs, int32_t window, int32_t causal,
+                    int32_t per_seq_causal, int32_t chunk_size, int32_t chunk_lookback,
                     int32_t tile_size, int32_t block_q, int32_t max_qblocks_per_seq,
                     int32_t *out, int32_t *err, void *stream);
 
@@ -193,11 +202,18 @@ int swa_tile_bounds(const int32_t *query_start_loc, const int32_t *seq_lens,
  *
  * Key k of sequence s is visible to the query at absolute position q when
  * (vLLM PR #53147 summary, implementation items 1-2, "OR semantics"):
- *     base(q,k): window > 0: k >= q-window+1 and (causal ? k <= q : k <= q+window-1)
+ *     base(q,k): window > 0: k >= left(q) and (causal ? k <= q : k <= q+window-1)
  *                window <= 0: causal ? k <= q : true
  *  OR mm(q,k):   some valid range [s0,e0] holds both q and k, and
  *                (window > 0) k >= q - window + 1
  *  AND 0 <= k < seq_lens[s].
+ * left(q) = q - window + 1, or with chunked lookback (chunk_lookback >= 0,
+ * compute_tile_loop_bounds excerpt) the start of the chunk chunk_lookback
+ * chunks before q's: ((q / chunk_size) - chunk_lookback) * chunk_size.  The
+ * image term keeps the window clamp, so it can reach keys before the chunk
+ * (the reviewer's note on the same summary).  `causal` is sequence s's flag
+ * seq_causal[s] != 0 when seq_causal is not NULL (the per-sequence causal
+ * mode), else the argument.
  * With sc = scale * dot(q, k) over the visible keys:
  *     out = sum_k exp(sc - m) v_k / sum_k exp(sc - m),  lse = m + ln sum_k exp(sc - m)
  * (m = max sc, natural log).  Tiles outside the pruned loop range of
@@ -218,6 +234,10 @@ int swa_tile_bounds(const int32_t *query_start_loc, const int32_t *seq_lens,
  *   seq_lens              int32[num_seqs]
  *   context_lens          int32[num_seqs] or NULL (derived)
  *   mm_ranges             int32[num_seqs, max_mm_ranges, 2] or NULL
+ *   seq_causal            int32[num_seqs] or NULL (per-sequence causal flags)
+ *   chunk_size, chunk_lookback  chunked lookback; chunk_lookback < 0: off
+ *                         (chunk_size ignored), >= 0 needs window > 0 and
+ *                         chunk_size > 0 (else SWA_E_SIZE)
  *   max_query_len         host-side upper bound of every query length (it
  *                         selects the decode or the prefill kernel; a value
  *                         below a sequence's query length sets SWA_ERR_LENS
@@ -239,7 +259,8 @@ int swa_mm_paged_attention(const void *q, const void *k_cache, const void *v_cac
                            const int32_t *mm_ranges, int32_t max_mm_ranges, int32_t num_seqs,
                            int64_t num_tokens, int32_t max_query_len, int32_t num_heads_q,
                            int32_t num_heads_kv, int32_t head_dim, int32_t block_size,
-                           int32_t window, int32_t causal, float scale, int32_t dtype,
+                           int32_t window, int32_t causal, const int32_t *seq_causal,
+                           int32_t chunk_size, int32_t chunk_lookback, float scale, int32_t dtype,
                            int32_t num_splits, const int32_t *splits_per_seq, void *out,
                            float *lse, void *partial_out, float *partial_lse, int32_t *err,
                            void *stream);

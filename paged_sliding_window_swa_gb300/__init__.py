@@ -39,10 +39,11 @@ _SIGS = {
                             _c_i32, _c_i32, _c_p, _c_p, _c_p],
     "swa_kv_cache_write": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i64, _c_p, _c_p],
     "swa_tile_bounds": [_c_p, _c_p, _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
-                        _c_p, _c_p, _c_p],
+                        _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_p],
     "swa_mm_paged_attention": [_c_p, _c_p, _c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_i32,
                                _c_i32, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
-                               _c_f, _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p],
+                               _c_p, _c_i32, _c_i32, _c_f, _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_p,
+                               _c_p, _c_p],
     "lse_combine": [_c_p, _c_p, _c_i32, _c_i64, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_p],
 }
 EXPORTED = tuple(_SIGS) + ("swa_version",)
@@ -167,7 +168,8 @@ def swa_kv_cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, *, err=None
 
 
 def swa_tile_bounds(query_start_loc, seq_lens, *, context_lens=None, mm_ranges=None, window: int,
-                    causal: bool, tile_size: int, block_q: int, max_qblocks_per_seq: int, out=None,
+                    causal: bool, tile_size: int, block_q: int, max_qblocks_per_seq: int,
+                    per_seq_causal: bool = False, chunk_size: int = 0, chunk_lookback: int = -1, out=None,
                     err=None, stream=None):
     """int32 [num_seqs, max_qblocks_per_seq, 3] = {lo, hi, max_seq_prefix_len}."""
     _dev(query_start_loc, "query_start_loc", torch.int32)
@@ -181,7 +183,8 @@ def swa_tile_bounds(query_start_loc, seq_lens, *, context_lens=None, mm_ranges=N
     _dev(err, "err", torch.int32)
     R = 0 if mm_ranges is None else mm_ranges.shape[1]
     rc = lib().swa_tile_bounds(_ptr(query_start_loc), _ptr(seq_lens), _ptr(context_lens), _ptr(mm_ranges),
-                               R, S, window, int(bool(causal)), tile_size, block_q, max_qblocks_per_seq,
+                               R, S, window, int(bool(causal)), int(bool(per_seq_causal)), int(chunk_size),
+                               int(chunk_lookback), tile_size, block_q, max_qblocks_per_seq,
                                _ptr(out), _ptr(err), _stream(stream))
     _check(rc, "swa_tile_bounds")
     return out
@@ -189,7 +192,8 @@ def swa_tile_bounds(query_start_loc, seq_lens, *, context_lens=None, mm_ranges=N
 
 def swa_mm_paged_attention(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *,
                            context_lens=None, mm_ranges=None, max_query_len=None, window: int,
-                           causal: bool, scale: float, num_splits: int = 1, splits_per_seq=None,
+                           causal: bool, scale: float, seq_causal=None, chunk_size: int = 0,
+                           chunk_lookback: int = -1, num_splits: int = 1, splits_per_seq=None,
                            out=None, lse=None, return_lse: bool = True, partial_out=None,
                            partial_lse=None, err=None, stream=None):
     """Paged attention; returns (out, lse) or, with num_splits > 1, (partial_out, partial_lse)."""
@@ -199,7 +203,7 @@ def swa_mm_paged_attention(q, k_cache, v_cache, block_table, query_start_loc, se
     _dev(v_cache, "v_cache", q.dtype)
     for name, t in (("block_table", block_table), ("query_start_loc", query_start_loc),
                     ("seq_lens", seq_lens), ("context_lens", context_lens), ("mm_ranges", mm_ranges),
-                    ("splits_per_seq", splits_per_seq), ("err", err)):
+                    ("splits_per_seq", splits_per_seq), ("seq_causal", seq_causal), ("err", err)):
         _dev(t, name, torch.int32)
     T, Hq, D = q.shape
     num_blocks, B, Hkv, D2 = k_cache.shape
@@ -226,7 +230,8 @@ def swa_mm_paged_attention(q, k_cache, v_cache, block_table, query_start_loc, se
     rc = lib().swa_mm_paged_attention(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), num_blocks, _ptr(block_table), block_table.shape[1],
         _ptr(query_start_loc), _ptr(seq_lens), _ptr(context_lens), _ptr(mm_ranges), R, S, T,
-        int(max_query_len), Hq, Hkv, D, B, int(window), int(bool(causal)), float(scale), code,
+        int(max_query_len), Hq, Hkv, D, B, int(window), int(bool(causal)), _ptr(seq_causal),
+        int(chunk_size), int(chunk_lookback), float(scale), code,
         int(num_splits), _ptr(splits_per_seq), _ptr(out), _ptr(lse), _ptr(partial_out),
         _ptr(partial_lse), _ptr(err), _stream(stream))
     _check(rc, "swa_mm_paged_attention")

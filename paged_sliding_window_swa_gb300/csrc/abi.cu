@@ -12,6 +12,10 @@ inline bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
 inline bool block_size_ok(int b) { return b == 16 || b == 32 || b == 64 || b == 128; }
 inline cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 inline int finish(cudaError_t e) { return e == cudaSuccess ? SWA_OK : SWA_E_CUDA; }
+// chunked lookback replaces the sliding window's left edge: it needs a window and a chunk size
+inline bool chunk_ok(int window, int chunk_size, int chunk_lookback) {
+  return chunk_lookback < 0 || (window > 0 && chunk_size > 0);
+}
 
 }  // namespace
 
@@ -75,17 +79,19 @@ int swa_kv_cache_write(const void *k_new, const void *v_new, const int32_t *slot
 
 int swa_tile_bounds(const int32_t *query_start_loc, const int32_t *seq_lens,
                     const int32_t *context_lens, const int32_t *mm_ranges, int32_t max_mm_ranges,
-                    int32_t num_seqs, int32_t window, int32_t causal, int32_t tile_size,
-                    int32_t block_q, int32_t max_qblocks_per_seq, int32_t *out, int32_t *err,
-                    void *stream) {
+                    int32_t num_seqs, int32_t window, int32_t causal, int32_t per_seq_causal,
+                    int32_t chunk_size, int32_t chunk_lookback, int32_t tile_size, int32_t block_q,
+                    int32_t max_qblocks_per_seq, int32_t *out, int32_t *err, void *stream) {
   if (tile_size <= 0 || block_q <= 0 || num_seqs < 0 || max_qblocks_per_seq < 0 || max_mm_ranges < 0)
     return SWA_E_SIZE;
+  if (!chunk_ok(window, chunk_size, chunk_lookback)) return SWA_E_SIZE;
   if (num_seqs == 0 || max_qblocks_per_seq == 0) return SWA_OK;
   if (query_start_loc == nullptr || seq_lens == nullptr || out == nullptr) return SWA_E_NULL;
   if (num_seqs > 65535) return SWA_E_SIZE;
   return finish(swa::launch_tile_bounds(query_start_loc, seq_lens, context_lens, mm_ranges,
-                                        max_mm_ranges, num_seqs, window, causal, tile_size, block_q,
-                                        max_qblocks_per_seq, out, err, as_stream(stream)));
+                                        max_mm_ranges, num_seqs, window, causal != 0, per_seq_causal != 0,
+                                        chunk_size, chunk_lookback < 0 ? -1 : chunk_lookback, tile_size,
+                                        block_q, max_qblocks_per_seq, out, err, as_stream(stream)));
 }
 
 int swa_mm_paged_attention(const void *q, const void *k_cache, const void *v_cache,
@@ -95,7 +101,8 @@ int swa_mm_paged_attention(const void *q, const void *k_cache, const void *v_cac
                            const int32_t *mm_ranges, int32_t max_mm_ranges, int32_t num_seqs,
                            int64_t num_tokens, int32_t max_query_len, int32_t num_heads_q,
                            int32_t num_heads_kv, int32_t head_dim, int32_t block_size,
-                           int32_t window, int32_t causal, float scale, int32_t dtype,
+                           int32_t window, int32_t causal, const int32_t *seq_causal,
+                           int32_t chunk_size, int32_t chunk_lookback, float scale, int32_t dtype,
                            int32_t num_splits, const int32_t *splits_per_seq, void *out,
                            float *lse, void *partial_out, float *partial_lse, int32_t *err,
                            void *stream) {
@@ -108,6 +115,7 @@ int swa_mm_paged_attention(const void *q, const void *k_cache, const void *v_cac
   if (dtype != SWA_DTYPE_BF16 && dtype != SWA_DTYPE_FP32) return SWA_E_UNSUPPORTED;
   if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return SWA_E_UNSUPPORTED;
   if (!std::isfinite(scale)) return SWA_E_SIZE;
+  if (!chunk_ok(window, chunk_size, chunk_lookback)) return SWA_E_SIZE;
   if (num_tokens == 0 || num_seqs == 0) return SWA_OK;
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
       query_start_loc == nullptr || seq_lens == nullptr)
@@ -130,6 +138,8 @@ int swa_mm_paged_attention(const void *q, const void *k_cache, const void *v_cac
   a.num_seqs = num_seqs; a.num_tokens = num_tokens; a.max_query_len = max_query_len;
   a.hq = num_heads_q; a.hkv = num_heads_kv; a.head_dim = head_dim; a.block_size = block_size;
   a.window = window; a.causal = causal != 0; a.scale = scale; a.dtype = dtype;
+  a.seq_causal = seq_causal;
+  a.chunk_size = chunk_size; a.chunk_lookback = chunk_lookback < 0 ? -1 : chunk_lookback;
   a.num_splits = num_splits; a.splits_per_seq = (num_splits > 1) ? splits_per_seq : nullptr;
   a.out = out; a.lse = lse; a.partial_out = partial_out; a.partial_lse = partial_lse; a.err = err;
 

@@ -96,6 +96,7 @@ attn_decode_kernel(AttnArgs a) {
   }
   const int seq_len = __ldg(a.seq_lens + s);
   const int ctx = seq_len - qlen;
+  const bool causal = a.seq_causal != nullptr ? __ldg(a.seq_causal + s) != 0 : a.causal != 0;
   if (ctx < 0 || (a.ctx_lens != nullptr && __ldg(a.ctx_lens + s) != ctx)) {
     if (threadIdx.x == 0) report(a.err, SWA_ERR_LENS);
     return;
@@ -118,8 +119,8 @@ attn_decode_kernel(AttnArgs a) {
     const int r = threadIdx.x;
     if (live && r < rows) {
       const int32_t *ranges = a.mm_ranges ? a.mm_ranges + (int64_t)s * a.max_mm_ranges * 2 : nullptr;
-      const Span sp = visible_span(ctx + r / G, seq_len, a.window, a.causal != 0, ranges,
-                                   a.mm_ranges ? a.max_mm_ranges : 0);
+      const Span sp = visible_span(ctx + r / G, seq_len, a.window, causal, a.chunk_size, a.chunk_lookback,
+                                   ranges, a.mm_ranges ? a.max_mm_ranges : 0);
       lo = max(sp.lo, part.lo);
       hi = min(sp.hi, part.hi);
     }

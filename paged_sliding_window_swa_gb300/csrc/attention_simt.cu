@@ -54,6 +54,7 @@ attn_simt_kernel(AttnArgs a, int bq) {
   }
   const int seq_len = __ldg(a.seq_lens + s);
   const int ctx = seq_len - qlen;
+  const bool causal = a.seq_causal != nullptr ? __ldg(a.seq_causal + s) != 0 : a.causal != 0;
   if (ctx < 0 || (a.ctx_lens != nullptr && __ldg(a.ctx_lens + s) != ctx)) {
     if (threadIdx.x == 0) report(a.err, SWA_ERR_LENS);
     return;
@@ -79,7 +80,8 @@ attn_simt_kernel(AttnArgs a, int bq) {
   for (int r = threadIdx.x; r < kMaxRows; r += kThreads) {
     int lo = 1, hi = 0;
     if (r < rows && qpos_lo + r / G < qlen) {
-      Span sp = visible_span(ctx + qpos_lo + r / G, seq_len, a.window, a.causal != 0, ranges, nr);
+      Span sp = visible_span(ctx + qpos_lo + r / G, seq_len, a.window, causal, a.chunk_size, a.chunk_lookback,
+                             ranges, nr);
       lo = max(sp.lo, part.lo);
       hi = min(sp.hi, part.hi);
     }

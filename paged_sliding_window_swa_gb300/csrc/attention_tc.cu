@@ -99,6 +99,7 @@ constexpr int smem_bytes() { return C::OFF_CTRL + (int)sizeof(Ctrl); }
 struct Item {
   int s, hk, qstart, qlen, qpos_lo, seq_len, ctx;
   int q_lo, q_hi;                        // absolute positions of the block's first and last rows
+  bool causal;                           // the sequence's flag, or the call's
 };
 
 // Item -> (query block, kv head).  False for blocks past their sequence's
@@ -126,41 +127,44 @@ __device__ inline bool decode_item(const AttnArgs &a, int item, int bq, Item &it
   }
   it.q_lo = it.ctx + it.qpos_lo;
   it.q_hi = it.ctx + min(it.qpos_lo + bq - 1, it.qlen - 1);
+  it.causal = a.seq_causal != nullptr ? __ldg(a.seq_causal + it.s) != 0 : a.causal != 0;
   return true;
 }
 
-// The union of the block's rows' visible intervals: left edge of the first
-// row's window, right edge the larger of the last row's window and the end of
-// every valid image range that meets the block (largest such end: `emax`, -1
-// if none), clamped to the sequence.  A range meets the block exactly when it
-// holds one of its rows, so this equals the union of the per-row intervals.
-__device__ inline void union_keys(const AttnArgs &a, const Item &it, int emax, int &kmin, int &kmax) {
-  int lo, hi;
-  if (a.window > 0) {
-    lo = max(0, it.q_lo - a.window + 1);
-    hi = a.causal ? it.q_hi : it.q_hi + a.window - 1;
-  } else {
-    lo = 0;
-    hi = a.causal ? it.q_hi : it.seq_len - 1;
-  }
-  kmin = lo;
-  kmax = min(max(hi, emax), it.seq_len - 1);
+// The union of the block's rows' visible intervals.  Right edge: the larger of
+// the last row's base window and the end of every valid image range that meets
+// the block (largest such end: `emax`, -1 if none).  Left edge: the smaller of
+// the first row's base window (the base left edge never decreases with q) and
+// every such range's clamped start max(s, q_lo-W+1) (smallest: `smin`,
+// INT_MAX if none; a range meeting the block holds its row max(s, q_lo), whose
+// clamped start that is).  A range meets the block exactly when it holds one
+// of its rows, so this equals the union of the per-row intervals.
+__device__ inline void union_keys(const AttnArgs &a, const Item &it, int emax, int smin, int &kmin, int &kmax) {
+  kmin = max(0, min(base_lo(it.q_lo, a.window, a.chunk_size, a.chunk_lookback), smin));
+  kmax = min(max(base_hi(it.q_hi, a.window, it.causal, it.seq_len), emax), it.seq_len - 1);
 }
 
 // Ranges scanned by lanes `start`, `start + step`, ...; `warp_reduce`
 // combines the lanes.
 __device__ inline void block_keys(const AttnArgs &a, const Item &it, int start, int step, bool warp_reduce,
                                   int &kmin, int &kmax) {
-  int emax = -1;
+  int emax = -1, smin = INT_MAX;
   if (a.mm_ranges != nullptr) {
     const int32_t *rg = a.mm_ranges + (int64_t)it.s * a.max_mm_ranges * 2;
+    const int clamp = a.window > 0 ? it.q_lo - a.window + 1 : INT_MIN;
     for (int i = start; i < a.max_mm_ranges; i += step) {
       const int s0 = __ldg(rg + 2 * i), e0 = __ldg(rg + 2 * i + 1);
-      if (s0 < e0 && s0 <= it.q_hi && e0 >= it.q_lo) emax = max(emax, e0);
+      if (s0 < e0 && s0 <= it.q_hi && e0 >= it.q_lo) {
+        emax = max(emax, e0);
+        smin = min(smin, max(s0, clamp));
+      }
     }
   }
-  if (warp_reduce) emax = __reduce_max_sync(0xffffffffu, emax);
-  union_keys(a, it, emax, kmin, kmax);
+  if (warp_reduce) {
+    emax = __reduce_max_sync(0xffffffffu, emax);
+    smin = __reduce_min_sync(0xffffffffu, smin);
+  }
+  union_keys(a, it, emax, smin, kmin, kmax);
 }
 
 // Next valid item of this CTA's stream after `item` (false at the end).
@@ -186,7 +190,7 @@ struct RowSetup {
 // and every lane's own interval: a range is tested against the warp's 32 rows
 // only when it meets their span (ballot), which is rarely more than once.
 // Same rule as the visible interval of a single query: a valid range holding q
-// moves the right edge to its end.
+// moves the right edge to its end and the left edge to its clamped start.
 template <int N>
 __device__ inline void row_setup(const AttnArgs &a, const Item &it, int row, int G, int lane, RowSetup &rs) {
   rs.it = it;
@@ -195,9 +199,11 @@ __device__ inline void row_setup(const AttnArgs &a, const Item &it, int row, int
   const int wq_hi = it.ctx + it.qpos_lo + (wrow0 + 31) / G;
   const int qpos = it.qpos_lo + row / G;
   const int q = it.ctx + qpos;
-  int emax = -1, rhi = -1;
+  int emax = -1, rhi = -1, smin = INT_MAX, rlo = INT_MAX;
   if (a.mm_ranges != nullptr) {
     const int32_t *rg = a.mm_ranges + (int64_t)it.s * a.max_mm_ranges * 2;
+    const int bclamp = a.window > 0 ? it.q_lo - a.window + 1 : INT_MIN;
+    const int rclamp = a.window > 0 ? q - a.window + 1 : INT_MIN;
     for (int b = 0; b < a.max_mm_ranges; b += 32) {
       int s0 = 0, e0 = -1;
       if (b + lane < a.max_mm_ranges) {
@@ -205,33 +211,32 @@ __device__ inline void row_setup(const AttnArgs &a, const Item &it, int row, int
         e0 = __ldg(rg + 2 * (b + lane) + 1);
       }
       const bool valid = s0 < e0;
-      if (valid && s0 <= it.q_hi && e0 >= it.q_lo) emax = max(emax, e0);
+      if (valid && s0 <= it.q_hi && e0 >= it.q_lo) {
+        emax = max(emax, e0);
+        smin = min(smin, max(s0, bclamp));
+      }
       uint32_t m = __ballot_sync(0xffffffffu, valid && s0 <= wq_hi && e0 >= wq_lo);
       while (m != 0) {
         const int src = __ffs(m) - 1;
         m &= m - 1;
         const int s1 = __shfl_sync(0xffffffffu, s0, src), e1 = __shfl_sync(0xffffffffu, e0, src);
-        if (s1 <= q && q <= e1) rhi = max(rhi, e1);
+        if (s1 <= q && q <= e1) {
+          rhi = max(rhi, e1);
+          rlo = min(rlo, max(s1, rclamp));
+        }
       }
     }
     emax = __reduce_max_sync(0xffffffffu, emax);
+    smin = __reduce_min_sync(0xffffffffu, smin);
   }
   int kmin, kmax;
-  union_keys(a, it, emax, kmin, kmax);
+  union_keys(a, it, emax, smin, kmin, kmax);
   rs.tile_lo = kmin / N;
   rs.n_tiles = kmax / N - rs.tile_lo + 1;
   rs.row_valid = qpos < it.qlen;
   if (rs.row_valid) {
-    int lo, hi;
-    if (a.window > 0) {
-      lo = max(0, q - a.window + 1);
-      hi = a.causal ? q : q + a.window - 1;
-    } else {
-      lo = 0;
-      hi = a.causal ? q : it.seq_len - 1;
-    }
-    rs.klo = lo;
-    rs.khi = min(max(hi, rhi), it.seq_len - 1);
+    rs.klo = max(0, min(base_lo(q, a.window, a.chunk_size, a.chunk_lookback), rlo));
+    rs.khi = min(max(base_hi(q, a.window, it.causal, it.seq_len), rhi), it.seq_len - 1);
     rs.out_row = (int64_t)(it.qstart + qpos) * a.hq + it.hk * G + row % G;
   } else {
     rs.klo = 1;

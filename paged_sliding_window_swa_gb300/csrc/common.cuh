@@ -49,29 +49,49 @@ __device__ inline int find_seq(const int32_t *qsl, int num_seqs, int64_t block, 
   return lo;
 }
 
+// The base window of the query at absolute position q, before the image union
+// and the clamp to the sequence.  Left edge: q-W+1, or with chunked lookback
+// (lookback L >= 0, chunk size C, only with W > 0) the start of the chunk L
+// chunks before q's, ((q / C) - L) * C; 0 without a window.  Right edge: q
+// (causal), q+W-1 (non-causal), the sequence end without a window.  Edges are
+// clamped to [0, seq_len - 1] in 64-bit arithmetic, so no window or lookback
+// overflows.
+__device__ inline int base_lo(int q, int window, int chunk_size, int chunk_lookback) {
+  if (window <= 0) return 0;
+  int64_t lo = chunk_lookback >= 0 ? ((int64_t)(q / chunk_size) - chunk_lookback) * chunk_size
+                                   : (int64_t)q - window + 1;
+  return lo < 0 ? 0 : (int)lo;
+}
+__device__ inline int base_hi(int q, int window, bool causal, int seq_len) {
+  if (causal) return q;
+  if (window <= 0) return seq_len - 1;
+  return (int)min((int64_t)q + window - 1, (int64_t)seq_len - 1);
+}
+
 // Visible keys of the query at absolute position q form one interval:
-// [max(0, q-W+1), min(seq_len-1, max(right(q), max{e : valid range [s,e] holds q}))]
-// (right(q) = q causal, q+W-1 non-causal; with W <= 0 the left edge is 0 and a
-// non-causal right edge is the sequence end).  Every range holding q starts at
-// or before q, so its clamped part [max(s, q-W+1), e] joins the base window
-// without a gap.  Returns lo > hi when nothing is visible.  `ranges` may point
-// to global or shared memory (plain generic loads).
+//   lo = max(0, min(base_lo(q), min{max(s, q-W+1) : valid range [s,e] holds q}))
+//   hi = min(seq_len-1, max(base_hi(q), max{e : valid range [s,e] holds q}))
+// (the image terms' left edge only with W > 0).  The base window and every
+// range holding q contain q itself, so their union has no gap: the image mask
+// keeps the ordinary window clamp even where the chunk start is later, and so
+// reaches keys before the chunk.  Returns lo > hi when nothing is visible.
+// `ranges` may point to global or shared memory (plain generic loads).
 struct Span { int lo, hi; };
 
-__device__ inline Span visible_span(int q, int seq_len, int window, bool causal,
-                                    const int32_t *ranges, int num_ranges) {
+__device__ inline Span visible_span(int q, int seq_len, int window, bool causal, int chunk_size,
+                                    int chunk_lookback, const int32_t *ranges, int num_ranges) {
   Span sp;
-  if (window > 0) {
-    sp.lo = max(0, q - window + 1);
-    sp.hi = causal ? q : q + window - 1;
-  } else {
-    sp.lo = 0;
-    sp.hi = causal ? q : seq_len - 1;
-  }
+  sp.lo = base_lo(q, window, chunk_size, chunk_lookback);
+  sp.hi = base_hi(q, window, causal, seq_len);
+  const int clamp = window > 0 ? q - window + 1 : INT_MIN;
   for (int i = 0; i < num_ranges; ++i) {
     const int s = ranges[2 * i], e = ranges[2 * i + 1];
-    if (s < e && s <= q && q <= e) sp.hi = max(sp.hi, e);
+    if (s < e && s <= q && q <= e) {
+      sp.hi = max(sp.hi, e);
+      sp.lo = min(sp.lo, max(s, clamp));
+    }
   }
+  sp.lo = max(sp.lo, 0);
   sp.hi = min(sp.hi, seq_len - 1);
   return sp;
 }

@@ -16,6 +16,8 @@ struct AttnArgs {
   int32_t max_mm_ranges, num_seqs;
   int64_t num_tokens;
   int32_t max_query_len, hq, hkv, head_dim, block_size, window, causal;
+  const int32_t *seq_causal;            // per-sequence causal flags (replace `causal`) or null
+  int32_t chunk_size, chunk_lookback;   // chunked lookback; chunk_lookback < 0: off
   float scale;
   int32_t dtype, num_splits;
   const int32_t *splits_per_seq;
@@ -43,7 +45,8 @@ cudaError_t launch_kv_cache_write(const void *k_new, const void *v_new, const in
 
 cudaError_t launch_tile_bounds(const int32_t *qsl, const int32_t *seq_lens, const int32_t *ctx,
                                const int32_t *mm, int32_t max_mm, int32_t num_seqs, int32_t window,
-                               int32_t causal, int32_t tile, int32_t bq, int32_t max_qblocks,
+                               int32_t causal, int32_t per_seq_causal, int32_t chunk_size,
+                               int32_t chunk_lookback, int32_t tile, int32_t bq, int32_t max_qblocks,
                                int32_t *out, int32_t *err, cudaStream_t st);
 
 cudaError_t launch_lse_combine(const void *po, const float *pl, int32_t num_splits,

@@ -1,20 +1,22 @@
 // Per-query-block KV-tile loop range after sliding-window pruning with the
 // window-clamped image union (vLLM PR #53147 summary, compute_tile_loop_bounds
-// excerpt).  One thread per (sequence, query block).
+// excerpt, with its chunked-lookback left edge and per-sequence causal right
+// edge).  One thread per (sequence, query block).
 #include "common.cuh"
 #include "launch.h"
 
 namespace swa {
 namespace {
 
-__device__ inline int floor_div(int a, int b) {
-  int q = a / b;
-  return (a % b != 0 && ((a < 0) != (b < 0))) ? q - 1 : q;
+__device__ inline int64_t floor_div64(int64_t a, int64_t b) {   // b > 0
+  const int64_t q = a / b;
+  return (a % b != 0 && a < 0) ? q - 1 : q;
 }
 
 __global__ void tile_bounds_kernel(const int32_t *__restrict__ qsl, const int32_t *__restrict__ seq_lens,
                                    const int32_t *__restrict__ ctx_lens, const int32_t *__restrict__ mm,
                                    int32_t max_mm, int32_t num_seqs, int32_t window, int32_t causal,
+                                   int32_t per_seq_causal, int32_t chunk_size, int32_t chunk_lookback,
                                    int32_t tile, int32_t bq, int32_t max_qblocks,
                                    int32_t *__restrict__ out, int32_t *__restrict__ err) {
   const int s = blockIdx.y;
@@ -33,26 +35,30 @@ __global__ void tile_bounds_kernel(const int32_t *__restrict__ qsl, const int32_
   if (qpos_lo >= qlen) { o[0] = o[1] = o[2] = 0; return; }
   const int qpos_hi = min(qpos_lo + bq - 1, qlen - 1);
   const bool use_mm = (mm != nullptr) && (max_mm > 0);
+  // the per-sequence causal mode is bounded as non-causal (the flags are not read here)
+  const bool right_causal = causal && !per_seq_causal;
   const int q_lo = ctx + qpos_lo, q_hi = ctx + qpos_hi;
-  const int max_prefix = (use_mm || !causal) ? seq_len : min(q_hi + 1, seq_len);
+  const int max_prefix = (use_mm || !right_causal) ? seq_len : min(q_hi + 1, seq_len);
   const int num_tiles = (int)ceil_div(max_prefix, tile);
   int lo = 0, hi = num_tiles;
   if (window > 0) {
-    int first = q_lo - window + 1;
-    int last = causal ? q_hi : q_hi + window - 1;
+    // 64-bit edges: a large window or lookback reaches past the int range
+    int64_t first = chunk_lookback >= 0 ? ((int64_t)(q_lo / chunk_size) - chunk_lookback) * chunk_size
+                                        : (int64_t)q_lo - window + 1;
+    int64_t last = right_causal ? (int64_t)q_hi : (int64_t)q_hi + window - 1;
     if (use_mm) {
       const int32_t *r = mm + (int64_t)s * max_mm * 2;
       for (int i = 0; i < max_mm; ++i) {
         const int rs = __ldg(r + 2 * i), re = __ldg(r + 2 * i + 1);
         if (rs < re && rs <= q_hi && re >= q_lo) {
-          first = min(first, max(rs, q_lo - window + 1));
-          last = max(last, re);
+          first = min(first, max((int64_t)rs, (int64_t)q_lo - window + 1));
+          last = max(last, (int64_t)re);
         }
       }
     }
-    last = min(last, seq_len - 1);
-    lo = max(0, floor_div(first, tile));
-    hi = min(floor_div(last, tile) + 1, num_tiles);
+    last = min(last, (int64_t)seq_len - 1);
+    lo = first <= 0 ? 0 : (int)(first / tile);
+    hi = (int)min(floor_div64(last, tile) + 1, (int64_t)num_tiles);
   }
   o[0] = lo;
   o[1] = hi;
@@ -63,13 +69,15 @@ __global__ void tile_bounds_kernel(const int32_t *__restrict__ qsl, const int32_
 
 cudaError_t launch_tile_bounds(const int32_t *qsl, const int32_t *seq_lens, const int32_t *ctx,
                                const int32_t *mm, int32_t max_mm, int32_t num_seqs, int32_t window,
-                               int32_t causal, int32_t tile, int32_t bq, int32_t max_qblocks,
+                               int32_t causal, int32_t per_seq_causal, int32_t chunk_size,
+                               int32_t chunk_lookback, int32_t tile, int32_t bq, int32_t max_qblocks,
                                int32_t *out, int32_t *err, cudaStream_t st) {
   if (num_seqs == 0 || max_qblocks == 0) return cudaSuccess;
   const int threads = 128;
   dim3 grid((unsigned)ceil_div(max_qblocks, threads), (unsigned)num_seqs);
-  tile_bounds_kernel<<<grid, threads, 0, st>>>(qsl, seq_lens, ctx, mm, max_mm, num_seqs, window,
-                                               causal, tile, bq, max_qblocks, out, err);
+  tile_bounds_kernel<<<grid, threads, 0, st>>>(qsl, seq_lens, ctx, mm, max_mm, num_seqs, window, causal,
+                                               per_seq_causal, chunk_size, chunk_lookback, tile, bq,
+                                               max_qblocks, out, err);
   return cudaGetLastError();
 }
 

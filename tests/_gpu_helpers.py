@@ -32,6 +32,7 @@ def run_attention(lay, q, k, v, d, err=None, num_splits=None, mm=True):
         q, k, v, d["block_table"], d["query_start_loc"], d["seq_lens"],
         context_lens=d["context_lens"], mm_ranges=d["mm_ranges"] if mm else None,
         max_query_len=lay.max_query_len, window=lay.window, causal=lay.causal, scale=lay.scale,
+        seq_causal=d.get("seq_causal"), chunk_size=lay.chunk_size, chunk_lookback=lay.chunk_lookback,
         num_splits=P, splits_per_seq=d["splits_per_seq"] if P > 1 else None, err=err)
 
 
@@ -49,7 +50,8 @@ def subproblem(lay, q, k, v, s):
                     mm_ranges=None if lay.mm_ranges is None else lay.mm_ranges[s:s + 1].copy(),
                     block_table=np.arange(max(npages, 1), dtype=np.int32)[None],
                     num_blocks=npages,
-                    splits_per_seq=None if lay.splits_per_seq is None else lay.splits_per_seq[s:s + 1].copy())
+                    splits_per_seq=None if lay.splits_per_seq is None else lay.splits_per_seq[s:s + 1].copy(),
+                    seq_causal=None if lay.seq_causal is None else lay.seq_causal[s:s + 1].copy())
     return lay_s, q_s, k_s, v_s
 
 
@@ -66,7 +68,9 @@ def oracle_rows(lay, q, k, v, rows, mm=True, num_splits=1):
         local = [(t - int(qsl[s]), h) for t, h in lst]
         o, l = O.attention(q_s, k_s, v_s, lay_s.block_table, lay_s.query_start_loc, lay_s.seq_lens,
                            lay_s.mm_ranges if mm else None, lay.window, lay.causal, lay.scale,
-                           rows=local, num_splits=num_splits, splits_per_seq=lay_s.splits_per_seq)
+                           rows=local, num_splits=num_splits, splits_per_seq=lay_s.splits_per_seq,
+                           seq_causal=lay_s.seq_causal, chunk_size=lay.chunk_size,
+                           chunk_lookback=lay.chunk_lookback)
         for key, val in o.items():
             if num_splits > 1:
                 p, tl, h = key

@@ -60,13 +60,18 @@ def test_slot_mapping_rejects_bad_sizes(lib):
 
 
 def test_tile_bounds_rejects_bad_sizes(lib):
-    assert lib.swa_tile_bounds(NULL, NULL, NULL, NULL, 0, 1, 64, 1, 0, 8, 4, NULL, NULL, NULL) == -2
-    assert lib.swa_tile_bounds(NULL, NULL, NULL, NULL, 0, 1, 64, 1, 32, 8, 4, NULL, NULL, NULL) == -1
+    assert lib.swa_tile_bounds(NULL, NULL, NULL, NULL, 0, 1, 64, 1, 0, 0, -1, 0, 8, 4, NULL, NULL, NULL) == -2
+    assert lib.swa_tile_bounds(NULL, NULL, NULL, NULL, 0, 1, 64, 1, 0, 0, -1, 32, 8, 4, NULL, NULL, NULL) == -1
+    # chunked lookback needs a window and a chunk size
+    assert lib.swa_tile_bounds(NULL, NULL, NULL, NULL, 0, 1, 0, 1, 0, 16, 2, 32, 8, 4, NULL, NULL, NULL) == -2
+    assert lib.swa_tile_bounds(NULL, NULL, NULL, NULL, 0, 1, 64, 1, 0, 0, 2, 32, 8, 4, NULL, NULL, NULL) == -2
+    assert lib.swa_tile_bounds(NULL, NULL, NULL, NULL, 0, 1, 64, 1, 1, 16, 2, 32, 8, 4, NULL, NULL, NULL) == -1
 
 
 def _attn(lib, **kw):
     args = dict(q=NULL, k=NULL, v=NULL, nb=10, bt=NULL, stride=4, qsl=NULL, seq=NULL, ctx=NULL,
-                mm=NULL, R=0, S=1, T=8, mq=8, hq=8, hkv=2, d=128, b=16, w=64, causal=1, scale=0.1,
+                mm=NULL, R=0, S=1, T=8, mq=8, hq=8, hkv=2, d=128, b=16, w=64, causal=1, seq_causal=NULL,
+                chunk_size=0, chunk_lookback=-1, scale=0.1,
                 dtype=0, P=1, sps=NULL, out=NULL, lse=NULL, po=NULL, pl=NULL, err=NULL, st=NULL)
     args.update(kw)
     return lib.swa_mm_paged_attention(*args.values())
@@ -78,6 +83,9 @@ def test_attention_rejects_bad_arguments(lib):
     assert _attn(lib, b=8) == -3                        # block size not built
     assert _attn(lib, dtype=7) == -3
     assert _attn(lib, scale=float("nan")) == -2
+    assert _attn(lib, chunk_lookback=1) == -2           # chunking without a chunk size
+    assert _attn(lib, chunk_lookback=0, chunk_size=64, w=0) == -2   # chunking without a window
+    assert _attn(lib, chunk_lookback=0, chunk_size=64) == -1        # valid: reaches the NULL check
     assert _attn(lib) == -1                             # NULL tensors
     assert _attn(lib, T=0) == 0                         # nothing to do
     p = ctypes.c_void_p(0x1000)
