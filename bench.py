@@ -21,6 +21,7 @@ for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")     # the oracle leg runs on one core, stated as such
 
 import argparse
+import dataclasses
 import json
 import math
 import statistics
@@ -46,29 +47,38 @@ UNIT = "TFLOP/s"
 def visible_pairs_per_head(lay) -> int:
     """Visible (query, key) pairs of one head.
 
-    The visible keys of a query form one interval (left edge q-W+1, right edge
-    the larger of the base window's right edge and the end of every image
-    range holding q), so the count is a sum of interval lengths.
+    The visible keys of a query form one interval: left edge the base
+    window's (q-W+1, or with chunked lookback the start of the chunk L chunks
+    back), lowered to max(s, q-W+1) by every image range [s, e] holding q;
+    right edge the larger of the base window's right edge and the end of every
+    such range.  So the count is a sum of interval lengths.
     """
     total = 0
-    qsl, ctx = lay.query_start_loc, lay.context_lens
+    ctx = lay.context_lens
+    chunked = lay.window > 0 and lay.chunk_lookback >= 0
     for s in range(lay.num_seqs):
         n = int(lay.seq_lens[s])
+        causal = lay.causal if lay.seq_causal is None else bool(lay.seq_causal[s])
         q = ctx[s] + np.arange(int(lay.query_lens[s]), dtype=np.int64)
         if lay.window > 0:
-            lo = np.maximum(0, q - lay.window + 1)
-            hi = q.copy() if lay.causal else q + lay.window - 1
+            if chunked:
+                lo = (q // lay.chunk_size - lay.chunk_lookback) * lay.chunk_size
+            else:
+                lo = q - lay.window + 1
+            hi = q.copy() if causal else q + lay.window - 1
         else:
             lo = np.zeros_like(q)
-            hi = q.copy() if lay.causal else np.full_like(q, n - 1)
+            hi = q.copy() if causal else np.full_like(q, n - 1)
         if lay.mm_ranges is not None:
             for a, b in lay.mm_ranges[s]:
                 if a < b:
                     sel = (q >= a) & (q <= b)
                     hi[sel] = np.maximum(hi[sel], b)
+                    if lay.window > 0:
+                        lo[sel] = np.minimum(lo[sel], np.maximum(a, q[sel] - lay.window + 1))
+        lo = np.maximum(lo, 0)
         hi = np.minimum(hi, n - 1)
         total += int(np.maximum(hi - lo + 1, 0).sum())
-    del qsl
     return total
 
 
@@ -86,7 +96,7 @@ def kernel_traffic():
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one attention launch (ncu, 1 pass)
-MEASURED_TRAFFIC = {"kernel_sha": "d7ef05fd6ea73cbf", "bytes": (1085.4 + 519.5) * 1e6}
+MEASURED_TRAFFIC = {"kernel_sha": "b3dc33cb58977b3b", "bytes": (1085.4 + 518.5) * 1e6}
 
 
 def peaks():
@@ -367,9 +377,13 @@ def run_extras(dev, pk):
     def flush():
         scratch.fill_(1)
 
-    # chunked prefill over cached context (head_dim 128, GQA 4), causal and non-causal
-    for causal in (True, False):
-        lay = W.chunked_prefill(causal)
+    # chunked prefill over cached context (head_dim 128, GQA 4), causal and non-causal, and
+    # causal with chunked lookback (chunks of 2048, one chunk back) and alternating
+    # per-sequence causal flags
+    chunk_lay = dataclasses.replace(W.chunked_prefill(True), name="chunked_prefill-chunk2048-lookback1-mixed",
+                                    chunk_size=2048, chunk_lookback=1,
+                                    seq_causal=np.array([s % 2 for s in range(8)], np.int32))
+    for lay in (W.chunked_prefill(True), W.chunked_prefill(False), chunk_lay):
         q, k, v = W.make_tensors(lay, device=dev)
         d = W.device_layout(lay, dev)
         out = torch.empty_like(q)
@@ -378,8 +392,9 @@ def run_extras(dev, pk):
         def attn():
             swa.swa_mm_paged_attention(q, k, v, d["block_table"], d["query_start_loc"], d["seq_lens"],
                                        context_lens=d["context_lens"], mm_ranges=d["mm_ranges"],
-                                       max_query_len=lay.max_query_len, window=lay.window, causal=causal,
-                                       scale=lay.scale, out=out, lse=lse)
+                                       max_query_len=lay.max_query_len, window=lay.window, causal=lay.causal,
+                                       seq_causal=d["seq_causal"], chunk_size=lay.chunk_size,
+                                       chunk_lookback=lay.chunk_lookback, scale=lay.scale, out=out, lse=lse)
         attn()
         ms = _time_ms(attn)
         fl = 4.0 * lay.head_dim * lay.num_heads_q * visible_pairs_per_head(lay)

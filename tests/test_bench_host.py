@@ -21,3 +21,17 @@ def test_gemma_like_count_is_stable():
     n = bench.visible_pairs_per_head(lay)
     # about W + half an image per query beyond the window
     assert 60e6 < n < 90e6
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_visible_pair_count_with_chunks_and_flags_matches_oracle(seed):
+    from dataclasses import replace
+    rng = np.random.default_rng(seed)
+    lay = W.random_small(60 + seed, max_seqs=3, max_ctx=200, max_q=150, with_ranges=True,
+                         window=int(rng.choice([5, 40, 300])))
+    lay = replace(lay, chunk_size=int(rng.choice([1, 16, 50])), chunk_lookback=int(rng.choice([-1, 0, 2])),
+                  seq_causal=rng.integers(0, 2, size=lay.num_seqs).astype(np.int32))
+    ref = O.allowed_pair_count(lay.query_start_loc, lay.seq_lens, lay.mm_ranges, lay.window, lay.causal,
+                               seq_causal=lay.seq_causal, chunk_size=lay.chunk_size,
+                               chunk_lookback=lay.chunk_lookback)
+    assert bench.visible_pairs_per_head(lay) == ref
