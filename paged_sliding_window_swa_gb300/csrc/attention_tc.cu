@@ -21,16 +21,20 @@
 // columns): O [0, D) and two S buffers of 128 fp32 columns; the softmax
 // overwrites the front of S with P as bf16 pairs, the A operand of PV.
 //
-// Eleven warps:
-//   warp 0     Q and K producer, warp 10 V producer: every lane resolves the
-//              cache slot of one page box through the block table (32 boxes
-//              per batch, one batch ahead) and one warp instruction issues a
-//              whole unit (one box per page and 64-column chunk); pages past
-//              the sequence or with a bad block id are read from outside the
-//              tensor, which the TMA fills with 0.
+// Sixteen warps; setmaxnreg moves registers from the first two warpgroups
+// (64 each) to the softmax warpgroups (192 each):
+//   warps 0, 2  K producers (warp 0 also loads Q), warps 4-6 V producers:
+//              every lane resolves the cache slot of one page box through the
+//              block table (32 boxes per batch, one batch ahead); a unit's
+//              boxes (one per page and 64-column chunk) are dealt round-robin
+//              over the operand's producer warps, since one warp issues TMA
+//              boxes one after another; pages past the sequence or with a bad
+//              block id are read from outside the tensor, which the TMA fills
+//              with 0.
 //   warp 1     tcgen05 issuer and TMEM owner: QK runs two tiles ahead of PV
 //              along the CTA's flat tile stream.
-//   warps 2-9  softmax, two warpgroups: thread i of each owns row i (TMEM lane
+//   warps 3, 7 no role (their registers go to the softmax).
+//   warps 8-15 softmax, two warpgroups: thread i of each owns row i (TMEM lane
 //              i) and one half of the tile's columns; half-row maxima meet in
 //              shared memory once per tile.  Masks only tiles not fully inside
 //              the row's interval, keeps the running max in the log2 domain,
@@ -52,7 +56,15 @@ using namespace tc;
 constexpr uint64_t kWaitLimitNs = 200000000ull;    // 200 ms per wait: far above any real stall
 constexpr int kMaxUnits = 8;                       // ring slots per operand
 
-template <int D_, int KSU_, int VSU_>
+// Sixteen warps in four warpgroups.  Warpgroups 0-1 hold the TMA producers and
+// the MMA issuer and give registers away; warpgroups 2-3 are the softmax.
+constexpr int kThreads = 512;
+constexpr int kLaunchRegs = 65536 / kThreads;      // what the launch allocates per thread
+constexpr int kLowRegs = 64, kHighRegs = 192;      // after setmaxnreg: producers/MMA, softmax
+static_assert(kLowRegs + kHighRegs == 2 * kLaunchRegs, "the split must hand over exactly what it frees");
+constexpr int kFirstSoftmaxWarp = 8;
+
+template <int D_, int KSU_, int VSU_, int KW_, int VW_>
 struct Cfg {
   static constexpr int D = D_;          // head dim
   static constexpr int N = 128;         // keys per tile
@@ -60,6 +72,11 @@ struct Cfg {
   static constexpr int CH = D / 64;     // 128-byte column chunks per row
   static constexpr int KSU = KSU_;      // K ring slots (units)
   static constexpr int VSU = VSU_;      // V ring slots (units)
+  // TMA issue from one warp is serial (about one 2 KB page box per 90 cycles),
+  // so each K and V unit's boxes are shared between KW and VW producer warps:
+  // K warps 0 (which also loads Q), 2, 3; V warps 4 .. 4 + VW - 1.
+  static constexpr int KW = KW_;
+  static constexpr int VW = VW_;
   static constexpr int Q_CHUNK = M * 128;
   static constexpr int Q_BYTES = M * D * 2;
   static constexpr int UNIT = N * D;                 // bytes of a K or V unit
@@ -78,6 +95,7 @@ struct Cfg {
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
   static_assert(D + 2 * N <= 512, "TMEM budget");
   static_assert(KSU <= kMaxUnits && VSU <= kMaxUnits && KSU >= 2 && VSU >= 2, "ring sizes");
+  static_assert(KW >= 1 && KW <= 3 && VW >= 1 && VW <= 4, "producer warps");
   static_assert((N / 16) * KU_CH <= 32 && (VU_KEYS / 16) * CH <= 32, "one warp instruction per unit");
 };
 
@@ -246,7 +264,7 @@ __device__ inline void row_setup(const AttnArgs &a, const Item &it, int row, int
 }
 
 template <class C>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const int G, const int n_items) {
   // Everything lives in dynamic shared memory, which starts 1024-byte aligned
@@ -302,9 +320,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const volatile int32_t *gerr = a.err;
   const int stride = gridDim.x;
 
-  if (warp == 0 || warp == 10) {
+  // Register split (warpgroup-wide, at the top of each side so every warp of a
+  // warpgroup executes it converged; the freed registers are handed over at
+  // once, so the increase never waits on work of the other side).
+  if (warp < kFirstSoftmaxWarp) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLowRegs));
+  const bool k_warp = warp == 0 || (warp >= 2 && warp < 1 + C::KW);
+  const bool v_warp = warp >= 4 && warp < 4 + C::VW;
+  if (k_warp || v_warp) {
     // =============================== TMA producers ==============================
-    const bool is_v = warp == 10;
+    // Every producer warp of an operand walks all units; the unit's boxes are
+    // dealt round-robin over the warps (share), and share 0 posts the expected
+    // bytes (a box of another share may land first: the transaction count may
+    // go below zero, but the phase cannot complete before that arrival).
+    const bool is_v = v_warp;
+    const int nsh = is_v ? C::VW : C::KW;
+    const int share = is_v ? warp - 4 : (warp == 0 ? 0 : warp - 1);
     const int SU = is_v ? C::VSU : C::KSU;
     const CUtensorMap *map = is_v ? &tm_v : &tm_k;
     const int unit_keys = is_v ? C::VU_KEYS : C::N;     // K units: 128 keys, V units: 64 keys
@@ -319,14 +350,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       Item it;
       int32_t eb;
       if (!decode_item(a, item, bq, it, eb)) {
-        if (eb != 0 && !is_v && lane == 0) report(a.err, eb);
+        if (eb != 0 && warp == 0 && lane == 0) report(a.err, eb);
         continue;
       }
       int kmin, kmax;
       block_keys(a, it, lane, 32, true, kmin, kmax);
       const int tile_lo = kmin / C::N;
       const int n_tiles = kmax / C::N - tile_lo + 1;
-      if (!is_v && lane == 0) {
+      if (warp == 0 && lane == 0) {
         // Q: the previous item's last QK has to be done with the buffer
         if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, gerr, kWaitLimitNs);
         if (ok) {
@@ -349,7 +380,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           const int page = k / a.block_size;
           const int32_t blk = page < a.bt_stride ? __ldg(bt + page) : -1;
           if (blk >= 0 && blk < a.num_blocks) slot = blk * a.block_size + (k - page * a.block_size);
-          else if (!is_v) report(a.err, SWA_ERR_BLOCK_ID);
+          else if (warp == 0) report(a.err, SWA_ERR_BLOCK_ID);
         }
         return slot;
       };
@@ -368,7 +399,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int t = ul >> 1, half = ul & 1;
         const uint32_t full = smem_u32(is_v ? &ctl.v_full[slot_i] : &ctl.k_full[slot_i]);
         const uint32_t dst = (is_v ? v_s : k_s) + slot_i * C::UNIT;
-        if (lane == 0) mbar_expect_tx(full, C::UNIT);
+        if (share == 0 && lane == 0) mbar_expect_tx(full, C::UNIT);
         __syncwarp();
         // K: unit = head_dim half `half` of tile t's 128 keys; V: key half `half`
         const int b0 = is_v ? (2 * t + half) * boxes : t * boxes;
@@ -385,7 +416,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int slot = b >= batch * 32 ? from_cur : from_prv;
         const int x = (is_v ? c : half * C::KU_CH + c) * 64;
         const uint32_t d = dst + c * (is_v ? C::VU_CHUNK : C::KU_CHUNK) + i * R * 128;
-        if (lane < boxes * uch) tma_load_3d(d, map, x, it.hk, slot, full);
+        if (lane < boxes * uch && lane % nsh == share) tma_load_3d(d, map, x, it.hk, slot, full);
       }
       u_base += ul;                                     // units issued (all of them unless aborted)
     }
@@ -398,10 +429,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       for (int64_t u = max((int64_t)0, u_base - SU); u < u_base; ++u)
         mbar_wait(smem_u32(is_v ? &ctl.v_full[u % SU] : &ctl.k_full[u % SU]), (uint32_t)((u / SU) & 1), nullptr,
                   nullptr, kWaitLimitNs);
-      if (!is_v && ord > 0) mbar_wait(smem_u32(&ctl.q_full), (ord - 1) & 1, nullptr, nullptr, kWaitLimitNs);
+      if (warp == 0 && ord > 0) mbar_wait(smem_u32(&ctl.q_full), (ord - 1) & 1, nullptr, nullptr, kWaitLimitNs);
       // end of stream for the MMA warp: one more q_full phase without data, once
       // the MMA warp is past the last real one (its last QK released q_empty)
-      if (!is_v && ok &&
+      if (warp == 0 && ok &&
           (ord == 0 || mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, gerr, kWaitLimitNs))) {
         ctl.sched_n[ord & 3] = 0;
         mbar_arrive(smem_u32(&ctl.q_full));
@@ -522,7 +553,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mma_commit(smem_u32(&ctl.drain));
       mbar_wait(smem_u32(&ctl.drain), 0, nullptr, nullptr, kWaitLimitNs);
     }
+  }
+  // warps 3 and 7 have no role: they only give their registers to the softmax
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kHighRegs));
     // =============================== softmax ====================================
     // Two warpgroups share every row: warpgroup h owns S columns
     // [h*N/2, (h+1)*N/2) and O columns [h*D/2, (h+1)*D/2).  Both keep the
@@ -530,8 +564,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // once per tile, ordered by a bounded mbarrier) and a partial row sum.
     constexpr int NH = C::N / 2;
     constexpr int DH = C::D / 2;
-    const int h = (warp - 2) >> 2;
-    const int sid = threadIdx.x - 64;                    // 0..255 over both warpgroups
+    const int h = (warp - kFirstSoftmaxWarp) >> 2;
+    const int sid = threadIdx.x - 32 * kFirstSoftmaxWarp;   // 0..255 over both warpgroups
     const int row = 32 * (warp & 3) + lane;              // TMEM lane of this thread
     const uint32_t lane_t = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = a.scale * kLog2e;
@@ -781,12 +815,17 @@ cudaError_t run(const AttnArgs &a, cudaStream_t st) {
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int grid = (int)(items < sms ? items : (int64_t)sms);
-  attn_tc_kernel<C><<<grid, 352, smem, st>>>(mq, mk, mv, a, G, (int)items);
+  // The register split hands over exactly the launch allocation: a kernel built
+  // with another per-thread count would wait forever in setmaxnreg.inc.
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, attn_tc_kernel<C>) != cudaSuccess || fa.numRegs != kLaunchRegs)
+    return cudaErrorInvalidConfiguration;
+  attn_tc_kernel<C><<<grid, kThreads, smem, st>>>(mq, mk, mv, a, G, (int)items);
   return cudaGetLastError();
 }
 
-using Cfg256 = Cfg<256, 2, 3>;    // 64 KB Q + 2 K + 3 V units of 32 KB
-using Cfg128 = Cfg<128, 6, 6>;    // 32 KB Q + 6 K + 6 V units of 16 KB
+using Cfg256 = Cfg<256, 2, 3, 2, 3>;    // 64 KB Q + 2 K + 3 V units of 32 KB
+using Cfg128 = Cfg<128, 6, 6, 1, 1>;    // 32 KB Q + 6 K + 6 V units of 16 KB
 
 }  // namespace
 

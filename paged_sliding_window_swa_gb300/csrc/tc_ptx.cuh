@@ -53,8 +53,10 @@ __device__ inline bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // false) after `limit_ns`, or early when the CTA-local flag *abort is set or
 // the launch-wide error word already carries SWA_ERR_TIMEOUT (so one stalled
 // CTA makes the others quit quickly).  Either pointer may be null: drain
-// waits pass nulls so they only stop at the time limit.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const volatile int *abort,
+// waits pass nulls so they only stop at the time limit.  Inlined: a kernel
+// that splits its registers with setmaxnreg cannot call one function from
+// both sides of the split.
+__device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const volatile int *abort,
                                             const volatile int32_t *err, uint64_t limit_ns) {
   uint64_t t0 = 0;     // the clock is read only once a wait has really stalled
   for (uint32_t i = 1;; ++i) {
