@@ -31,9 +31,11 @@
 //              boxes one after another; pages past the sequence or with a bad
 //              block id are read from outside the tensor, which the TMA fills
 //              with 0.
-//   warp 1     tcgen05 issuer and TMEM owner: QK runs two tiles ahead of PV
-//              along the CTA's flat tile stream.
-//   warps 3, 7 no role (their registers go to the softmax).
+//   warp 1     QK issuer and TMEM owner, warp 3 PV issuer: two tcgen05
+//              streams, so a ready PV never waits behind a QK issue that the
+//              tensor pipe holds up; QK runs two tiles ahead of PV along the
+//              CTA's flat tile stream (QK_t waits until PV_{t-2} is issued).
+//   warp 7     no role (its registers go to the softmax).
 //   warps 8-15 softmax, two warpgroups: thread i of each owns row i (TMEM lane
 //              i) and one half of the tile's columns; half-row maxima meet in
 //              shared memory once per tile.  Masks only tiles not fully inside
@@ -74,7 +76,7 @@ struct Cfg {
   static constexpr int VSU = VSU_;      // V ring slots (units)
   // TMA issue from one warp is serial (about one 2 KB page box per 90 cycles),
   // so each K and V unit's boxes are shared between KW and VW producer warps:
-  // K warps 0 (which also loads Q), 2, 3; V warps 4 .. 4 + VW - 1.
+  // K warps 0 (which also loads Q) and 2; V warps 4 .. 4 + VW - 1.
   static constexpr int KW = KW_;
   static constexpr int VW = VW_;
   static constexpr int Q_CHUNK = M * 128;
@@ -95,7 +97,7 @@ struct Cfg {
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
   static_assert(D + 2 * N <= 512, "TMEM budget");
   static_assert(KSU <= kMaxUnits && VSU <= kMaxUnits && KSU >= 2 && VSU >= 2, "ring sizes");
-  static_assert(KW >= 1 && KW <= 3 && VW >= 1 && VW <= 4, "producer warps");
+  static_assert(KW >= 1 && KW <= 2 && VW >= 1 && VW <= 4, "producer warps");
   static_assert((N / 16) * KU_CH <= 32 && (VU_KEYS / 16) * CH <= 32, "one warp instruction per unit");
 };
 
@@ -104,7 +106,8 @@ struct Ctrl {
   uint64_t q_full, q_empty;
   uint64_t k_full[kMaxUnits], k_empty[kMaxUnits], v_full[kMaxUnits], v_empty[kMaxUnits];
   uint64_t s_full[2], p_full[2];
-  uint64_t o_full, o_item, drain;
+  uint64_t o_full, o_item, drain, drain2;
+  uint64_t pv_iss[2];                    // PV of the tile issued (S buffer may be overwritten)
   uint64_t xch[2];                       // exchanges between the two softmax warpgroups
   int32_t sched_n[4];                    // tile count of item ord at [ord & 3] (0: end of stream)
   uint32_t tmem_base;
@@ -303,6 +306,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     mbar_init(smem_u32(&ctl.o_full), 1);
     mbar_init(smem_u32(&ctl.o_item), 1);
     mbar_init(smem_u32(&ctl.drain), 1);
+    mbar_init(smem_u32(&ctl.drain2), 1);
+    mbar_init(smem_u32(&ctl.pv_iss[0]), 1);
+    mbar_init(smem_u32(&ctl.pv_iss[1]), 1);
     mbar_fence_init();
     tma_prefetch_map(&tm_q);
     tma_prefetch_map(&tm_k);
@@ -438,123 +444,104 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_arrive(smem_u32(&ctl.q_full));
       }
     }
-  } else if (warp == 1) {
-    // =============================== MMA issuer =================================
-    if (lane == 0) {
-      // Event-driven issue: the tensor pipe queues only a few instructions, so
-      // any wait of this thread while work is ready elsewhere is lost MMA
-      // time.  Each pass polls the next PV half (needs P_t and its V unit) and
-      // the next QK half (needs its K unit, the item's Q, and S buffer t & 1
-      // free: PV_{t-2} issued -- tcgen05 ops from one thread run in issue
-      // order) and issues whichever is ready, PV first.
+  } else if (warp == 1 || warp == 3) {
+    // =============================== MMA issuers ================================
+    // Warp 1 issues the QK MMAs, warp 3 the PV MMAs, each from its own stream,
+    // so a PV never waits behind a QK issue that is blocked on the tensor pipe.
+    // QK_t writes S buffer t & 1, which holds P_{t-2}: it is issued only after
+    // PV_{t-2} (warp 3 fences and arrives on pv_iss after issuing it; tcgen05
+    // work ordered through a fence pair runs in that order).
+    if (lane == 0 && warp == 1) {
       bool ok = true;
-      // QK cursor: item ordinal, tile within the item, half; item tile counts
-      // come from the Q producer through ctl.sched_n with each q_full phase.
-      int qk_ord = -1, qk_j = 0, qk_n = 0, qk_half = 0;
-      bool qk_done = false;
-      int qk_t = 0;                                      // tiles whose QK is fully issued
-      // PV cursor
-      int pv_ord = 0, pv_t = 0, pv_j = 0, pv_n = 0, pv_half = 0;
-      bool pv_p_ok = false;
-      uint64_t stall_t0 = 0;
-      uint32_t spins = 0;
-      while (true) {
-        bool progressed = false;
-        if (pv_n == 0 && pv_ord <= qk_ord) {             // the PV cursor enters item pv_ord
-          pv_n = ctl.sched_n[pv_ord & 3];
-          pv_j = 0;
-        }
-        if (pv_t < qk_t) {
-          if (!pv_p_ok) pv_p_ok = mbar_test_wait(smem_u32(&ctl.p_full[pv_t & 1]), (uint32_t)((pv_t >> 1) & 1));
-          const int u = 2 * pv_t + pv_half;
-          const int slot = u % C::VSU;
-          if (pv_p_ok && mbar_test_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1))) {
+      int ord = 0;
+      int64_t t = 0;                                     // tiles of this CTA's stream
+      while (ok) {
+        // the next item's Q has landed (or the stream has ended: 0 tiles)
+        ok = mbar_wait(smem_u32(&ctl.q_full), (uint32_t)(ord & 1), abort_flag, gerr, kWaitLimitNs);
+        if (!ok) break;
+        const int n = ctl.sched_n[ord & 3];
+        if (n == 0) break;
+        tc_fence_after();
+        for (int j = 0; ok && j < n; ++j, ++t) {
+          if (t >= 2) {
+            ok = mbar_wait(smem_u32(&ctl.pv_iss[t & 1]), (uint32_t)(((t - 2) >> 1) & 1), abort_flag, gerr,
+                           kWaitLimitNs);
+            if (!ok) break;
             tc_fence_after();
-            const uint32_t p_t = tmem + C::TM_S + (uint32_t)(pv_t & 1) * C::N + pv_half * (C::VU_KEYS / 16) * 8;
-            const uint32_t vb = v_s + slot * C::UNIT;
-#pragma unroll
-            for (int kk = 0; kk < C::VU_KEYS / 16; ++kk)
-              mma_ts(tmem + C::TM_O, p_t + kk * 8, smem_desc_sw128(vb + kk * 16 * 128, C::VU_CHUNK, 1024), C::IDESC_PV,
-                     (pv_j > 0 || pv_half > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(smem_u32(&ctl.v_empty[slot]));
-            if (pv_half == 1) {
-              mma_commit(smem_u32(&ctl.o_full));
-              pv_half = 0;
-              pv_p_ok = false;
-              ++pv_t;
-              if (++pv_j == pv_n) {
-                mma_commit(smem_u32(&ctl.o_item));       // the item's O is final
-                ++pv_ord;
-                pv_n = 0;
-              }
-            } else {
-              pv_half = 1;
-            }
-            progressed = true;
           }
-        }
-        if (!qk_done && qk_t < pv_t + 2) {
-          if (qk_j == qk_n && mbar_test_wait(smem_u32(&ctl.q_full), (uint32_t)((qk_ord + 1) & 1))) {
-            // the next item's Q has landed (or the stream has ended)
-            const int n = ctl.sched_n[(qk_ord + 1) & 3];
-            if (n == 0) {
-              qk_done = true;
-            } else {
-              ++qk_ord;
-              qk_n = n;
-              qk_j = 0;
-              tc_fence_after();
-            }
-            progressed = true;
-          }
-          const int u = 2 * qk_t + qk_half;
-          const int slot = u % C::KSU;
-          if (qk_j < qk_n && mbar_test_wait(smem_u32(&ctl.k_full[slot]), (uint32_t)((u / C::KSU) & 1))) {
+          const uint32_t d = tmem + C::TM_S + (uint32_t)(t & 1) * C::N;
+          for (int half = 0; ok && half < 2; ++half) {
+            const int64_t u = 2 * t + half;
+            const int slot = (int)(u % C::KSU);
+            ok = mbar_wait(smem_u32(&ctl.k_full[slot]), (uint32_t)((u / C::KSU) & 1), abort_flag, gerr, kWaitLimitNs);
+            if (!ok) break;
             tc_fence_after();
-            const uint32_t d = tmem + C::TM_S + (uint32_t)(qk_t & 1) * C::N;
-            const uint32_t qa = q_s + qk_half * C::KU_CH * C::Q_CHUNK;
+            const uint32_t qa = q_s + half * C::KU_CH * C::Q_CHUNK;
             const uint32_t kb = k_s + slot * C::UNIT;
 #pragma unroll
             for (int kk = 0; kk < C::D / 32; ++kk) {    // 16-column steps over this half of head_dim
               const uint32_t off = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;   // chunk, then 32 B in the swizzle row
               const uint32_t offk = (kk >> 2) * C::KU_CHUNK + (kk & 3) * 32;
               mma_ss(d, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + offk, 16, 1024), C::IDESC_QK,
-                     (qk_half > 0 || kk > 0) ? 1u : 0u);
+                     (half > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(smem_u32(&ctl.k_empty[slot]));
-            if (qk_half == 1) {
-              mma_commit(smem_u32(&ctl.s_full[qk_t & 1]));
-              if (qk_j == qk_n - 1) mma_commit(smem_u32(&ctl.q_empty));   // the item's Q is no longer read
-              qk_half = 0;
-              ++qk_t;
-              ++qk_j;
-            } else {
-              qk_half = 1;
-            }
-            progressed = true;
           }
+          if (!ok) break;
+          mma_commit(smem_u32(&ctl.s_full[t & 1]));
+          if (j == n - 1) mma_commit(smem_u32(&ctl.q_empty));   // the item's Q is no longer read
         }
-        if (qk_done && pv_ord > qk_ord) break;           // every issued QK has had its PV
-        if (progressed) {
-          stall_t0 = 0;
-          spins = 0;
-        } else if ((++spins & 255u) == 0) {
-          if (*abort_flag || (*gerr & SWA_ERR_TIMEOUT)) { ok = false; break; }
-          const uint64_t now = global_ns();
-          if (stall_t0 == 0) stall_t0 = now;
-          else if (now - stall_t0 > kWaitLimitNs) { ok = false; break; }
+        ++ord;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        report(a.err, SWA_ERR_TIMEOUT);
+      }
+      // every MMA issued by this thread must finish before TMEM is released
+      mma_commit(smem_u32(&ctl.drain));
+      mbar_wait(smem_u32(&ctl.drain), 0, nullptr, nullptr, kWaitLimitNs);
+    } else if (lane == 0 && warp == 3) {
+      bool ok = true;
+      int64_t t = 0;
+      for (int item = blockIdx.x; ok && item < n_items; item += stride) {
+        Item it;
+        int32_t eb;
+        if (!decode_item(a, item, bq, it, eb)) continue;
+        int kmin, kmax;
+        block_keys(a, it, 0, 1, false, kmin, kmax);
+        const int n_tiles = kmax / C::N - kmin / C::N + 1;
+        for (int j = 0; ok && j < n_tiles; ++j, ++t) {
+          ok = mbar_wait(smem_u32(&ctl.p_full[t & 1]), (uint32_t)((t >> 1) & 1), abort_flag, gerr, kWaitLimitNs);
+          for (int half = 0; ok && half < 2; ++half) {
+            const int64_t u = 2 * t + half;
+            const int slot = (int)(u % C::VSU);
+            ok = mbar_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1), abort_flag, gerr, kWaitLimitNs);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t p_t = tmem + C::TM_S + (uint32_t)(t & 1) * C::N + half * (C::VU_KEYS / 16) * 8;
+            const uint32_t vb = v_s + slot * C::UNIT;
+#pragma unroll
+            for (int kk = 0; kk < C::VU_KEYS / 16; ++kk)
+              mma_ts(tmem + C::TM_O, p_t + kk * 8, smem_desc_sw128(vb + kk * 16 * 128, C::VU_CHUNK, 1024), C::IDESC_PV,
+                     (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(smem_u32(&ctl.v_empty[slot]));
+          }
+          if (!ok) break;
+          mma_commit(smem_u32(&ctl.o_full));
+          if (j == n_tiles - 1) mma_commit(smem_u32(&ctl.o_item));   // the item's O is final
+          tc_fence_before();
+          mbar_arrive(smem_u32(&ctl.pv_iss[t & 1]));
         }
       }
       if (!ok) {
         *abort_flag = 1;
         report(a.err, SWA_ERR_TIMEOUT);
       }
-      // every MMA issued so far must finish before TMEM is released
-      mma_commit(smem_u32(&ctl.drain));
-      mbar_wait(smem_u32(&ctl.drain), 0, nullptr, nullptr, kWaitLimitNs);
+      mma_commit(smem_u32(&ctl.drain2));
+      mbar_wait(smem_u32(&ctl.drain2), 0, nullptr, nullptr, kWaitLimitNs);
     }
   }
-  // warps 3 and 7 have no role: they only give their registers to the softmax
+  // warp 7 has no role: it only gives its registers to the softmax
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kHighRegs));
     // =============================== softmax ====================================
@@ -569,6 +556,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int row = 32 * (warp & 3) + lane;              // TMEM lane of this thread
     const uint32_t lane_t = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = a.scale * kLog2e;
+    // the scale is folded into the exponent's FFMA: maxima are taken on the raw
+    // scores (of -S for a negative scale) and scaled once
+    const bool neg_scale = sl2 < 0.f;
+    const float asl2 = fmaxf(fabsf(sl2), 1.17549435e-38f);
     int64_t t = 0;                                       // global tile index
     int64_t xc = 0;                                      // exchanges so far (buffer xc & 1)
     int n_done = 0;                                      // items finished
@@ -604,19 +595,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const bool full = klo <= kc0 && khi >= kc0 + NH - 1;
         if (__all_sync(0xffffffffu, full)) {
 #pragma unroll
-          for (int c = 0; c < NH; ++c) x[c] = __uint_as_float(raw[c]) * sl2;
+          for (int c = 0; c < NH; ++c) x[c] = neg_scale ? -__uint_as_float(raw[c]) : __uint_as_float(raw[c]);
         } else {
 #pragma unroll
           for (int c = 0; c < NH; ++c)
-            x[c] = (kc0 + c >= klo && kc0 + c <= khi) ? __uint_as_float(raw[c]) * sl2 : -INFINITY;
+            x[c] = (kc0 + c >= klo && kc0 + c <= khi) ? (neg_scale ? -__uint_as_float(raw[c]) : __uint_as_float(raw[c]))
+                                                      : -INFINITY;
         }
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < NH; ++c) m4[c & 3] = fmaxf(m4[c & 3], x[c]);
         float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        mx = mx == -INFINITY ? -INFINITY : mx * asl2;
         ctl.red[xc & 1][h][row] = mx;
         mbar_arrive(smem_u32(&ctl.xch[xc & 1]));
-        ok = mbar_wait(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag, gerr, kWaitLimitNs);
+        ok = mbar_wait_spin(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag, gerr, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         mx = fmaxf(mx, ctl.red[xc & 1][h ^ 1][row]);
         ++xc;
@@ -654,7 +647,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < NH / 2; ++c) {
-          const float p0 = ex2(x[2 * c] - ms), p1 = ex2(x[2 * c + 1] - ms);
+          const float p0 = ex2(fmaf(x[2 * c], asl2, -ms)), p1 = ex2(fmaf(x[2 * c + 1], asl2, -ms));
           s4[c & 3] += p0 + p1;
           pk[c] = pack_bf16(p0, p1);
         }
@@ -710,7 +703,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       if (!ok) break;
       ctl.red[xc & 1][h][row] = l;
       mbar_arrive(smem_u32(&ctl.xch[xc & 1]));
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag,
+      ok = __all_sync(0xffffffffu, mbar_wait_spin(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag,
                                              gerr, kWaitLimitNs));
       if (!ok) break;
       l += ctl.red[xc & 1][h ^ 1][row];
@@ -824,7 +817,7 @@ cudaError_t run(const AttnArgs &a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-using Cfg256 = Cfg<256, 2, 3, 2, 3>;    // 64 KB Q + 2 K + 3 V units of 32 KB
+using Cfg256 = Cfg<256, 3, 2, 2, 3>;    // 64 KB Q + 3 K + 2 V units of 32 KB
 using Cfg128 = Cfg<128, 6, 6, 1, 1>;    // 32 KB Q + 6 K + 6 V units of 16 KB
 
 }  // namespace

@@ -75,6 +75,14 @@ __device__ inline bool mbar_wait(uint32_t bar, uint32_t parity, const volatile i
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, abort, err, limit_ns);
 }
+// For waits that are usually short (a partner warpgroup at the same point):
+// poll without suspending first, then wait as above.
+__device__ inline bool mbar_wait_spin(uint32_t bar, uint32_t parity, const volatile int *abort,
+                                      const volatile int32_t *err, uint64_t limit_ns) {
+  for (int i = 0; i < 64; ++i)
+    if (mbar_test_wait(bar, parity)) return true;
+  return mbar_wait(bar, parity, abort, err, limit_ns);
+}
 
 // ---------------------------------------------------------------- TMA
 __device__ inline void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
