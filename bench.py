@@ -82,10 +82,12 @@ def visible_pairs_per_head(lay) -> int:
     return total
 
 
-def kernel_traffic():
+def kernel_traffic(num_requests):
     """DRAM bytes per attention launch on the 4-request workload from the committed ncu
-    launch list (profiles/attn_tc_gemma_like.md), or None when the kernel source has
-    changed since those counters were taken."""
+    launch list (profiles/attn_tc_gemma_like.md), or None for another workload or when
+    the kernel source has changed since those counters were taken."""
+    if num_requests != MEASURED_TRAFFIC["requests"]:
+        return None
     import hashlib
     src = os.path.join(ROOT, "paged_sliding_window_swa_gb300", "csrc", "attention_tc.cu")
     try:
@@ -96,7 +98,7 @@ def kernel_traffic():
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one attention launch (ncu, 1 pass)
-MEASURED_TRAFFIC = {"kernel_sha": "98dd97f1addcb351", "bytes": (1094.1 + 521.0) * 1e6}
+MEASURED_TRAFFIC = {"kernel_sha": "98dd97f1addcb351", "requests": 4, "bytes": (1094.1 + 521.0) * 1e6}
 
 
 def peaks():
@@ -334,7 +336,7 @@ def report_line(args, lay, step, flops, pairs, ms_per_step, attn_ms, feed_ms, cl
             "peak": pk["bf16_tflops"],
             "unit": "TFLOP/s",
             "frac": round(achieved / pk["bf16_tflops"], 4),
-            "traffic": kernel_traffic(),
+            "traffic": kernel_traffic(args.requests),
             "peak_source": f"{pk['source']} bf16 dense (burst)",
             "avg_launch_ms": round(attn_avg, 4),
         },
