@@ -1,38 +1,45 @@
 // Per-query-block KV-tile loop range after sliding-window pruning with the
 // window-clamped image union (vLLM PR #53147 summary, compute_tile_loop_bounds
 // excerpt, with its chunked-lookback left edge and per-sequence causal right
-// edge).  One thread per (sequence, query block).
+// edge).
 #include "common.cuh"
 #include "launch.h"
 
 namespace swa {
 namespace {
 
-__device__ inline int64_t floor_div64(int64_t a, int64_t b) {   // b > 0
-  const int64_t q = a / b;
-  return (a % b != 0 && a < 0) ? q - 1 : q;
-}
+constexpr int kWarpsPerBlock = 4;
 
-__global__ void tile_bounds_kernel(const int32_t *__restrict__ qsl, const int32_t *__restrict__ seq_lens,
-                                   const int32_t *__restrict__ ctx_lens, const int32_t *__restrict__ mm,
-                                   int32_t max_mm, int32_t num_seqs, int32_t window, int32_t causal,
-                                   int32_t per_seq_causal, int32_t chunk_size, int32_t chunk_lookback,
-                                   int32_t tile, int32_t bq, int32_t max_qblocks,
-                                   int32_t *__restrict__ out, int32_t *__restrict__ err) {
+// One warp per (sequence, query block): the lanes split the sequence's image
+// ranges and the warp reduces the edges.  Each edge is clamped to the range it
+// ends up in before the reduction (left edge >= 0, right edge <= seq_len - 1),
+// which keeps it in 32 bits and leaves min/max unchanged after the clamp.
+__global__ void __launch_bounds__(32 * kWarpsPerBlock)
+tile_bounds_kernel(const int32_t *__restrict__ qsl, const int32_t *__restrict__ seq_lens,
+                   const int32_t *__restrict__ ctx_lens, const int32_t *__restrict__ mm, int32_t max_mm,
+                   int32_t num_seqs, int32_t window, int32_t causal, int32_t per_seq_causal, int32_t chunk_size,
+                   int32_t chunk_lookback, int32_t tile, int32_t bq, int32_t max_qblocks,
+                   int32_t *__restrict__ out, int32_t *__restrict__ err) {
+  const int lane = threadIdx.x & 31;
   const int s = blockIdx.y;
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (s >= num_seqs || b >= max_qblocks) return;
+  const int b = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (s >= num_seqs || b >= max_qblocks) return;             // uniform per warp
   int32_t *o = out + ((int64_t)s * max_qblocks + b) * 3;
   const int qlen = __ldg(qsl + s + 1) - __ldg(qsl + s);
   const int seq_len = __ldg(seq_lens + s);
   int ctx = seq_len - qlen;
   if (qlen < 0 || ctx < 0 || (ctx_lens != nullptr && __ldg(ctx_lens + s) != ctx)) {
-    if (b == 0) report(err, SWA_ERR_LENS);
-    o[0] = o[1] = o[2] = 0;
+    if (lane == 0) {
+      if (b == 0) report(err, SWA_ERR_LENS);
+      o[0] = o[1] = o[2] = 0;
+    }
     return;
   }
   const int qpos_lo = b * bq;
-  if (qpos_lo >= qlen) { o[0] = o[1] = o[2] = 0; return; }
+  if (qpos_lo >= qlen) {
+    if (lane == 0) o[0] = o[1] = o[2] = 0;
+    return;
+  }
   const int qpos_hi = min(qpos_lo + bq - 1, qlen - 1);
   const bool use_mm = (mm != nullptr) && (max_mm > 0);
   // the per-sequence causal mode is bounded as non-causal (the flags are not read here)
@@ -43,26 +50,32 @@ __global__ void tile_bounds_kernel(const int32_t *__restrict__ qsl, const int32_
   int lo = 0, hi = num_tiles;
   if (window > 0) {
     // 64-bit edges: a large window or lookback reaches past the int range
-    int64_t first = chunk_lookback >= 0 ? ((int64_t)(q_lo / chunk_size) - chunk_lookback) * chunk_size
-                                        : (int64_t)q_lo - window + 1;
-    int64_t last = right_causal ? (int64_t)q_hi : (int64_t)q_hi + window - 1;
+    const int64_t first0 = chunk_lookback >= 0 ? ((int64_t)(q_lo / chunk_size) - chunk_lookback) * chunk_size
+                                               : (int64_t)q_lo - window + 1;
+    const int64_t last0 = right_causal ? (int64_t)q_hi : (int64_t)q_hi + window - 1;
+    int first = (int)max(first0, (int64_t)0);                // in [0, q_lo]
+    int last = (int)min(last0, (int64_t)seq_len - 1);        // in [q_hi, seq_len - 1]
     if (use_mm) {
+      const int clamp_lo = (int)max((int64_t)q_lo - window + 1, (int64_t)0);
       const int32_t *r = mm + (int64_t)s * max_mm * 2;
-      for (int i = 0; i < max_mm; ++i) {
+      for (int i = lane; i < max_mm; i += 32) {
         const int rs = __ldg(r + 2 * i), re = __ldg(r + 2 * i + 1);
         if (rs < re && rs <= q_hi && re >= q_lo) {
-          first = min(first, max((int64_t)rs, (int64_t)q_lo - window + 1));
-          last = max(last, (int64_t)re);
+          first = min(first, max(rs, clamp_lo));
+          last = max(last, min(re, seq_len - 1));
         }
       }
+      first = __reduce_min_sync(0xffffffffu, first);
+      last = __reduce_max_sync(0xffffffffu, last);
     }
-    last = min(last, (int64_t)seq_len - 1);
-    lo = first <= 0 ? 0 : (int)(first / tile);
-    hi = (int)min(floor_div64(last, tile) + 1, (int64_t)num_tiles);
+    lo = first / tile;
+    hi = min(last / tile + 1, num_tiles);
   }
-  o[0] = lo;
-  o[1] = hi;
-  o[2] = max_prefix;
+  if (lane == 0) {
+    o[0] = lo;
+    o[1] = hi;
+    o[2] = max_prefix;
+  }
 }
 
 }  // namespace
@@ -73,9 +86,8 @@ cudaError_t launch_tile_bounds(const int32_t *qsl, const int32_t *seq_lens, cons
                                int32_t chunk_lookback, int32_t tile, int32_t bq, int32_t max_qblocks,
                                int32_t *out, int32_t *err, cudaStream_t st) {
   if (num_seqs == 0 || max_qblocks == 0) return cudaSuccess;
-  const int threads = 128;
-  dim3 grid((unsigned)ceil_div(max_qblocks, threads), (unsigned)num_seqs);
-  tile_bounds_kernel<<<grid, threads, 0, st>>>(qsl, seq_lens, ctx, mm, max_mm, num_seqs, window, causal,
+  dim3 grid((unsigned)ceil_div(max_qblocks, kWarpsPerBlock), (unsigned)num_seqs);
+  tile_bounds_kernel<<<grid, 32 * kWarpsPerBlock, 0, st>>>(qsl, seq_lens, ctx, mm, max_mm, num_seqs, window, causal,
                                                per_seq_causal, chunk_size, chunk_lookback, tile, bq,
                                                max_qblocks, out, err);
   return cudaGetLastError();
