@@ -58,15 +58,11 @@ using namespace tc;
 constexpr uint64_t kWaitLimitNs = 200000000ull;    // 200 ms per wait: far above any real stall
 constexpr int kMaxUnits = 8;                       // ring slots per operand
 
-// Sixteen warps in four warpgroups.  Warpgroups 0-1 hold the TMA producers and
-// the MMA issuer and give registers away; warpgroups 2-3 are the softmax.
-constexpr int kThreads = 512;
-constexpr int kLaunchRegs = 65536 / kThreads;      // what the launch allocates per thread
-constexpr int kLowRegs = 64, kHighRegs = 192;      // after setmaxnreg: producers/MMA, softmax
-static_assert(kLowRegs + kHighRegs == 2 * kLaunchRegs, "the split must hand over exactly what it frees");
+// Warpgroups 0-1 hold the TMA producers and the MMA issuers and give registers
+// away (setmaxnreg); the NSW warpgroups from warp 8 on are the softmax.
 constexpr int kFirstSoftmaxWarp = 8;
 
-template <int D_, int KSU_, int VSU_, int KW_, int VW_>
+template <int D_, int KSU_, int VSU_, int KW_, int VW_, int NSW_, int NS_>
 struct Cfg {
   static constexpr int D = D_;          // head dim
   static constexpr int N = 128;         // keys per tile
@@ -79,6 +75,15 @@ struct Cfg {
   // K warps 0 (which also loads Q) and 2; V warps 4 .. 4 + VW - 1.
   static constexpr int KW = KW_;
   static constexpr int VW = VW_;
+  // NSW softmax warpgroups share every row (each owns N / NSW columns of S and
+  // D / NSW of O); NS S buffers in TMEM let QK run NS tiles ahead of PV.
+  static constexpr int NSW = NSW_;
+  static constexpr int NS = NS_;
+  static constexpr int THREADS = 32 * (kFirstSoftmaxWarp + 4 * NSW);
+  static constexpr int LAUNCH_REGS = (65536 / THREADS) & ~7;   // what the launch allocates per thread
+  static constexpr int LOW_REGS = 64;                           // producers and MMA issuers
+  static constexpr int HIGH_REGS =                             // softmax: all that the others free
+      ((LAUNCH_REGS * THREADS - 32 * kFirstSoftmaxWarp * LOW_REGS) / (128 * NSW)) & ~7;
   static constexpr int Q_CHUNK = M * 128;
   static constexpr int Q_BYTES = M * D * 2;
   static constexpr int UNIT = N * D;                 // bytes of a K or V unit
@@ -95,27 +100,32 @@ struct Cfg {
   static constexpr uint32_t TM_COLS = 512;
   static constexpr uint32_t IDESC_QK = idesc_bf16(128, N, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
-  static_assert(D + 2 * N <= 512, "TMEM budget");
+  static_assert(D + NS * N <= 512, "TMEM budget");
+  static_assert((NSW == 2 || NSW == 4) && NS >= 2 && NS <= 3, "softmax warpgroups, S buffers");
+  static_assert(32 * kFirstSoftmaxWarp * LOW_REGS + 128 * NSW * HIGH_REGS <= LAUNCH_REGS * THREADS,
+                "the register split can only hand over what the launch allocated");
   static_assert(KSU <= kMaxUnits && VSU <= kMaxUnits && KSU >= 2 && VSU >= 2, "ring sizes");
   static_assert(KW >= 1 && KW <= 2 && VW >= 1 && VW <= 4, "producer warps");
   static_assert((N / 16) * KU_CH <= 32 && (VU_KEYS / 16) * CH <= 32, "one warp instruction per unit");
 };
 
+template <int NSW, int NS>
 struct Ctrl {
-  float red[2][2][128];                  // half-row max / row-sum exchange buffers
+  float red[2][NSW][128];                // partial row max / row-sum exchange buffers
   uint64_t q_full, q_empty;
   uint64_t k_full[kMaxUnits], k_empty[kMaxUnits], v_full[kMaxUnits], v_empty[kMaxUnits];
-  uint64_t s_full[2], p_full[2];
-  uint64_t o_full, o_item, drain, drain2;
-  uint64_t pv_iss[2];                    // PV of the tile issued (S buffer may be overwritten)
-  uint64_t xch[2];                       // exchanges between the two softmax warpgroups
+  uint64_t s_full[NS], p_full[NS];
+  uint64_t pv_iss[NS];                   // PV of the tile issued (its S buffer may be overwritten)
+  uint64_t o_full[2];                    // PV of tile t complete, alternating by t & 1
+  uint64_t o_item, drain, drain2;
+  uint64_t xch[2];                       // exchanges between the softmax warpgroups
   int32_t sched_n[4];                    // tile count of item ord at [ord & 3] (0: end of stream)
   uint32_t tmem_base;
   int abort;
 };
 
 template <class C>
-constexpr int smem_bytes() { return C::OFF_CTRL + (int)sizeof(Ctrl); }
+constexpr int smem_bytes() { return C::OFF_CTRL + (int)sizeof(Ctrl<C::NSW, C::NS>); }
 
 struct Item {
   int s, hk, qstart, qlen, qpos_lo, seq_len, ctx;
@@ -267,7 +277,7 @@ __device__ inline void row_setup(const AttnArgs &a, const Item &it, int row, int
 }
 
 template <class C>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(C::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const int G, const int n_items) {
   // Everything lives in dynamic shared memory, which starts 1024-byte aligned
@@ -275,7 +285,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   // swizzled tiles need that alignment and there is no room for slack.
   extern __shared__ __align__(1024) uint8_t dsm_ptr[];
   const uint32_t dsm = smem_u32(dsm_ptr);
-  Ctrl &ctl = *reinterpret_cast<Ctrl *>(dsm_ptr + C::OFF_CTRL);
+  Ctrl<C::NSW, C::NS> &ctl = *reinterpret_cast<Ctrl<C::NSW, C::NS> *>(dsm_ptr + C::OFF_CTRL);
   const uint32_t q_s = dsm + C::OFF_Q;
   const uint32_t k_s = dsm + C::OFF_K;
   const uint32_t v_s = dsm + C::OFF_V;
@@ -298,17 +308,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(smem_u32(&ctl.v_full[i]), 1);
       mbar_init(smem_u32(&ctl.v_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::NS; ++i) {
       mbar_init(smem_u32(&ctl.s_full[i]), 1);
-      mbar_init(smem_u32(&ctl.p_full[i]), 256);
-      mbar_init(smem_u32(&ctl.xch[i]), 256);
+      mbar_init(smem_u32(&ctl.p_full[i]), 128 * C::NSW);
+      mbar_init(smem_u32(&ctl.pv_iss[i]), 1);
     }
-    mbar_init(smem_u32(&ctl.o_full), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&ctl.xch[i]), 128 * C::NSW);
+      mbar_init(smem_u32(&ctl.o_full[i]), 1);
+    }
     mbar_init(smem_u32(&ctl.o_item), 1);
     mbar_init(smem_u32(&ctl.drain), 1);
     mbar_init(smem_u32(&ctl.drain2), 1);
-    mbar_init(smem_u32(&ctl.pv_iss[0]), 1);
-    mbar_init(smem_u32(&ctl.pv_iss[1]), 1);
     mbar_fence_init();
     tma_prefetch_map(&tm_q);
     tma_prefetch_map(&tm_k);
@@ -330,7 +341,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   // warpgroup executes it converged; the freed registers are handed over at
   // once, so the increase never waits on work of the other side).
   if (warp < kFirstSoftmaxWarp) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLowRegs));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::LOW_REGS));
   const bool k_warp = warp == 0 || (warp >= 2 && warp < 1 + C::KW);
   const bool v_warp = warp >= 4 && warp < 4 + C::VW;
   if (k_warp || v_warp) {
@@ -463,13 +474,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (n == 0) break;
         tc_fence_after();
         for (int j = 0; ok && j < n; ++j, ++t) {
-          if (t >= 2) {
-            ok = mbar_wait(smem_u32(&ctl.pv_iss[t & 1]), (uint32_t)(((t - 2) >> 1) & 1), abort_flag, gerr,
+          const int sb = (int)(t % C::NS);               // S buffer of tile t
+          if (t >= C::NS) {
+            ok = mbar_wait(smem_u32(&ctl.pv_iss[sb]), (uint32_t)(((t / C::NS) - 1) & 1), abort_flag, gerr,
                            kWaitLimitNs);
             if (!ok) break;
             tc_fence_after();
           }
-          const uint32_t d = tmem + C::TM_S + (uint32_t)(t & 1) * C::N;
+          const uint32_t d = tmem + C::TM_S + (uint32_t)sb * C::N;
           for (int half = 0; ok && half < 2; ++half) {
             const int64_t u = 2 * t + half;
             const int slot = (int)(u % C::KSU);
@@ -488,7 +500,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mma_commit(smem_u32(&ctl.k_empty[slot]));
           }
           if (!ok) break;
-          mma_commit(smem_u32(&ctl.s_full[t & 1]));
+          mma_commit(smem_u32(&ctl.s_full[sb]));
           if (j == n - 1) mma_commit(smem_u32(&ctl.q_empty));   // the item's Q is no longer read
         }
         ++ord;
@@ -511,14 +523,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         block_keys(a, it, 0, 1, false, kmin, kmax);
         const int n_tiles = kmax / C::N - kmin / C::N + 1;
         for (int j = 0; ok && j < n_tiles; ++j, ++t) {
-          ok = mbar_wait(smem_u32(&ctl.p_full[t & 1]), (uint32_t)((t >> 1) & 1), abort_flag, gerr, kWaitLimitNs);
+          const int sb = (int)(t % C::NS);
+          ok = mbar_wait(smem_u32(&ctl.p_full[sb]), (uint32_t)((t / C::NS) & 1), abort_flag, gerr, kWaitLimitNs);
           for (int half = 0; ok && half < 2; ++half) {
             const int64_t u = 2 * t + half;
             const int slot = (int)(u % C::VSU);
             ok = mbar_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1), abort_flag, gerr, kWaitLimitNs);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t p_t = tmem + C::TM_S + (uint32_t)(t & 1) * C::N + half * (C::VU_KEYS / 16) * 8;
+            const uint32_t p_t = tmem + C::TM_S + (uint32_t)sb * C::N + half * (C::VU_KEYS / 16) * 8;
             const uint32_t vb = v_s + slot * C::UNIT;
 #pragma unroll
             for (int kk = 0; kk < C::VU_KEYS / 16; ++kk)
@@ -527,10 +540,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mma_commit(smem_u32(&ctl.v_empty[slot]));
           }
           if (!ok) break;
-          mma_commit(smem_u32(&ctl.o_full));
+          mma_commit(smem_u32(&ctl.o_full[t & 1]));
           if (j == n_tiles - 1) mma_commit(smem_u32(&ctl.o_item));   // the item's O is final
           tc_fence_before();
-          mbar_arrive(smem_u32(&ctl.pv_iss[t & 1]));
+          mbar_arrive(smem_u32(&ctl.pv_iss[sb]));
         }
       }
       if (!ok) {
@@ -543,16 +556,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   }
   // warp 7 has no role: it only gives its registers to the softmax
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kHighRegs));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::HIGH_REGS));
     // =============================== softmax ====================================
     // Two warpgroups share every row: warpgroup h owns S columns
     // [h*N/2, (h+1)*N/2) and O columns [h*D/2, (h+1)*D/2).  Both keep the
     // same running max (half-row maxima are exchanged through shared memory
     // once per tile, ordered by a bounded mbarrier) and a partial row sum.
-    constexpr int NH = C::N / 2;
-    constexpr int DH = C::D / 2;
+    constexpr int NSW = C::NSW;
+    constexpr int NH = C::N / NSW;                       // S columns of one warpgroup
+    constexpr int DH = C::D / NSW;                       // O columns of one warpgroup
+    constexpr int EPW = DH < 64 ? DH : 64;               // O columns per epilogue pass
     const int h = (warp - kFirstSoftmaxWarp) >> 2;
-    const int sid = threadIdx.x - 32 * kFirstSoftmaxWarp;   // 0..255 over both warpgroups
+    const int sid = threadIdx.x - 32 * kFirstSoftmaxWarp;   // 0 .. 128 * NSW - 1
     const int row = 32 * (warp & 3) + lane;              // TMEM lane of this thread
     const uint32_t lane_t = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = a.scale * kLog2e;
@@ -582,13 +597,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       for (int j = 0; j < n_tiles; ++j, ++t) {
         const int kt0 = (tile_lo + j) * C::N;
         const int kc0 = kt0 + h * NH;                    // key of this warpgroup's first column
-        ok = mbar_wait(smem_u32(&ctl.s_full[t & 1]), (uint32_t)((t >> 1) & 1), abort_flag, gerr, kWaitLimitNs);
+        const int sb = (int)(t % C::NS);                 // S buffer of tile t
+        ok = mbar_wait(smem_u32(&ctl.s_full[sb]), (uint32_t)((t / C::NS) & 1), abort_flag, gerr, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         uint32_t raw[NH];
 #pragma unroll
         for (int c = 0; c < NH / 32; ++c)
-          tmem_ld32(tmem + lane_t + C::TM_S + (uint32_t)(t & 1) * C::N + h * NH + 32 * c,
+          tmem_ld32(tmem + lane_t + C::TM_S + (uint32_t)sb * C::N + h * NH + 32 * c,
                     *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
         tmem_wait_ld();
         float x[NH];
@@ -611,7 +627,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_arrive(smem_u32(&ctl.xch[xc & 1]));
         ok = mbar_wait_spin(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag, gerr, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        mx = fmaxf(mx, ctl.red[xc & 1][h ^ 1][row]);
+#pragma unroll
+        for (int g = 0; g < NSW; ++g)
+          if (g != h) mx = fmaxf(mx, ctl.red[xc & 1][g][row]);
         ++xc;
         const float m_new = fmaxf(m_used, mx);
         const bool need = m_new > m_used + 8.f;           // also true on the first visible tile
@@ -625,7 +643,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           const float m_next = need ? m_new : m_used;
           const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_next);
           if (j > 0) {
-            ok = mbar_wait(smem_u32(&ctl.o_full), (uint32_t)((t - 1) & 1), abort_flag, gerr, kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.o_full[(t - 1) & 1]), (uint32_t)(((t - 1) >> 1) & 1), abort_flag, gerr,
+                           kWaitLimitNs);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll 1
@@ -657,7 +676,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           // them.  Once PV_{t-1} is done every earlier unit of each V slot has
           // been consumed, so the v_full parity below is unambiguous.
           if (j > 0) {
-            ok = mbar_wait(smem_u32(&ctl.o_full), (uint32_t)((t - 1) & 1), abort_flag, gerr, kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.o_full[(t - 1) & 1]), (uint32_t)(((t - 1) >> 1) & 1), abort_flag, gerr,
+                           kWaitLimitNs);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           }
           for (int half = 0; half < 2 && ok; ++half) {
@@ -670,7 +690,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (!ok) break;
             const int r0 = max(0, it.seq_len - k0);
             const int n16 = (C::VU_KEYS - r0) * 8 * C::CH;
-            for (int i = sid; i < n16; i += 256) {
+            for (int i = sid; i < n16; i += 128 * NSW) {
               const int c = i / ((C::VU_KEYS - r0) * 8), rem = i % ((C::VU_KEYS - r0) * 8);
               uint4 *dst = reinterpret_cast<uint4 *>(dsm_ptr + C::OFF_V + slot * C::UNIT + c * C::VU_CHUNK +
                                                      (r0 + rem / 8) * 128 + (rem % 8) * 16);
@@ -680,13 +700,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           if (!ok) break;
           fence_proxy_async_smem();
         }
+        if constexpr (NH / 2 >= 32) {
 #pragma unroll
-        for (int c = 0; c < NH / 2; c += 32)
-          tmem_st32(tmem + lane_t + C::TM_S + (uint32_t)(t & 1) * C::N + h * (NH / 2) + c,
-                    *reinterpret_cast<const uint32_t(*)[32]>(pk + c));
+          for (int c = 0; c < NH / 2; c += 32)
+            tmem_st32(tmem + lane_t + C::TM_S + (uint32_t)sb * C::N + h * (NH / 2) + c,
+                      *reinterpret_cast<const uint32_t(*)[32]>(pk + c));
+        } else {
+          tmem_st16(tmem + lane_t + C::TM_S + (uint32_t)sb * C::N + h * (NH / 2), pk);
+        }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(&ctl.p_full[t & 1]));
+        mbar_arrive(smem_u32(&ctl.p_full[sb]));
       }
       if (!ok) break;
       const bool row_valid = cur.row_valid;
@@ -706,7 +730,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       ok = __all_sync(0xffffffffu, mbar_wait_spin(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag,
                                              gerr, kWaitLimitNs));
       if (!ok) break;
-      l += ctl.red[xc & 1][h ^ 1][row];
+#pragma unroll
+      for (int g = 0; g < NSW; ++g)
+        if (g != h) l += ctl.red[xc & 1][g][row];
       ++xc;
       // epilogue: O / l -> bf16, 64 columns per pass, 32-byte stores.  The
       // next item's first PV overwrites O only after this thread's P for it
@@ -715,18 +741,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + out_row * C::D + h * DH;
 #pragma unroll 1
-      for (int c = 0; c < DH / 64; ++c) {
-        uint32_t r[64];
-        tmem_ld32(tmem + lane_t + C::TM_O + h * DH + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(r));
-        tmem_ld32(tmem + lane_t + C::TM_O + h * DH + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+      for (int c = 0; c < DH / EPW; ++c) {
+        uint32_t r[EPW];
+#pragma unroll
+        for (int k = 0; k < EPW / 32; ++k)
+          tmem_ld32(tmem + lane_t + C::TM_O + h * DH + EPW * c + 32 * k, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * k));
         tmem_wait_ld();
         if (row_valid) {
-          uint32_t w[32];
+          uint32_t w[EPW / 2];
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
+          for (int e = 0; e < EPW / 2; ++e)
             w[e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) st_global_v8(o + 64 * c + 16 * e, w + 8 * e);
+          for (int e = 0; e < EPW / 16; ++e) st_global_v8(o + EPW * c + 16 * e, w + 8 * e);
         }
       }
       if (row_valid && h == 0 && a.lse != nullptr)
@@ -811,14 +838,14 @@ cudaError_t run(const AttnArgs &a, cudaStream_t st) {
   // The register split hands over exactly the launch allocation: a kernel built
   // with another per-thread count would wait forever in setmaxnreg.inc.
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, attn_tc_kernel<C>) != cudaSuccess || fa.numRegs != kLaunchRegs)
+  if (cudaFuncGetAttributes(&fa, attn_tc_kernel<C>) != cudaSuccess || fa.numRegs != C::LAUNCH_REGS)
     return cudaErrorInvalidConfiguration;
-  attn_tc_kernel<C><<<grid, kThreads, smem, st>>>(mq, mk, mv, a, G, (int)items);
+  attn_tc_kernel<C><<<grid, C::THREADS, smem, st>>>(mq, mk, mv, a, G, (int)items);
   return cudaGetLastError();
 }
 
-using Cfg256 = Cfg<256, 3, 2, 2, 3>;    // 64 KB Q + 3 K + 2 V units of 32 KB
-using Cfg128 = Cfg<128, 6, 6, 1, 1>;    // 32 KB Q + 6 K + 6 V units of 16 KB
+using Cfg256 = Cfg<256, 3, 2, 2, 3, 2, 2>;    // 64 KB Q + 3 K + 2 V units of 32 KB; 2 softmax WGs, 2 S
+using Cfg128 = Cfg<128, 6, 6, 1, 1, 2, 2>;    // 32 KB Q + 6 K + 6 V units of 16 KB; 2 softmax WGs, 2 S
 
 }  // namespace
 
