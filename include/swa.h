@@ -76,27 +76,31 @@ extern "C" {
  *
  * Defined by the vllm-ascend article on _compute_slot_mapping_kernel,
  * section 2 ("non-CP path") and section 1 (the padded tail): for token t of
- * request r, with pos = positions[t],
+ * request r, with pos = positions[t] (or, when positions is NULL,
+ * pos = context_lens[r] + (t - query_start_loc[r]): the request's cached
+ * context followed by its new tokens),
  *     slot_mapping[t] = block_table[r][pos / block_size] * block_size
  *                       + pos % block_size,
  * and slot_mapping[t] = pad_id for t in [num_tokens, max_num_tokens), which
  * keeps the output shape fixed for graph capture.
  *
  *   query_start_loc  int32[num_reqs + 1], CSR offsets of each request's tokens
- *   positions        int64[num_tokens]
+ *   positions        int64[num_tokens], or NULL to derive them
+ *   context_lens     int32[num_reqs]; read only when positions is NULL
  *   block_table      int32[num_reqs, block_table_stride]
  *   slot_mapping     int32[max_num_tokens] (output)
- * Host errors: NULL pointers (except err), num_reqs < 0, num_tokens < 0,
+ * Host errors: NULL pointers (except err, and one of positions /
+ *   context_lens), num_reqs < 0, num_tokens < 0,
  *   max_num_tokens < num_tokens, block_size <= 0, stride < 1.
  * Device errors: a position < 0 or whose page index >= block_table_stride
  *   sets SWA_ERR_POSITION and writes pad_id; query_start_loc that decreases or
  *   passes num_tokens sets SWA_ERR_QSL (tokens outside every request get pad_id).
  */
 int swa_slot_mapping(const int32_t *query_start_loc, const int64_t *positions,
-                     const int32_t *block_table, int64_t block_table_stride,
-                     int32_t block_size, int32_t num_reqs, int64_t num_tokens,
-                     int64_t max_num_tokens, int32_t pad_id, int32_t *slot_mapping,
-                     int32_t *err, void *stream);
+                     const int32_t *context_lens, const int32_t *block_table,
+                     int64_t block_table_stride, int32_t block_size, int32_t num_reqs,
+                     int64_t num_tokens, int64_t max_num_tokens, int32_t pad_id,
+                     int32_t *slot_mapping, int32_t *err, void *stream);
 
 /*
  * swa_slot_mapping_cp -- swa_slot_mapping on one rank of a context-parallel

@@ -70,7 +70,7 @@ SPLIT_ALIGN = 128
 # slot mapping (vllm-ascend slot-mapping article, sections 1, 2 and 5)
 # ---------------------------------------------------------------------------
 def slot_mapping(query_start_loc, positions, block_table, block_size, num_tokens,
-                 max_num_tokens, pad_id=-1):
+                 max_num_tokens, pad_id=-1, context_lens=None):
     """Physical KV slot of every token, then ``pad_id`` over the padded tail.
 
     For token t of request r: block index = pos // block_size, offset =
@@ -78,9 +78,17 @@ def slot_mapping(query_start_loc, positions, block_table, block_size, num_tokens
     offset.  Tokens in ``[num_tokens, max_num_tokens)`` get ``pad_id``.  A
     token whose position is negative or whose block index lies outside the
     request's block-table row is not mapped (it gets ``pad_id``); its index is
-    returned in ``bad``.
+    returned in ``bad``.  With ``positions`` None, the i-th token of request r
+    sits at ``context_lens[r] + i`` (its cached context followed by the new
+    tokens).
     """
     qsl = np.asarray(query_start_loc, dtype=np.int64)
+    if positions is None:
+        ctx = np.asarray(context_lens, dtype=np.int64)
+        positions = np.zeros(int(qsl[-1]) if len(qsl) else 0, dtype=np.int64)
+        for r in range(len(qsl) - 1):
+            for i, t in enumerate(range(int(qsl[r]), int(qsl[r + 1]))):
+                positions[t] = ctx[r] + i
     pos_arr = np.asarray(positions, dtype=np.int64)
     bt = np.asarray(block_table, dtype=np.int64)
     stride = bt.shape[1]

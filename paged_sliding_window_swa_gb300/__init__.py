@@ -34,7 +34,8 @@ ERR_BITS = {0x01: "BLOCK_ID", 0x02: "POSITION", 0x04: "QSL", 0x08: "LENS", 0x10:
 
 _c_i32, _c_i64, _c_f, _c_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 _SIGS = {
-    "swa_slot_mapping": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i64, _c_i64, _c_i32, _c_p, _c_p, _c_p],
+    "swa_slot_mapping": [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i64, _c_i64, _c_i32, _c_p, _c_p,
+                         _c_p],
     "swa_slot_mapping_cp": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i64, _c_i64, _c_i32, _c_i32, _c_i32,
                             _c_i32, _c_i32, _c_p, _c_p, _c_p],
     "swa_kv_cache_write": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i64, _c_p, _c_p],
@@ -109,18 +110,28 @@ def _dtype_code(t):
 
 
 def swa_slot_mapping(query_start_loc, positions, block_table, block_size: int, max_num_tokens: int,
-                     *, pad_id: int = -1, out=None, err=None, stream=None):
-    """int32 slots [max_num_tokens]; see ``swa_slot_mapping`` in include/swa.h."""
+                     *, context_lens=None, num_tokens=None, pad_id: int = -1, out=None, err=None,
+                     stream=None):
+    """int32 slots [max_num_tokens]; see ``swa_slot_mapping`` in include/swa.h.
+
+    ``positions`` None: token i of request r sits at ``context_lens[r] + i``;
+    ``num_tokens`` must then be given (no device read is made to find it)."""
     _dev(query_start_loc, "query_start_loc", torch.int32)
     _dev(positions, "positions", torch.int64)
+    _dev(context_lens, "context_lens", torch.int32)
     _dev(block_table, "block_table", torch.int32)
+    if positions is None:
+        if context_lens is None or num_tokens is None:
+            raise SwaError("swa_slot_mapping: without positions, context_lens and num_tokens are required")
+    else:
+        num_tokens = positions.numel()
     if out is None:
-        out = torch.empty(max_num_tokens, dtype=torch.int32, device=positions.device)
+        out = torch.empty(max_num_tokens, dtype=torch.int32, device=block_table.device)
     _dev(out, "out", torch.int32)
     _dev(err, "err", torch.int32)
-    rc = lib().swa_slot_mapping(_ptr(query_start_loc), _ptr(positions), _ptr(block_table),
+    rc = lib().swa_slot_mapping(_ptr(query_start_loc), _ptr(positions), _ptr(context_lens), _ptr(block_table),
                                 block_table.shape[1], block_size, query_start_loc.numel() - 1,
-                                positions.numel(), max_num_tokens, pad_id, _ptr(out), _ptr(err),
+                                int(num_tokens), max_num_tokens, pad_id, _ptr(out), _ptr(err),
                                 _stream(stream))
     _check(rc, "swa_slot_mapping")
     return out

@@ -24,18 +24,19 @@ extern "C" {
 const char *swa_version(void) { return "swa-gb300 0.1 sm_103a"; }
 
 int swa_slot_mapping(const int32_t *query_start_loc, const int64_t *positions,
-                     const int32_t *block_table, int64_t block_table_stride, int32_t block_size,
-                     int32_t num_reqs, int64_t num_tokens, int64_t max_num_tokens, int32_t pad_id,
-                     int32_t *slot_mapping, int32_t *err, void *stream) {
+                     const int32_t *context_lens, const int32_t *block_table, int64_t block_table_stride,
+                     int32_t block_size, int32_t num_reqs, int64_t num_tokens, int64_t max_num_tokens,
+                     int32_t pad_id, int32_t *slot_mapping, int32_t *err, void *stream) {
   if (num_reqs < 0 || num_tokens < 0 || max_num_tokens < num_tokens || block_size <= 0 ||
       block_table_stride < 1)
     return SWA_E_SIZE;
   if (max_num_tokens == 0) return SWA_OK;
   if (slot_mapping == nullptr || query_start_loc == nullptr) return SWA_E_NULL;
-  if (num_tokens > 0 && (positions == nullptr || block_table == nullptr)) return SWA_E_NULL;
+  if (num_tokens > 0 && ((positions == nullptr && context_lens == nullptr) || block_table == nullptr))
+    return SWA_E_NULL;
   if (max_num_tokens > INT32_MAX) return SWA_E_SIZE;
-  return finish(swa::launch_slot_mapping(query_start_loc, positions, block_table, block_table_stride,
-                                         block_size, num_reqs, num_tokens, max_num_tokens, pad_id,
+  return finish(swa::launch_slot_mapping(query_start_loc, positions, positions ? nullptr : context_lens, block_table,
+                                         block_table_stride, block_size, num_reqs, num_tokens, max_num_tokens, pad_id,
                                          slot_mapping, err, as_stream(stream)));
 }
 
@@ -56,7 +57,7 @@ int swa_slot_mapping_cp(const int32_t *query_start_loc, const int64_t *positions
   if (num_tokens > 0 && (positions == nullptr || block_table == nullptr)) return SWA_E_NULL;
   if (max_num_tokens > INT32_MAX) return SWA_E_SIZE;
   const swa::CpArgs cp{kv_cache_block_size, cp_world_size, cp_rank, cp_interleave};
-  return finish(swa::launch_slot_mapping(query_start_loc, positions, block_table, block_table_stride,
+  return finish(swa::launch_slot_mapping(query_start_loc, positions, nullptr, block_table, block_table_stride,
                                          block_size, num_reqs, num_tokens, max_num_tokens, pad_id,
                                          slot_mapping, err, as_stream(stream), &cp));
 }

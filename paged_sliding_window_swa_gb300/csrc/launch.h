@@ -33,7 +33,8 @@ struct CpArgs {
   int32_t kv_cache_block_size, world, rank, interleave;
 };
 
-cudaError_t launch_slot_mapping(const int32_t *qsl, const int64_t *pos, const int32_t *bt,
+// pos == nullptr: token i of request r sits at ctx[r] + i.
+cudaError_t launch_slot_mapping(const int32_t *qsl, const int64_t *pos, const int32_t *ctx, const int32_t *bt,
                                 int64_t stride, int32_t block_size, int32_t num_reqs,
                                 int64_t num_tokens, int64_t max_num_tokens, int32_t pad_id,
                                 int32_t *out, int32_t *err, cudaStream_t st, const CpArgs *cp = nullptr);

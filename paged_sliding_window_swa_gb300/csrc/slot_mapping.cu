@@ -43,10 +43,10 @@ struct Geom {
   int32_t vbs_shift, inter_shift, wi_shift;   // kCpPow2: log2 of vbs, interleave, world * interleave
 };
 
-template <bool kVec, int kMode>
+template <bool kVec, int kMode, bool kDerive>
 __global__ void __launch_bounds__(kThreads)
 slot_mapping_kernel(const int32_t *__restrict__ qsl, const int64_t *__restrict__ pos,
-                    const int32_t *__restrict__ bt, int64_t stride, const Geom g,
+                    const int32_t *__restrict__ ctx, const int32_t *__restrict__ bt, int64_t stride, const Geom g,
                     int32_t num_reqs, int64_t num_tokens, int64_t max_num_tokens, int32_t pad_id,
                     int32_t *__restrict__ out, int32_t *__restrict__ err) {
   const int32_t block_size = g.block_size;
@@ -64,8 +64,13 @@ slot_mapping_kernel(const int32_t *__restrict__ qsl, const int64_t *__restrict__
 #pragma unroll
     for (int i = 0; i < kTokPerThread; ++i) res[i] = pad_id;
   } else {
+    // positions: given, or (kDerive) the request's context length plus the
+    // token's index in the request
     int64_t p[kTokPerThread];
-    if (kVec && t0 + kTokPerThread <= num_tokens) {
+    if (kDerive) {
+#pragma unroll
+      for (int i = 0; i < kTokPerThread; ++i) p[i] = 0;
+    } else if (kVec && t0 + kTokPerThread <= num_tokens) {
       const longlong2 *src = reinterpret_cast<const longlong2 *>(pos + t0);
 #pragma unroll
       for (int i = 0; i < kTokPerThread / 2; ++i) {
@@ -78,7 +83,8 @@ slot_mapping_kernel(const int32_t *__restrict__ qsl, const int64_t *__restrict__
       for (int i = 0; i < kTokPerThread; ++i) p[i] = (t0 + i < num_tokens) ? __ldg(pos + t0 + i) : 0;
     }
     int r = find_req(qsl, num_reqs, t0);
-    int32_t r_end = __ldg(qsl + r + 1);
+    int32_t r_start = __ldg(qsl + r), r_end = __ldg(qsl + r + 1);
+    int32_t r_ctx = kDerive ? __ldg(ctx + r) : 0;
     int64_t last = -1;                                       // (request, page) of the last lookup
     int32_t blk = 0;
 #pragma unroll
@@ -86,9 +92,14 @@ slot_mapping_kernel(const int32_t *__restrict__ qsl, const int64_t *__restrict__
       const int64_t t = t0 + i;
       res[i] = pad_id;
       if (t >= num_tokens) continue;
-      while (r + 1 < num_reqs && t >= r_end) { ++r; r_end = __ldg(qsl + r + 1); }
-      if (t < __ldg(qsl + r) || t >= r_end) continue;        // outside every request
-      const int64_t ps = p[i];
+      while (r + 1 < num_reqs && t >= r_end) {
+        ++r;
+        r_start = r_end;
+        r_end = __ldg(qsl + r + 1);
+        if (kDerive) r_ctx = __ldg(ctx + r);
+      }
+      if (t < r_start || t >= r_end) continue;              // outside every request
+      const int64_t ps = kDerive ? (int64_t)r_ctx + (t - r_start) : p[i];
       if (ps < 0) { report(err, SWA_ERR_POSITION); continue; }
       int64_t page, off;
       if (kMode == kCpPow2) {
@@ -144,14 +155,14 @@ slot_mapping_kernel(const int32_t *__restrict__ qsl, const int64_t *__restrict__
 
 }  // namespace
 
-cudaError_t launch_slot_mapping(const int32_t *qsl, const int64_t *pos, const int32_t *bt,
+cudaError_t launch_slot_mapping(const int32_t *qsl, const int64_t *pos, const int32_t *ctx, const int32_t *bt,
                                 int64_t stride, int32_t block_size, int32_t num_reqs,
                                 int64_t num_tokens, int64_t max_num_tokens, int32_t pad_id,
                                 int32_t *out, int32_t *err, cudaStream_t st, const CpArgs *cp) {
   const int64_t work = max(ceil_div(max_num_tokens, kTokPerThread), (int64_t)num_reqs);
   if (work == 0) return cudaSuccess;
   const unsigned grid = (unsigned)ceil_div(work, kThreads);
-  const bool vec = ((uintptr_t)pos % 16 == 0) && ((uintptr_t)out % 16 == 0);   // t0 is a multiple of 8
+  const bool vec = ((uintptr_t)pos % 16 == 0) && ((uintptr_t)out % 16 == 0);   // t0 is a multiple of 8 (a null pos is aligned)
   Geom g{};
   g.block_size = block_size;
   while (g.shift < 30 && (1 << g.shift) < block_size) ++g.shift;
@@ -174,13 +185,18 @@ cudaError_t launch_slot_mapping(const int32_t *qsl, const int64_t *pos, const in
                       log2_exact(g.world) >= 0;
     mode = pow2 ? kCpPow2 : kCp;
   }
-  using K = void (*)(const int32_t *, const int64_t *, const int32_t *, int64_t, const Geom, int32_t, int64_t,
-                     int64_t, int32_t, int32_t *, int32_t *);
-  const K table[2][4] = {{slot_mapping_kernel<false, kPlainPow2>, slot_mapping_kernel<false, kPlain>,
-                          slot_mapping_kernel<false, kCp>, slot_mapping_kernel<false, kCpPow2>},
-                         {slot_mapping_kernel<true, kPlainPow2>, slot_mapping_kernel<true, kPlain>,
-                          slot_mapping_kernel<true, kCp>, slot_mapping_kernel<true, kCpPow2>}};
-  table[vec ? 1 : 0][mode]<<<grid, kThreads, 0, st>>>(qsl, pos, bt, stride, g, num_reqs, num_tokens,
+  using K = void (*)(const int32_t *, const int64_t *, const int32_t *, const int32_t *, int64_t, const Geom,
+                     int32_t, int64_t, int64_t, int32_t, int32_t *, int32_t *);
+  const K table[2][4] = {{slot_mapping_kernel<false, kPlainPow2, false>, slot_mapping_kernel<false, kPlain, false>,
+                          slot_mapping_kernel<false, kCp, false>, slot_mapping_kernel<false, kCpPow2, false>},
+                         {slot_mapping_kernel<true, kPlainPow2, false>, slot_mapping_kernel<true, kPlain, false>,
+                          slot_mapping_kernel<true, kCp, false>, slot_mapping_kernel<true, kCpPow2, false>}};
+  // derived positions (plain mapping only): no position reads; vector stores when out is aligned
+  const K derived[2][2] = {{slot_mapping_kernel<false, kPlainPow2, true>, slot_mapping_kernel<false, kPlain, true>},
+                           {slot_mapping_kernel<true, kPlainPow2, true>, slot_mapping_kernel<true, kPlain, true>}};
+  const K fn = (pos == nullptr && cp == nullptr) ? derived[(uintptr_t)out % 16 == 0 ? 1 : 0][mode]
+                                                 : table[vec ? 1 : 0][mode];
+  fn<<<grid, kThreads, 0, st>>>(qsl, pos, ctx, bt, stride, g, num_reqs, num_tokens,
                                                        max_num_tokens, pad_id, out, err);
   return cudaGetLastError();
 }

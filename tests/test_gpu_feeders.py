@@ -52,6 +52,39 @@ def test_slot_mapping_named_layouts(name, err):
     assert np.array_equal(out.cpu().numpy(), ref) and bad == [] and err.item() == 0
 
 
+@pytest.mark.parametrize("name", ["tiny", "gemma_like", "chunked_prefill", "decode"])
+def test_slot_mapping_derived_positions_named_layouts(name, err):
+    """positions = NULL: context length + index, the same slots as the layout's
+    explicit positions (which are exactly that)."""
+    lay = W.NAMED[name]()
+    d = W.device_layout(lay, "cuda")
+    out = swa.swa_slot_mapping(d["query_start_loc"], None, d["block_table"], lay.block_size, lay.max_num_tokens,
+                               context_lens=d["context_lens"], num_tokens=lay.num_tokens, err=err)
+    ref, bad = O.slot_mapping(lay.query_start_loc, None, lay.block_table, lay.block_size, lay.num_tokens,
+                              lay.max_num_tokens, context_lens=lay.context_lens)
+    assert np.array_equal(out.cpu().numpy(), ref) and bad == [] and err.item() == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_slot_mapping_derived_positions_random(seed, err):
+    """Random context lengths, some past the block-table row (reported, pad_id)."""
+    rng = np.random.default_rng(40 + seed)
+    S, B = int(rng.integers(1, 7)), int(rng.choice([16, 32, 64]))
+    qlen = rng.integers(0, 500, size=S)
+    ctx = rng.integers(0, 3000, size=S)
+    qsl = np.concatenate([[0], np.cumsum(qlen)])
+    stride = int(-(-(ctx + qlen).max() // B)) - (1 if seed % 3 == 0 else 0)   # sometimes one page short
+    stride = max(stride, 1)
+    bt = rng.permutation(S * stride + 5)[:S * stride].reshape(S, stride)
+    T = int(qsl[-1])
+    maxn = T + int(rng.integers(0, 33))
+    out = swa.swa_slot_mapping(_i32(qsl), None, _i32(bt), B, maxn, context_lens=_i32(ctx), num_tokens=T, err=err)
+    ref, bad = O.slot_mapping(qsl, None, bt, B, T, maxn, context_lens=ctx)
+    assert np.array_equal(out.cpu().numpy(), ref)
+    torch.cuda.synchronize()
+    assert bool(err.item() & 0x02) == bool(bad)
+
+
 @pytest.mark.parametrize("seed", range(12))
 @pytest.mark.parametrize("misaligned", [False, True])
 def test_slot_mapping_random(seed, misaligned, err):
@@ -224,3 +257,16 @@ def test_lse_combine_large_sampled():
     l = lse[ts].cpu().numpy()
     fin = np.isfinite(rl)
     assert np.array_equal(np.isfinite(l), fin) and np.abs(l[fin] - rl[fin]).max() < 1e-4
+
+
+def test_slot_mapping_derived_positions_misaligned_output(err):
+    """An output buffer at a 4-byte offset takes the scalar store path."""
+    lay = W.random_small(3, max_seqs=4, max_q=300)
+    d = W.device_layout(lay, "cuda")
+    buf = torch.full((lay.max_num_tokens + 1,), 7, dtype=torch.int32, device="cuda")
+    out = buf[1:]
+    swa.swa_slot_mapping(d["query_start_loc"], None, d["block_table"], lay.block_size, lay.max_num_tokens,
+                         context_lens=d["context_lens"], num_tokens=lay.num_tokens, out=out, err=err)
+    ref, _ = O.slot_mapping(lay.query_start_loc, None, lay.block_table, lay.block_size, lay.num_tokens,
+                            lay.max_num_tokens, context_lens=lay.context_lens)
+    assert np.array_equal(out.cpu().numpy(), ref) and buf[0].item() == 7 and err.item() == 0

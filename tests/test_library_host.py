@@ -53,10 +53,13 @@ def test_version(lib):
 
 
 def test_slot_mapping_rejects_bad_sizes(lib):
-    assert lib.swa_slot_mapping(NULL, NULL, NULL, 4, 16, 1, 10, 5, -1, NULL, NULL, NULL) == -2
-    assert lib.swa_slot_mapping(NULL, NULL, NULL, 4, 0, 1, 10, 20, -1, NULL, NULL, NULL) == -2
-    assert lib.swa_slot_mapping(NULL, NULL, NULL, 4, 16, 1, 10, 20, -1, NULL, NULL, NULL) == -1
-    assert lib.swa_slot_mapping(NULL, NULL, NULL, 4, 16, 0, 0, 0, -1, NULL, NULL, NULL) == 0
+    assert lib.swa_slot_mapping(NULL, NULL, NULL, NULL, 4, 16, 1, 10, 5, -1, NULL, NULL, NULL) == -2
+    assert lib.swa_slot_mapping(NULL, NULL, NULL, NULL, 4, 0, 1, 10, 20, -1, NULL, NULL, NULL) == -2
+    assert lib.swa_slot_mapping(NULL, NULL, NULL, NULL, 4, 16, 1, 10, 20, -1, NULL, NULL, NULL) == -1
+    assert lib.swa_slot_mapping(NULL, NULL, NULL, NULL, 4, 16, 0, 0, 0, -1, NULL, NULL, NULL) == 0
+    # positions or context lengths: one of the two is needed once there are tokens
+    p = ctypes.c_void_p(0x1000)
+    assert lib.swa_slot_mapping(p, NULL, NULL, p, 4, 16, 1, 10, 20, -1, p, NULL, NULL) == -1
 
 
 def test_tile_bounds_rejects_bad_sizes(lib):

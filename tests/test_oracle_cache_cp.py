@@ -160,3 +160,23 @@ def test_rank_split_decode_merges_to_full_attention(W, I):
         for h in range(hq):
             assert np.allclose(mo[s, h], full_out[(s, h)], atol=1e-12)
             assert abs(ml[s, h] - full_lse[(s, h)]) < 1e-12
+
+
+def test_slot_mapping_positions_derived_from_context_lengths():
+    """Without positions, request r's i-th token sits after its cached context:
+    the same slots as explicit positions ctx[r] + i; a worked case by hand."""
+    bt = np.array([[5, 2, 9], [7, 1, 0]])
+    qsl = [0, 3, 5]
+    ctx = [14, 0]                                   # request 0: positions 14, 15, 16; request 1: 0, 1
+    got, bad = O.slot_mapping(qsl, None, bt, 8, 5, 8, context_lens=ctx)
+    # 14 -> page 1 (block 2) offset 6 = 22; 15 -> 23; 16 -> page 2 (block 9) offset 0 = 72; 0 -> 56; 1 -> 57
+    assert got.tolist() == [22, 23, 72, 56, 57, -1, -1, -1] and bad == []
+    rng = np.random.default_rng(9)
+    for _ in range(5):
+        qsl, pos, bt = _random_requests(rng, 3, 200, 16)
+        ctxs = rng.integers(0, 300, size=3)
+        explicit = np.concatenate([ctxs[r] + np.arange(int(qsl[r + 1] - qsl[r])) for r in range(3)])
+        bt = np.tile(np.arange(64), (3, 1))
+        a, ba = O.slot_mapping(qsl, None, bt, 16, int(qsl[-1]), int(qsl[-1]) + 4, context_lens=ctxs)
+        b, bb = O.slot_mapping(qsl, explicit, bt, 16, int(qsl[-1]), int(qsl[-1]) + 4)
+        assert np.array_equal(a, b) and ba == bb
