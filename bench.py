@@ -209,6 +209,22 @@ class PrefillStep:
         torch.cuda.synchronize(self.dev)
 
 
+def max_over_ranks(ms, world, device):
+    """The job's time: the slowest rank's (a MAX all-reduce over the process
+    group; NCCL needs a CUDA tensor, gloo a CPU one)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, ms):
+    """Units per second of the whole job: every replica processes the same
+    number of units in the (max-over-ranks) time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -257,10 +273,7 @@ def run_gpu(args, rank, world, local_rank):
     clk = clocks.stop()
     attn_ms = [a.elapsed_time(b) for _, a, b in ev]
     feed_ms = [a.elapsed_time(b) for a, b, _ in ev]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
 
     # end to end through the public API: pinned host inputs -> device -> three
@@ -305,11 +318,8 @@ def run_e2e(args, step, flops, barrier, stream, world, dev):
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    return {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    return {"value": round(job_rate(flops, world, e2e_ms) / 1e12, 3), "unit": UNIT,
             "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
@@ -317,8 +327,8 @@ def report_line(args, lay, step, flops, pairs, ms_per_step, attn_ms, feed_ms, cl
     pk = peaks()
     attn_avg = statistics.mean(attn_ms)
     achieved = flops / (attn_avg * 1e-3) / 1e12
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
-    tok_s = world * lay.num_tokens / (ms_per_step * 1e-3)
+    value = job_rate(flops, world, ms_per_step) / 1e12
+    tok_s = job_rate(lay.num_tokens, world, ms_per_step)
     line = {
         "metric": METRIC,
         "value": round(value, 3),
