@@ -9,7 +9,9 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * Ownership.  Every array argument is a DEVICE pointer owned by the caller.
- *   The library allocates no memory and keeps no pointer after a call returns.
+ *   The library allocates no memory and keeps no pointer after a call returns
+ *   (swa_mm_paged_attention_split_static works in a fixed array of its own
+ *   instead, allocated when the library is loaded; see there).
  * Streams.  `stream` is a cudaStream_t passed as void*; NULL means the legacy
  *   default stream.  Each call only enqueues work on `stream` and never
  *   synchronises the host.
@@ -52,6 +54,8 @@ extern "C" {
 #define SWA_E_UNSUPPORTED -3   /* dtype / head_dim / block_size not built         */
 #define SWA_E_ALIGN       -4   /* a pointer is not 16-byte aligned               */
 #define SWA_E_CUDA        -5   /* the CUDA runtime or driver reported an error    */
+#define SWA_E_SCRATCH     -6   /* the call needs more than the library's fixed
+                                  scratch array holds (see below)                 */
 
 /* ---- device-side error bits (atomicOr into *err) ------------------------ */
 #define SWA_ERR_BLOCK_ID   0x01  /* block_table entry outside [0, num_blocks)      */
@@ -290,6 +294,49 @@ int swa_mm_paged_attention(const void *q, const void *k_cache, const void *v_cac
 int lse_combine(const void *partial_out, const float *partial_lse, int32_t num_splits,
                 int64_t num_tokens, int32_t num_heads, int32_t head_dim, int32_t dtype,
                 void *out, float *out_lse, void *stream);
+
+/*
+ * swa_mm_paged_attention_split_static -- split-KV attention followed by its
+ * LSE merge, with no device allocation by anyone.
+ *
+ * The pages have no counterpart of this call; it is a convenience for callers
+ * that cannot allocate device memory when they run attention: an engine whose
+ * allocator reserved the device up front, a plugin host that hands its kernels
+ * fixed buffers and forbids allocation while enqueuing, or a loop that cannot
+ * take the device-wide synchronisation of cudaMalloc / cudaFree.  The split
+ * partials (partial_out, partial_lse of swa_mm_paged_attention) live in a
+ * library-owned array of SWA_STATIC_SCRATCH_BYTES bytes that every GPU loading
+ * the library holds until the process exits.  The result equals
+ * swa_mm_paged_attention with num_splits > 1 followed by lse_combine.
+ *
+ *   arguments as swa_mm_paged_attention, without partial_out / partial_lse;
+ *   num_splits >= 2; out [num_tokens, Hq, D] (dtype) and lse fp32
+ *   [num_tokens, Hq] (or NULL) are the caller's, as there.
+ * Scratch needed: round_up(num_splits * num_tokens * Hq * D * elem, 256)
+ *   + num_splits * num_tokens * Hq * 4 bytes (elem 2 for bf16, 4 for fp32);
+ *   more than SWA_STATIC_SCRATCH_BYTES returns SWA_E_SCRATCH and launches
+ *   nothing.
+ * First call on a device: it looks up the array's device address with that
+ *   device current and caches it; make that first call before any stream
+ *   capture.  Later calls do no set-up.
+ * Sharing: every call on a device uses the same array and leaves its contents
+ *   behind.  Calls whose work overlaps on the GPU (two streams, or two host
+ *   threads) race on it; serialise them.  The LSE part is reset to -inf at the
+ *   start of each call.
+ * Errors: those of swa_mm_paged_attention and lse_combine, plus
+ *   SWA_E_SCRATCH; num_splits < 2 is SWA_E_SIZE.  Rows of a sequence rejected
+ *   on the device come out as 0 with lse = -inf.
+ */
+#define SWA_STATIC_SCRATCH_BYTES (16u << 20)
+int swa_mm_paged_attention_split_static(
+    const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
+    const int32_t *block_table, int64_t block_table_stride, const int32_t *query_start_loc,
+    const int32_t *seq_lens, const int32_t *context_lens, const int32_t *mm_ranges,
+    int32_t max_mm_ranges, int32_t num_seqs, int64_t num_tokens, int32_t max_query_len,
+    int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t block_size, int32_t window,
+    int32_t causal, const int32_t *seq_causal, int32_t chunk_size, int32_t chunk_lookback, float scale,
+    int32_t dtype, int32_t num_splits, const int32_t *splits_per_seq, void *out, float *lse,
+    int32_t *err, void *stream);
 
 /* Library version string, e.g. "swa-gb300 0.1 sm_103a". */
 const char *swa_version(void);

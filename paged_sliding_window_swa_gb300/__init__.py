@@ -12,6 +12,8 @@ Entry points (same names as the C ABI):
 * ``swa_tile_bounds``        pruned KV-tile loop range per query block
 * ``swa_mm_paged_attention`` paged attention, SWA + window-clamped image mask
 * ``lse_combine``            merge of split-KV partials by their LSE
+* ``swa_mm_paged_attention_split_static``  split-KV attention and merge with
+  the partials in a library-owned array, for callers that cannot allocate
 """
 from __future__ import annotations
 
@@ -23,12 +25,12 @@ import torch
 from .build_lib import LIB_PATH
 
 __all__ = ["swa_slot_mapping", "swa_slot_mapping_cp", "swa_kv_cache_write", "swa_tile_bounds",
-           "swa_mm_paged_attention", "lse_combine", "lib", "SwaError", "DTYPE_BF16", "DTYPE_FP32", "ERR_BITS"]
+           "swa_mm_paged_attention", "lse_combine", "swa_mm_paged_attention_split_static", "lib", "SwaError", "DTYPE_BF16", "DTYPE_FP32", "ERR_BITS"]
 
 DTYPE_BF16 = 0
 DTYPE_FP32 = 1
 SPLIT_ALIGN = 128
-_RC = {-1: "SWA_E_NULL", -2: "SWA_E_SIZE", -3: "SWA_E_UNSUPPORTED", -4: "SWA_E_ALIGN", -5: "SWA_E_CUDA"}
+_RC = {-1: "SWA_E_NULL", -2: "SWA_E_SIZE", -3: "SWA_E_UNSUPPORTED", -4: "SWA_E_ALIGN", -5: "SWA_E_CUDA", -6: "SWA_E_SCRATCH"}
 ERR_BITS = {0x01: "BLOCK_ID", 0x02: "POSITION", 0x04: "QSL", 0x08: "LENS", 0x10: "TIMEOUT", 0x20: "SPLITS",
             0x40: "INTERNAL", 0x80: "SLOT"}
 
@@ -46,7 +48,13 @@ _SIGS = {
                                _c_p, _c_i32, _c_i32, _c_f, _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_p,
                                _c_p, _c_p],
     "lse_combine": [_c_p, _c_p, _c_i32, _c_i64, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_p],
+    "swa_mm_paged_attention_split_static": [_c_p, _c_p, _c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p,
+                                            _c_i32, _c_i32, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                            _c_i32, _c_i32, _c_p, _c_i32, _c_i32, _c_f, _c_i32, _c_i32, _c_p,
+                                            _c_p, _c_p, _c_p, _c_p],
 }
+# Bytes of the library-owned array behind swa_mm_paged_attention_split_static.
+STATIC_SCRATCH_BYTES = 16 << 20
 EXPORTED = tuple(_SIGS) + ("swa_version",)
 
 
@@ -268,3 +276,42 @@ def lse_combine(partial_out, partial_lse, *, out=None, out_lse=None, return_lse:
                            _ptr(out_lse), _stream(stream))
     _check(rc, "lse_combine")
     return out, out_lse
+
+
+def swa_mm_paged_attention_split_static(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, *,
+                                        context_lens=None, mm_ranges=None, max_query_len=None,
+                                        window: int, causal: bool, scale: float, seq_causal=None,
+                                        chunk_size: int = 0, chunk_lookback: int = -1, num_splits: int,
+                                        splits_per_seq=None, out=None, lse=None, return_lse: bool = True,
+                                        err=None, stream=None):
+    """Split-KV attention merged by LSE in one call that allocates no device
+    memory: the partials live in the library's fixed array, so the caller
+    passes (or here, torch allocates) only ``out`` and ``lse``.  Calls that
+    overlap on the GPU share that array and race; returns (out, lse)."""
+    _dev(q, "q")
+    code = _dtype_code(q)
+    _dev(k_cache, "k_cache", q.dtype)
+    _dev(v_cache, "v_cache", q.dtype)
+    for name, t in (("block_table", block_table), ("query_start_loc", query_start_loc),
+                    ("seq_lens", seq_lens), ("context_lens", context_lens), ("mm_ranges", mm_ranges),
+                    ("splits_per_seq", splits_per_seq), ("seq_causal", seq_causal), ("err", err)):
+        _dev(t, name, torch.int32)
+    T, Hq, D = q.shape
+    num_blocks, B, Hkv, D2 = k_cache.shape
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise SwaError("k/v cache shapes do not match q")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    _dev(out, "out", q.dtype)
+    _dev(lse, "lse", torch.float32)
+    rc = lib().swa_mm_paged_attention_split_static(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), num_blocks, _ptr(block_table), block_table.shape[1],
+        _ptr(query_start_loc), _ptr(seq_lens), _ptr(context_lens), _ptr(mm_ranges),
+        0 if mm_ranges is None else mm_ranges.shape[1], seq_lens.numel(), T,
+        int(T if max_query_len is None else max_query_len), Hq, Hkv, D, B, int(window), int(bool(causal)),
+        _ptr(seq_causal), int(chunk_size), int(chunk_lookback), float(scale), code, int(num_splits),
+        _ptr(splits_per_seq), _ptr(out), _ptr(lse), _ptr(err), _stream(stream))
+    _check(rc, "swa_mm_paged_attention_split_static")
+    return out, lse
