@@ -276,7 +276,7 @@ __device__ inline void row_setup(const AttnArgs &a, const Item &it, int row, int
   }
 }
 
-template <class C>
+template <class C, bool NEG>
 __global__ void __launch_bounds__(C::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const int G, const int n_items) {
@@ -570,11 +570,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int sid = threadIdx.x - 32 * kFirstSoftmaxWarp;   // 0 .. 128 * NSW - 1
     const int row = 32 * (warp & 3) + lane;              // TMEM lane of this thread
     const uint32_t lane_t = (uint32_t)(32 * (warp & 3)) << 16;
-    const float sl2 = a.scale * kLog2e;
     // the scale is folded into the exponent's FFMA: maxima are taken on the raw
-    // scores (of -S for a negative scale) and scaled once
-    const bool neg_scale = sl2 < 0.f;
-    const float asl2 = fmaxf(fabsf(sl2), 1.17549435e-38f);
+    // scores (of -S for a negative scale, NEG) and scaled once
+    const float asl2 = fmaxf(fabsf(a.scale * kLog2e), 1.17549435e-38f);
     int64_t t = 0;                                       // global tile index
     int64_t xc = 0;                                      // exchanges so far (buffer xc & 1)
     int n_done = 0;                                      // items finished
@@ -611,17 +609,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const bool full = klo <= kc0 && khi >= kc0 + NH - 1;
         if (__all_sync(0xffffffffu, full)) {
 #pragma unroll
-          for (int c = 0; c < NH; ++c) x[c] = neg_scale ? -__uint_as_float(raw[c]) : __uint_as_float(raw[c]);
+          for (int c = 0; c < NH; ++c) x[c] = NEG ? -__uint_as_float(raw[c]) : __uint_as_float(raw[c]);
         } else {
 #pragma unroll
           for (int c = 0; c < NH; ++c)
-            x[c] = (kc0 + c >= klo && kc0 + c <= khi) ? (neg_scale ? -__uint_as_float(raw[c]) : __uint_as_float(raw[c]))
+            x[c] = (kc0 + c >= klo && kc0 + c <= khi) ? (NEG ? -__uint_as_float(raw[c]) : __uint_as_float(raw[c]))
                                                       : -INFINITY;
         }
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float m4[4];
 #pragma unroll
-        for (int c = 0; c < NH; ++c) m4[c & 3] = fmaxf(m4[c & 3], x[c]);
-        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        for (int i = 0; i < 4; ++i) m4[i] = x[i];
+#pragma unroll
+        for (int c = 4; c + 8 <= NH; c += 8)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) m4[i] = fmax3(m4[i], x[c + 2 * i], x[c + 2 * i + 1]);
+#pragma unroll
+        for (int c = 4 + ((NH - 4) / 8) * 8; c < NH; ++c) m4[c & 3] = fmaxf(m4[c & 3], x[c]);
+        float mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
         mx = mx == -INFINITY ? -INFINITY : mx * asl2;
         ctl.red[xc & 1][h][row] = mx;
         mbar_arrive(smem_u32(&ctl.xch[xc & 1]));
@@ -662,15 +666,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           m_used = m_next;
         }
         const float ms = (m_used == -INFINITY) ? 0.f : m_used;
+        uint64_t sl2x2, nms;
+        asm volatile("mov.b64 %0, {%1, %1};" : "=l"(sl2x2) : "f"(asl2));
+        asm volatile("mov.b64 %0, {%1, %1};" : "=l"(nms) : "f"(-ms));
         uint32_t pk[NH / 2];
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint64_t s2[2] = {0, 0};
 #pragma unroll
         for (int c = 0; c < NH / 2; ++c) {
-          const float p0 = ex2(fmaf(x[2 * c], asl2, -ms)), p1 = ex2(fmaf(x[2 * c + 1], asl2, -ms));
-          s4[c & 3] += p0 + p1;
+          float e0, e1;
+          f2_unpack(f2_fma(f2_pack(x[2 * c], x[2 * c + 1]), sl2x2, nms), e0, e1);
+          const float p0 = ex2(e0), p1 = ex2(e1);
+          s2[c & 1] = f2_add(s2[c & 1], f2_pack(p0, p1));
           pk[c] = pack_bf16(p0, p1);
         }
-        l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(s2[0], a0, a1);
+          f2_unpack(s2[1], b0, b1);
+          l += (a0 + a1) + (b0 + b1);
+        }
         if (kt0 + C::N > it.seq_len) {
           // keys past the sequence end: their V rows may hold anything; zero
           // them.  Once PV_{t-1} is done every earlier unit of each V slot has
@@ -814,7 +828,7 @@ int sm_count() {
   return n;
 }
 
-template <class C>
+template <class C, bool NEG>
 cudaError_t run(const AttnArgs &a, cudaStream_t st) {
   const int G = a.hq / a.hkv;
   const int bq = C::M / G;
@@ -829,7 +843,7 @@ cudaError_t run(const AttnArgs &a, cudaStream_t st) {
     return cudaErrorInvalidValue;
   constexpr int smem = smem_bytes<C>();
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<C, NEG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t items = (a.num_tokens / bq + a.num_seqs) * (int64_t)a.hkv;
   const int sms = sm_count();
@@ -838,9 +852,9 @@ cudaError_t run(const AttnArgs &a, cudaStream_t st) {
   // The register split hands over exactly the launch allocation: a kernel built
   // with another per-thread count would wait forever in setmaxnreg.inc.
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, attn_tc_kernel<C>) != cudaSuccess || fa.numRegs != C::LAUNCH_REGS)
+  if (cudaFuncGetAttributes(&fa, attn_tc_kernel<C, NEG>) != cudaSuccess || fa.numRegs != C::LAUNCH_REGS)
     return cudaErrorInvalidConfiguration;
-  attn_tc_kernel<C><<<grid, C::THREADS, smem, st>>>(mq, mk, mv, a, G, (int)items);
+  attn_tc_kernel<C, NEG><<<grid, C::THREADS, smem, st>>>(mq, mk, mv, a, G, (int)items);
   return cudaGetLastError();
 }
 
@@ -859,7 +873,10 @@ bool tc_supported(const AttnArgs &a) {
 }
 
 cudaError_t launch_attention_tc(const AttnArgs &a, cudaStream_t st) {
-  return a.head_dim == 256 ? run<Cfg256>(a, st) : run<Cfg128>(a, st);
+  // the sign of the scale is a template argument: a negative scale takes the
+  // maximum of -S, without a per-score select
+  if (a.scale < 0.f) return a.head_dim == 256 ? run<Cfg256, true>(a, st) : run<Cfg128, true>(a, st);
+  return a.head_dim == 256 ? run<Cfg256, false>(a, st) : run<Cfg128, false>(a, st);
 }
 
 }  // namespace swa

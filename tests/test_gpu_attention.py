@@ -215,3 +215,24 @@ def test_repeated_calls_are_bit_identical(err):
         assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
     torch.cuda.synchronize()
     assert err.item() == 0
+
+
+@pytest.mark.parametrize("D,scale", [(256, -0.07), (128, -0.11), (256, 0.0), (128, 0.3)])
+def test_scale_sign_and_zero_all_rows(D, scale, err):
+    """Any finite scale: a negative one (the max is taken on -S), zero (every
+    visible key weighs the same) and a large one, on the tensor-core path."""
+    import paged_sliding_window_swa_gb300 as swa
+    lay = W.random_small(700 + D, head_dim=D, block_size=16, group=2, max_seqs=2, max_ctx=400, max_q=200,
+                         window=150, with_ranges=True, dtype="bf16")
+    q, k, v, d = gpu_inputs(lay)
+    out, lse = swa.swa_mm_paged_attention(
+        q, k, v, d["block_table"], d["query_start_loc"], d["seq_lens"], context_lens=d["context_lens"],
+        mm_ranges=d["mm_ranges"], max_query_len=lay.max_query_len, window=lay.window, causal=lay.causal,
+        scale=scale, err=err)
+    rows = _all_rows(lay)
+    ro, rl = O.attention(q.cpu(), k.cpu(), v.cpu(), lay.block_table, lay.query_start_loc, lay.seq_lens,
+                         lay.mm_ranges, lay.window, lay.causal, scale, rows=rows)
+    e_out, e_lse = max_errors(out, lse, ro, rl, rows)
+    assert e_out <= atol_for(lay) and e_lse <= LSE_ATOL, (e_out, e_lse)
+    torch.cuda.synchronize()
+    assert err.item() == 0
