@@ -98,7 +98,7 @@ def kernel_traffic(num_requests):
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one attention launch (ncu, 1 pass)
-MEASURED_TRAFFIC = {"kernel_sha": "98dd97f1addcb351", "requests": 4, "bytes": (1094.1 + 521.0) * 1e6}
+MEASURED_TRAFFIC = {"kernel_sha": "4c0ed08bd4d4db4a", "requests": 4, "bytes": (1094.3 + 520.9) * 1e6}
 
 
 def peaks():
@@ -287,27 +287,77 @@ def run_gpu(args, rank, world, local_rank):
 
 
 def run_e2e(args, step, flops, barrier, stream, world, dev):
-    host = {"q": step.q.cpu().pin_memory(), "k": step.k.cpu().pin_memory(), "v": step.v.cpu().pin_memory()}
-    for key, t in step.d.items():
-        if t is not None:
-            host[key] = t.cpu().pin_memory()
+    """The step end to end through the public API, as a prefill engine runs it:
+    every step copies the new tokens' q, k and v rows and the batch metadata
+    from pinned host memory, maps the tokens to cache slots, writes the new K/V
+    rows into the paged cache by slot (swa_kv_cache_write), computes the tile
+    bounds and the attention, and copies out and lse back to the host.  The
+    work is cut per request on three streams (host->device, compute,
+    device->host) so request r's copies overlap request r-1's kernels.  The
+    last step's host output is compared with the device-resident step's."""
+    swa, lay, d = step.swa, step.lay, step.d
+    qsl = [int(x) for x in lay.query_start_loc]
+    R = lay.num_seqs
+    slots = step.slots[:lay.num_tokens].long()
+    k_flat = step.k.view(-1, lay.num_heads_kv, lay.head_dim)
+    v_flat = step.v.view(-1, lay.num_heads_kv, lay.head_dim)
+    host = {"q": step.q.cpu().pin_memory(), "k_new": k_flat[slots].cpu().pin_memory(),
+            "v_new": v_flat[slots].cpu().pin_memory()}
+    meta = {key: t.cpu().pin_memory() for key, t in d.items() if t is not None}
+    dev_new = {"k_new": torch.empty_like(host["k_new"], device=dev), "v_new": torch.empty_like(host["v_new"], device=dev)}
     out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     lse_h = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + list(meta.values()))
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    # per-request views of the batch (request r alone, its query rows start at 0)
+    sub_qsl = [torch.tensor([0, qsl[r + 1] - qsl[r]], dtype=torch.int32, device=dev) for r in range(R)]
+    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
     def e2e_step():
-        step.q.copy_(host["q"], non_blocking=True)
-        step.k.copy_(host["k"], non_blocking=True)
-        step.v.copy_(host["v"], non_blocking=True)
-        for key, t in step.d.items():
-            if t is not None:
-                t.copy_(host[key], non_blocking=True)
-        step.feeders()
-        step.attention()
-        out_h.copy_(step.out, non_blocking=True)
-        lse_h.copy_(step.lse, non_blocking=True)
+        start = torch.cuda.Event()
+        start.record(stream)
+        s_h2d.wait_event(start)
+        got_meta, got = torch.cuda.Event(), []
+        with torch.cuda.stream(s_h2d):
+            for key, t in meta.items():
+                d[key].copy_(t, non_blocking=True)
+            got_meta.record(s_h2d)
+            for r in range(R):
+                a, b = qsl[r], qsl[r + 1]
+                step.q[a:b].copy_(host["q"][a:b], non_blocking=True)
+                dev_new["k_new"][a:b].copy_(host["k_new"][a:b], non_blocking=True)
+                dev_new["v_new"][a:b].copy_(host["v_new"][a:b], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(s_h2d)
+                got.append(e)
+        stream.wait_event(got_meta)
+        step.feeders()                                   # slot mapping + tile bounds, all requests
+        done = []
+        for r in range(R):
+            a, b = qsl[r], qsl[r + 1]
+            stream.wait_event(got[r])
+            swa.swa_kv_cache_write(dev_new["k_new"][a:b], dev_new["v_new"][a:b], step.slots[a:b], step.k, step.v,
+                                   err=step.err, stream=stream)
+            mm = d["mm_ranges"]
+            swa.swa_mm_paged_attention(
+                step.q[a:b], step.k, step.v, d["block_table"][r:r + 1], sub_qsl[r], d["seq_lens"][r:r + 1],
+                context_lens=d["context_lens"][r:r + 1], mm_ranges=None if mm is None else mm[r:r + 1],
+                max_query_len=b - a, window=lay.window, causal=lay.causal, scale=lay.scale,
+                out=step.out[a:b], lse=step.lse[a:b], err=step.err, stream=stream)
+            e = torch.cuda.Event()
+            e.record(stream)
+            done.append(e)
+        with torch.cuda.stream(s_d2h):
+            for r in range(R):
+                a, b = qsl[r], qsl[r + 1]
+                s_d2h.wait_event(done[r])
+                out_h[a:b].copy_(step.out[a:b], non_blocking=True)
+                lse_h[a:b].copy_(step.lse[a:b], non_blocking=True)
+        back = torch.cuda.Event()
+        back.record(s_d2h)
+        stream.wait_event(back)
 
+    ref_out = step.out.clone()
     e2e_step()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -319,8 +369,12 @@ def run_e2e(args, step, flops, barrier, stream, world, dev):
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    same = bool(torch.equal(out_h, ref_out.cpu()))
     return {"value": round(job_rate(flops, world, e2e_ms) / 1e12, 3), "unit": UNIT,
-            "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "step": "per request on three streams: H2D of q/k_new/v_new, swa_kv_cache_write + "
+                    "swa_mm_paged_attention, D2H of out/lse; slot mapping and tile bounds once per step",
+            "matches_device_step": same}
 
 
 def report_line(args, lay, step, flops, pairs, ms_per_step, attn_ms, feed_ms, clk, e2e, err, world):

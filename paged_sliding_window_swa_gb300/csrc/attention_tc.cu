@@ -859,7 +859,7 @@ cudaError_t run(const AttnArgs &a, cudaStream_t st) {
 }
 
 using Cfg256 = Cfg<256, 3, 2, 2, 3, 2, 2>;    // 64 KB Q + 3 K + 2 V units of 32 KB; 2 softmax WGs, 2 S
-using Cfg128 = Cfg<128, 6, 6, 1, 1, 2, 2>;    // 32 KB Q + 6 K + 6 V units of 16 KB; 2 softmax WGs, 2 S
+using Cfg128 = Cfg<128, 6, 6, 1, 3, 2, 2>;    // 32 KB Q + 6 K + 6 V units of 16 KB; 3 V producer warps; 2 softmax WGs, 2 S
 
 }  // namespace
 
