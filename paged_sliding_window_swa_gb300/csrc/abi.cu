@@ -145,6 +145,7 @@ int swa_mm_paged_attention(const void *q, const void *k_cache, const void *v_cac
   a.out = out; a.lse = lse; a.partial_out = partial_out; a.partial_lse = partial_lse; a.err = err;
 
   cudaStream_t st = as_stream(stream);
+  if (swa::tc_pair_supported(a)) return finish(swa::launch_attention_tc_pair(a, st));
   if (swa::tc_supported(a)) return finish(swa::launch_attention_tc(a, st));
   if (swa::decode_supported(a)) return finish(swa::launch_attention_decode(a, st));
   return finish(swa::launch_attention_simt(a, st));

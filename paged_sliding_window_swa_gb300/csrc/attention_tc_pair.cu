@@ -1,0 +1,605 @@
+// Tensor-core prefill attention for head_dim 128 with two query tiles per
+// work item (same mask and pruning as attention_tc.cu: vLLM PR #53147
+// summary, implementation items 1-2 and the compute_tile_loop_bounds excerpt).
+//
+// At head_dim 128 the tensor memory holds two O accumulators and two S
+// buffers (4 x 128 columns), so an item is a PAIR of consecutive 128-row query
+// tiles A and B of one sequence and kv head (2 x 128/G positions x G heads).
+// Every K/V tile is staged once for both, and each query tile has its own
+// softmax warpgroup that owns whole rows: no max exchange between warpgroups,
+// and while one warpgroup works on its tile's scores the tensor pipe runs the
+// other tile's MMAs.  The key loop covers the 128-key tiles of the union of
+// the pair's rows.
+//
+// Shared memory: Q_A and Q_B (32 KB each, TMA, 128-byte swizzle, K-major) and
+// two rings of 16 KB units: a K unit holds one 64-column half of head_dim for
+// the 128 keys of a tile, a V unit all 128 columns for one 64-key half.  TMEM
+// (512 columns): O_A [0,128), O_B [128,256), S_A [256,384), S_B [384,512); the
+// softmax writes P as bf16 pairs over the front of its S buffer.
+//
+// Sixteen warps; setmaxnreg moves registers from warps 0-7 (64 each) to the
+// softmax warpgroups (192 each):
+//   warp 0      K producer and Q loads; warps 4-6 V producers (a unit's page
+//               boxes are dealt over them, one TMA box per page and chunk)
+//   warp 1      QK issuer and TMEM owner: QK_A(t), QK_B(t) per key tile;
+//               QK_X(t) waits until PV_X(t-1) has been issued (it reads
+//               P_X(t-1) from S_X)
+//   warp 3      PV issuer: PV_A(t) once P_A(t) is published, then PV_B(t)
+//   warps 2, 7  no role
+//   warps 8-11  softmax of tile A, warps 12-15 softmax of tile B: thread i of
+//               a warpgroup owns row i (TMEM lane i) of its tile.
+// Every mbarrier wait is bounded in time; on expiry the CTA sets
+// SWA_ERR_TIMEOUT, drains its own TMA loads and MMAs, frees TMEM and exits.
+#include "attn_tc_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace swa {
+namespace {
+
+using namespace tc;
+
+struct PairCfg {
+  static constexpr int D = 128;
+  static constexpr int N = 128;                      // keys per tile
+  static constexpr int M = 128;                      // rows per query tile
+  static constexpr int CH = D / 64;                  // 128-byte column chunks per row
+  static constexpr int KSU = 5, VSU = 5;             // ring slots (16 KB units)
+  static constexpr int VW = 3;                       // V producer warps 4 .. 4 + VW - 1
+  static constexpr int THREADS = 512;
+  static constexpr int LAUNCH_REGS = 128;
+  static constexpr int LOW_REGS = 64;
+  static constexpr int HIGH_REGS = 192;
+  static constexpr int Q_CHUNK = M * 128;            // bytes of one 64-column chunk of a Q tile
+  static constexpr int Q_BYTES = M * D * 2;
+  static constexpr int UNIT = 16384;                 // bytes of a K or V unit
+  static constexpr int KU_CHUNK = N * 128;           // a K unit is one chunk of 128 keys
+  static constexpr int VU_KEYS = N / 2;              // keys per V unit
+  static constexpr int VU_CHUNK = VU_KEYS * 128;     // bytes per chunk of a V unit
+  static constexpr int OFF_Q = 0;                    // Q_A, then Q_B
+  static constexpr int OFF_K = 2 * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + KSU * UNIT;
+  static constexpr int OFF_CTRL = OFF_V + VSU * UNIT;
+  static constexpr int TM_O = 0;                     // O_X at X * D
+  static constexpr int TM_S = 2 * D;                 // S_X at TM_S + X * N
+  static constexpr uint32_t TM_COLS = 512;
+  static constexpr uint32_t IDESC_QK = idesc_bf16(128, N, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
+  static_assert(2 * D + 2 * N <= 512, "TMEM budget");
+  static_assert(LAUNCH_REGS * THREADS <= 65536 && (65536 / THREADS) >= LAUNCH_REGS, "launch registers");
+  static_assert(256 * LOW_REGS + 256 * HIGH_REGS <= LAUNCH_REGS * THREADS,
+                "the register split can only hand over what the launch allocated");
+  static_assert(KSU <= kMaxUnits && VSU <= kMaxUnits && KSU >= 2 && VSU >= 4, "ring sizes");
+};
+
+struct PairCtrl {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[kMaxUnits], k_empty[kMaxUnits], v_full[kMaxUnits], v_empty[kMaxUnits];
+  uint64_t s_full[2], p_full[2];         // per query tile X: S_X(t) complete, P_X(t) published
+  uint64_t pv_iss[2];                    // PV_X(t) issued: S_X may take QK_X(t+1)
+  uint64_t o_full[2], o_item[2];         // PV_X(t) complete; the item's last PV_X complete
+  uint64_t drain, drain2;
+  int32_t sched_n[4];                    // tile count of item ord at [ord & 3] (0: end of stream)
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr int pair_smem_bytes() { return PairCfg::OFF_CTRL + (int)sizeof(PairCtrl); }
+
+template <bool NEG>
+__global__ void __launch_bounds__(PairCfg::THREADS, 1)
+attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const int G, const int n_items) {
+  using C = PairCfg;
+  extern __shared__ __align__(1024) uint8_t dsm_ptr[];
+  const uint32_t dsm = smem_u32(dsm_ptr);
+  PairCtrl &ctl = *reinterpret_cast<PairCtrl *>(dsm_ptr + C::OFF_CTRL);
+  const uint32_t q_s = dsm + C::OFF_Q;
+  const uint32_t k_s = dsm + C::OFF_K;
+  const uint32_t v_s = dsm + C::OFF_V;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bq = C::M / G;                    // positions per query tile
+  const int bq2 = 2 * bq;                     // positions per item (the pair)
+  if ((dsm & 1023u) != 0) {
+    if (threadIdx.x == 0) report(a.err, SWA_ERR_INTERNAL);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    ctl.abort = 0;
+    mbar_init(smem_u32(&ctl.q_full), 1);
+    mbar_init(smem_u32(&ctl.q_empty), 1);
+    for (int i = 0; i < C::KSU; ++i) {
+      mbar_init(smem_u32(&ctl.k_full[i]), 1);
+      mbar_init(smem_u32(&ctl.k_empty[i]), 1);
+    }
+    for (int i = 0; i < C::VSU; ++i) {
+      mbar_init(smem_u32(&ctl.v_full[i]), 1);
+      mbar_init(smem_u32(&ctl.v_empty[i]), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(&ctl.s_full[x]), 1);
+      mbar_init(smem_u32(&ctl.p_full[x]), 128);
+      mbar_init(smem_u32(&ctl.pv_iss[x]), 1);
+      mbar_init(smem_u32(&ctl.o_full[x]), 1);
+      mbar_init(smem_u32(&ctl.o_item[x]), 1);
+    }
+    mbar_init(smem_u32(&ctl.drain), 1);
+    mbar_init(smem_u32(&ctl.drain2), 1);
+    mbar_fence_init();
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl.tmem_base), C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  volatile int *abort_flag = &ctl.abort;
+  const volatile int32_t *gerr = a.err;
+  const int stride = gridDim.x;
+
+  if (warp < 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::LOW_REGS));
+  const bool k_warp = warp == 0;
+  const bool v_warp = warp >= 4 && warp < 4 + C::VW;
+  if (k_warp || v_warp) {
+    // =============================== TMA producers ==============================
+    // As in attention_tc.cu: every producer warp of an operand walks all units,
+    // a unit's boxes are dealt round-robin over the warps, share 0 posts the
+    // expected bytes.
+    const bool is_v = v_warp;
+    const int nsh = is_v ? C::VW : 1;
+    const int share = is_v ? warp - 4 : 0;
+    const int SU = is_v ? C::VSU : C::KSU;
+    const CUtensorMap *map = is_v ? &tm_v : &tm_k;
+    const int unit_keys = is_v ? C::VU_KEYS : C::N;     // K units: 128 keys, V units: 64 keys
+    const int R = min(a.block_size, unit_keys);         // rows per box
+    const int boxes = unit_keys / R;                    // boxes per unit (per chunk)
+    const int uch = is_v ? C::CH : 1;                   // chunks per unit
+    const int oob = (int)(a.num_blocks * a.block_size);
+    int64_t u_base = 0;                                 // units issued by this warp before this item
+    int ord = 0;                                        // valid items so far
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += stride) {
+      Item it;
+      int32_t eb;
+      if (!decode_item(a, item, bq2, it, eb)) {
+        if (eb != 0 && warp == 0 && lane == 0) report(a.err, eb);
+        continue;
+      }
+      int kmin, kmax;
+      block_keys(a, it, lane, 32, true, kmin, kmax);
+      const int tile_lo = kmin / C::N;
+      const int n_tiles = kmax / C::N - tile_lo + 1;
+      if (warp == 0 && lane == 0) {
+        // Q_A and Q_B: the previous item's last QK_B has to be done with them
+        if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, gerr, kWaitLimitNs);
+        if (ok) {
+          ctl.sched_n[ord & 3] = n_tiles;
+          mbar_expect_tx(smem_u32(&ctl.q_full), 2 * C::Q_BYTES);
+          for (int x = 0; x < 2; ++x)
+            for (int c = 0; c < C::CH; ++c)
+              tma_load_3d(q_s + x * C::Q_BYTES + c * C::Q_CHUNK, &tm_q, c * 64, it.hk * G,
+                          it.qstart + it.qpos_lo + x * bq, smem_u32(&ctl.q_full));
+        }
+      }
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      ++ord;
+      const int total_boxes = (n_tiles * C::N) / R;
+      const int32_t *bt = a.block_table + (int64_t)it.s * a.bt_stride;
+      auto resolve = [&](int b) -> int {                // slot of the first key of box b
+        const int k = tile_lo * C::N + b * R;
+        int slot = oob;
+        if (b < total_boxes && k < it.seq_len) {
+          const int page = k / a.block_size;
+          const int32_t blk = page < a.bt_stride ? __ldg(bt + page) : -1;
+          if (blk >= 0 && blk < a.num_blocks) slot = blk * a.block_size + (k - page * a.block_size);
+          else if (warp == 0) report(a.err, SWA_ERR_BLOCK_ID);
+        }
+        return slot;
+      };
+      int batch = 0;
+      int prv = oob, cur = resolve(lane), nxt = resolve(32 + lane);
+      int ul = 0;
+      for (; ul < 2 * n_tiles; ++ul) {                 // unit ul of this item: tile ul/2, half ul%2
+        const int64_t u = u_base + ul;
+        const int slot_i = (int)(u % SU);
+        if (u >= SU) {
+          const uint32_t empty = smem_u32(is_v ? &ctl.v_empty[slot_i] : &ctl.k_empty[slot_i]);
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(empty, (uint32_t)(((u / SU) - 1) & 1), abort_flag, gerr, kWaitLimitNs));
+          if (!ok) break;
+        }
+        const int t = ul >> 1, half = ul & 1;
+        const uint32_t full = smem_u32(is_v ? &ctl.v_full[slot_i] : &ctl.k_full[slot_i]);
+        const uint32_t dst = (is_v ? v_s : k_s) + slot_i * C::UNIT;
+        if (share == 0 && lane == 0) mbar_expect_tx(full, C::UNIT);
+        __syncwarp();
+        // K: unit = 64-column half `half` of tile t's 128 keys; V: key half `half`
+        const int b0 = is_v ? (2 * t + half) * boxes : t * boxes;
+        while (b0 + boxes - 1 >= (batch + 1) * 32) {    // warp-uniform batch advance
+          prv = cur;
+          cur = nxt;
+          ++batch;
+          nxt = resolve((batch + 1) * 32 + lane);
+        }
+        const int i = min(lane / uch, boxes - 1), c = lane % uch;
+        const int b = b0 + i;
+        const int from_cur = __shfl_sync(0xffffffffu, cur, (b - batch * 32) & 31);
+        const int from_prv = __shfl_sync(0xffffffffu, prv, (b - (batch - 1) * 32) & 31);
+        const int slot = b >= batch * 32 ? from_cur : from_prv;
+        const int x = (is_v ? c : half) * 64;
+        const uint32_t d = dst + c * (is_v ? C::VU_CHUNK : C::KU_CHUNK) + i * R * 128;
+        if (lane < boxes * uch && lane % nsh == share) tma_load_3d(d, map, x, it.hk, slot, full);
+      }
+      u_base += ul;
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      report(a.err, SWA_ERR_TIMEOUT);
+    }
+    // drain: every load issued by this warp must have landed before the CTA exits
+    if (lane == 0) {
+      for (int64_t u = max((int64_t)0, u_base - SU); u < u_base; ++u)
+        mbar_wait(smem_u32(is_v ? &ctl.v_full[u % SU] : &ctl.k_full[u % SU]), (uint32_t)((u / SU) & 1), nullptr,
+                  nullptr, kWaitLimitNs);
+      if (warp == 0 && ord > 0) mbar_wait(smem_u32(&ctl.q_full), (ord - 1) & 1, nullptr, nullptr, kWaitLimitNs);
+      // end of stream for the QK issuer: one more q_full phase without data
+      if (warp == 0 && ok &&
+          (ord == 0 || mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, gerr, kWaitLimitNs))) {
+        ctl.sched_n[ord & 3] = 0;
+        mbar_arrive(smem_u32(&ctl.q_full));
+      }
+    }
+  } else if (warp == 1 || warp == 3) {
+    // =============================== MMA issuers ================================
+    // Warp 1 issues QK_A(t), QK_B(t); warp 3 issues PV_A(t), PV_B(t).  QK_X(t)
+    // overwrites S_X, which holds P_X(t-1) until PV_X(t-1) has read it: it is
+    // issued after warp 3 has issued PV_X(t-1), fenced and arrived on
+    // pv_iss[X] (tcgen05 work ordered through a fence pair runs in that order).
+    if (lane == 0 && warp == 1) {
+      bool ok = true;
+      int ord = 0;
+      int64_t t = 0;                                     // key tiles of this CTA's stream
+      while (ok) {
+        ok = mbar_wait(smem_u32(&ctl.q_full), (uint32_t)(ord & 1), abort_flag, gerr, kWaitLimitNs);
+        if (!ok) break;
+        const int n = ctl.sched_n[ord & 3];
+        if (n == 0) break;
+        tc_fence_after();
+        for (int j = 0; ok && j < n; ++j, ++t) {
+          for (int x = 0; ok && x < 2; ++x) {
+            if (t > 0) {
+              ok = mbar_wait(smem_u32(&ctl.pv_iss[x]), (uint32_t)((t - 1) & 1), abort_flag, gerr, kWaitLimitNs);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            const uint32_t d = tmem + C::TM_S + (uint32_t)x * C::N;
+            for (int half = 0; ok && half < 2; ++half) {    // K unit = 64-column half of head_dim
+              const int64_t u = 2 * t + half;
+              const int slot = (int)(u % C::KSU);
+              if (x == 0) {
+                ok = mbar_wait(smem_u32(&ctl.k_full[slot]), (uint32_t)((u / C::KSU) & 1), abort_flag, gerr,
+                               kWaitLimitNs);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              const uint32_t qa = q_s + x * C::Q_BYTES + half * C::Q_CHUNK;
+              const uint32_t kb = k_s + slot * C::UNIT;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)              // 16-column steps over the 64 columns
+                mma_ss(d, smem_desc_sw128(qa + kk * 32, 16, 1024), smem_desc_sw128(kb + kk * 32, 16, 1024),
+                       C::IDESC_QK, (half > 0 || kk > 0) ? 1u : 0u);
+              if (x == 1) mma_commit(smem_u32(&ctl.k_empty[slot]));
+            }
+            if (!ok) break;
+            mma_commit(smem_u32(&ctl.s_full[x]));
+          }
+          if (ok && j == n - 1) mma_commit(smem_u32(&ctl.q_empty));   // the item's Q is no longer read
+        }
+        ++ord;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        report(a.err, SWA_ERR_TIMEOUT);
+      }
+      // every MMA issued by this thread must finish before TMEM is released
+      mma_commit(smem_u32(&ctl.drain));
+      mbar_wait(smem_u32(&ctl.drain), 0, nullptr, nullptr, kWaitLimitNs);
+    } else if (lane == 0 && warp == 3) {
+      bool ok = true;
+      int64_t t = 0;
+      for (int item = blockIdx.x; ok && item < n_items; item += stride) {
+        Item it;
+        int32_t eb;
+        if (!decode_item(a, item, bq2, it, eb)) continue;
+        int kmin, kmax;
+        block_keys(a, it, 0, 1, false, kmin, kmax);
+        const int n_tiles = kmax / C::N - kmin / C::N + 1;
+        for (int j = 0; ok && j < n_tiles; ++j, ++t) {
+          for (int x = 0; ok && x < 2; ++x) {
+            ok = mbar_wait(smem_u32(&ctl.p_full[x]), (uint32_t)(t & 1), abort_flag, gerr, kWaitLimitNs);
+            if (!ok) break;
+            tc_fence_after();
+            for (int half = 0; ok && half < 2; ++half) {    // V unit = 64-key half of the tile
+              const int64_t u = 2 * t + half;
+              const int slot = (int)(u % C::VSU);
+              if (x == 0) {
+                ok = mbar_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1), abort_flag, gerr,
+                               kWaitLimitNs);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              const uint32_t p_t = tmem + C::TM_S + (uint32_t)x * C::N + half * (C::VU_KEYS / 16) * 8;
+              const uint32_t vb = v_s + slot * C::UNIT;
+#pragma unroll
+              for (int kk = 0; kk < C::VU_KEYS / 16; ++kk)
+                mma_ts(tmem + C::TM_O + (uint32_t)x * C::D, p_t + kk * 8,
+                       smem_desc_sw128(vb + kk * 16 * 128, C::VU_CHUNK, 1024), C::IDESC_PV,
+                       (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+              if (x == 1) mma_commit(smem_u32(&ctl.v_empty[slot]));
+            }
+            if (!ok) break;
+            mma_commit(smem_u32(&ctl.o_full[x]));
+            if (j == n_tiles - 1) mma_commit(smem_u32(&ctl.o_item[x]));   // the item's O_X is final
+            tc_fence_before();
+            mbar_arrive(smem_u32(&ctl.pv_iss[x]));
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        report(a.err, SWA_ERR_TIMEOUT);
+      }
+      mma_commit(smem_u32(&ctl.drain2));
+      mbar_wait(smem_u32(&ctl.drain2), 0, nullptr, nullptr, kWaitLimitNs);
+    }
+  }
+  // warps 2 and 7 have no role: they only give their registers to the softmax
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::HIGH_REGS));
+    // =============================== softmax ====================================
+    // Warpgroup x (0: tile A, 1: tile B); thread i owns row i of its tile: all
+    // N columns of S_x and all D columns of O_x.  The running max is kept in
+    // the log2 domain on raw scores (the scale is folded into the exponent's
+    // FFMA), O_x is rescaled in TMEM only when the max grows by more than 2^8.
+    constexpr int N = C::N;
+    const int x = (warp - 8) >> 2;
+    const int sid = threadIdx.x - 256 - 128 * x;         // 0 .. 127 within the warpgroup
+    const int row = 32 * (warp & 3) + lane;              // TMEM lane of this thread
+    const uint32_t lane_t = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t s_col = tmem + lane_t + C::TM_S + (uint32_t)x * N;
+    const uint32_t o_col = tmem + lane_t + C::TM_O + (uint32_t)x * C::D;
+    const float asl2 = fmaxf(fabsf(a.scale * kLog2e), 1.17549435e-38f);
+    int64_t t = 0;                                       // global tile index
+    int n_done = 0;                                      // items finished
+    bool ok = true;
+    int item = blockIdx.x - stride;
+    RowSetup cur;
+    bool have;
+    {
+      Item it;
+      have = next_item(a, item, stride, n_items, bq2, it);
+      if (have) {
+        it.qpos_lo += x * bq;                            // this warpgroup's tile of the pair
+        row_setup<N>(a, it, row, G, lane, cur);
+      }
+    }
+    while (ok && have) {
+      const Item &it = cur.it;
+      const int tile_lo = cur.tile_lo, n_tiles = cur.n_tiles;
+      const int klo = cur.klo, khi = cur.khi;
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < n_tiles; ++j, ++t) {
+        const int kt0 = (tile_lo + j) * N;
+        ok = mbar_wait(smem_u32(&ctl.s_full[x]), (uint32_t)(t & 1), abort_flag, gerr, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t raw[N];
+#pragma unroll
+        for (int c = 0; c < N / 32; ++c) tmem_ld32(s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
+        tmem_wait_ld();
+        float xv[N];
+        if (__all_sync(0xffffffffu, klo <= kt0 && khi >= kt0 + N - 1)) {
+#pragma unroll
+          for (int c = 0; c < N; ++c) xv[c] = NEG ? -__uint_as_float(raw[c]) : __uint_as_float(raw[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < N; ++c)
+            xv[c] = (kt0 + c >= klo && kt0 + c <= khi) ? (NEG ? -__uint_as_float(raw[c]) : __uint_as_float(raw[c]))
+                                                      : -INFINITY;
+        }
+        float m4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m4[i] = xv[i];
+#pragma unroll
+        for (int c = 4; c + 8 <= N; c += 8)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) m4[i] = fmax3(m4[i], xv[c + 2 * i], xv[c + 2 * i + 1]);
+#pragma unroll
+        for (int c = 4 + ((N - 4) / 8) * 8; c < N; ++c) m4[c & 3] = fmaxf(m4[c & 3], xv[c]);
+        float mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+        mx = mx == -INFINITY ? -INFINITY : mx * asl2;
+        const float m_new = fmaxf(m_used, mx);
+        const bool need = m_new > m_used + 8.f;           // also true on the first visible tile
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_next = need ? m_new : m_used;
+          const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_next);
+          if (j > 0) {
+            // PV_x(t-1) must be complete before O_x is rescaled (S_x(t), seen
+            // complete, was issued after it, so its o_full phase is the only
+            // one that can still be open)
+            ok = mbar_wait(smem_u32(&ctl.o_full[x]), (uint32_t)((t - 1) & 1), abort_flag, gerr, kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < C::D / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(o_col + 32 * c, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+              tmem_st32(o_col + 32 * c, r);
+            }
+            tmem_wait_st();
+          }
+          l *= alpha;
+          m_used = m_next;
+        }
+        const float ms = (m_used == -INFINITY) ? 0.f : m_used;
+        uint64_t sl2x2, nms;
+        asm volatile("mov.b64 %0, {%1, %1};" : "=l"(sl2x2) : "f"(asl2));
+        asm volatile("mov.b64 %0, {%1, %1};" : "=l"(nms) : "f"(-ms));
+        uint64_t s2[2] = {0, 0};                         // two paired partial sums (0.0f bits)
+        if (x == 0 && kt0 + N > it.seq_len) {
+          // keys past the sequence end: their V rows may hold anything; zero
+          // them before P_A(t) is published (PV_B(t) follows PV_A(t)).  The
+          // V units of tile t sit in other ring slots than tile t-1's, which
+          // PV_B(t-1) may still read, and their fill is the latest one of
+          // their slots, so the v_full parity is unambiguous.
+          for (int half = 0; half < 2 && ok; ++half) {
+            const int k0 = kt0 + half * C::VU_KEYS;
+            if (k0 + C::VU_KEYS <= it.seq_len) continue;
+            const int64_t u = 2 * t + half;
+            const int slot = (int)(u % C::VSU);
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1),
+                                                   abort_flag, gerr, kWaitLimitNs));
+            if (!ok) break;
+            const int r0 = max(0, it.seq_len - k0);
+            const int n16 = (C::VU_KEYS - r0) * 8 * C::CH;
+            for (int i = sid; i < n16; i += 128) {
+              const int c = i / ((C::VU_KEYS - r0) * 8), rem = i % ((C::VU_KEYS - r0) * 8);
+              uint4 *dst = reinterpret_cast<uint4 *>(dsm_ptr + C::OFF_V + slot * C::UNIT + c * C::VU_CHUNK +
+                                                     (r0 + rem / 8) * 128 + (rem % 8) * 16);
+              *dst = make_uint4(0, 0, 0, 0);
+            }
+          }
+          if (!ok) break;
+          fence_proxy_async_smem();
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {                 // P in two stores of 32 columns (64 keys each)
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            float e0, e1;
+            f2_unpack(f2_fma(f2_pack(xv[64 * hh + 2 * c], xv[64 * hh + 2 * c + 1]), sl2x2, nms), e0, e1);
+            const float p0 = ex2(e0), p1 = ex2(e1);
+            s2[c & 1] = f2_add(s2[c & 1], f2_pack(p0, p1));
+            pk[c] = pack_bf16(p0, p1);
+          }
+          tmem_st32(s_col + 32 * hh, pk);
+        }
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(s2[0], a0, a1);
+          f2_unpack(s2[1], b0, b1);
+          l += (a0 + a1) + (b0 + b1);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&ctl.p_full[x]));
+      }
+      if (!ok) break;
+      const bool row_valid = cur.row_valid;
+      const int64_t out_row = cur.out_row;
+      {
+        Item nit;
+        have = next_item(a, item, stride, n_items, bq2, nit);
+        if (have) {
+          nit.qpos_lo += x * bq;
+          row_setup<N>(a, nit, row, G, lane, cur);
+        }
+      }
+      // the item's last PV_x (one o_item phase per item)
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item[x]), (uint32_t)(n_done & 1), abort_flag, gerr,
+                                             kWaitLimitNs));
+      ++n_done;
+      if (!ok) break;
+      // epilogue: O / l -> bf16, 64 columns per pass, 32-byte stores.  The
+      // next item's first PV_x overwrites O_x only after this thread's P for
+      // it (published after these loads completed).
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + out_row * C::D;
+#pragma unroll 1
+      for (int c = 0; c < C::D / 64; ++c) {
+        uint32_t r[64];
+        tmem_ld32(o_col + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(r));
+        tmem_ld32(o_col + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+        tmem_wait_ld();
+        if (row_valid) {
+          uint32_t w[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) st_global_v8(o + 64 * c + 16 * e, w + 8 * e);
+        }
+      }
+      if (row_valid && a.lse != nullptr) a.lse[out_row] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      tc_fence_before();
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      report(a.err, SWA_ERR_TIMEOUT);
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+template <bool NEG>
+cudaError_t run_pair(const AttnArgs &a, cudaStream_t st) {
+  using C = PairCfg;
+  const int G = a.hq / a.hkv;
+  const int bq = C::M / G;
+  CUtensorMap mq, mk, mv;
+  const uint64_t esz = 2;
+  const uint64_t slots = (uint64_t)a.num_blocks * a.block_size;
+  if (!make_map(&mq, a.q, C::D, a.hq, a.num_tokens, C::D * esz, (uint64_t)a.hq * C::D * esz, 64, G, bq) ||
+      !make_map(&mk, a.k_cache, C::D, a.hkv, slots, C::D * esz, (uint64_t)a.hkv * C::D * esz, 64, 1,
+                (uint32_t)min(a.block_size, C::N)) ||
+      !make_map(&mv, a.v_cache, C::D, a.hkv, slots, C::D * esz, (uint64_t)a.hkv * C::D * esz, 64, 1,
+                (uint32_t)min(a.block_size, C::VU_KEYS)))
+    return cudaErrorInvalidValue;
+  constexpr int smem = pair_smem_bytes();
+  static_assert(smem <= 227 * 1024, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_pair_kernel<NEG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t items = (a.num_tokens / (2 * bq) + a.num_seqs) * (int64_t)a.hkv;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int grid = (int)(items < sms ? items : (int64_t)sms);
+  // The register split hands over exactly the launch allocation: a kernel built
+  // with another per-thread count would wait forever in setmaxnreg.inc.
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, attn_tc_pair_kernel<NEG>) != cudaSuccess || fa.numRegs != C::LAUNCH_REGS)
+    return cudaErrorInvalidConfiguration;
+  attn_tc_pair_kernel<NEG><<<grid, C::THREADS, smem, st>>>(mq, mk, mv, a, G, (int)items);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_pair_supported(const AttnArgs &a) {
+  const int G = a.hq / a.hkv;
+  return a.head_dim == 128 && tc_supported(a) && (G == 1 || G == 2 || G == 4 || G == 8 || G == 16);
+}
+
+cudaError_t launch_attention_tc_pair(const AttnArgs &a, cudaStream_t st) {
+  // the sign of the scale is a template argument, as in attention_tc.cu
+  return a.scale < 0.f ? run_pair<true>(a, st) : run_pair<false>(a, st);
+}
+
+}  // namespace swa

@@ -1,0 +1,210 @@
+// Pieces shared by the tensor-core attention kernels (attention_tc.cu and
+// attention_tc_pair.cu): the work items (a query block, or a pair of
+// consecutive query blocks, of one sequence and one kv head), the union of
+// their rows' visible intervals, the per-row interval a softmax thread needs,
+// and the host-side TMA descriptor helpers.
+#pragma once
+
+#include <climits>
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace swa {
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 200000000ull;    // 200 ms per wait: far above any real stall
+constexpr int kMaxUnits = 8;                       // ring slots per operand
+
+struct Item {
+  int s, hk, qstart, qlen, qpos_lo, seq_len, ctx;
+  int q_lo, q_hi;                        // absolute positions of the block's first and last rows
+  bool causal;                           // the sequence's flag, or the call's
+};
+
+// Item -> (query block, kv head).  False for blocks past their sequence's
+// query length (nothing to do) and for inconsistent metadata (err bits set).
+__device__ inline bool decode_item(const AttnArgs &a, int item, int bq, Item &it, int32_t &errbits) {
+  const int bx = item / a.hkv;
+  it.hk = item - bx * a.hkv;
+  it.s = find_seq(a.qsl, a.num_seqs, bx, bq);
+  const int64_t first = (int64_t)__ldg(a.qsl + it.s) / bq + it.s;
+  const int local = (int)(bx - first);
+  it.qstart = __ldg(a.qsl + it.s);
+  it.qlen = __ldg(a.qsl + it.s + 1) - it.qstart;
+  it.qpos_lo = local * bq;
+  errbits = 0;
+  if (local < 0 || it.qpos_lo >= it.qlen) return false;
+  if (it.qstart < 0 || (int64_t)it.qstart + it.qlen > a.num_tokens) {
+    errbits = SWA_ERR_QSL;
+    return false;
+  }
+  it.seq_len = __ldg(a.seq_lens + it.s);
+  it.ctx = it.seq_len - it.qlen;
+  if (it.ctx < 0 || (a.ctx_lens != nullptr && __ldg(a.ctx_lens + it.s) != it.ctx)) {
+    errbits = SWA_ERR_LENS;
+    return false;
+  }
+  it.q_lo = it.ctx + it.qpos_lo;
+  it.q_hi = it.ctx + min(it.qpos_lo + bq - 1, it.qlen - 1);
+  it.causal = a.seq_causal != nullptr ? __ldg(a.seq_causal + it.s) != 0 : a.causal != 0;
+  return true;
+}
+
+// The union of the block's rows' visible intervals.  Right edge: the larger of
+// the last row's base window and the end of every valid image range that meets
+// the block (largest such end: `emax`, -1 if none).  Left edge: the smaller of
+// the first row's base window (the base left edge never decreases with q) and
+// every such range's clamped start max(s, q_lo-W+1) (smallest: `smin`,
+// INT_MAX if none; a range meeting the block holds its row max(s, q_lo), whose
+// clamped start that is).  A range meets the block exactly when it holds one
+// of its rows, so this equals the union of the per-row intervals.
+__device__ inline void union_keys(const AttnArgs &a, const Item &it, int emax, int smin, int &kmin, int &kmax) {
+  kmin = max(0, min(base_lo(it.q_lo, a.window, a.chunk_size, a.chunk_lookback), smin));
+  kmax = min(max(base_hi(it.q_hi, a.window, it.causal, it.seq_len), emax), it.seq_len - 1);
+}
+
+// Ranges scanned by lanes `start`, `start + step`, ...; `warp_reduce`
+// combines the lanes.
+__device__ inline void block_keys(const AttnArgs &a, const Item &it, int start, int step, bool warp_reduce,
+                                  int &kmin, int &kmax) {
+  int emax = -1, smin = INT_MAX;
+  if (a.mm_ranges != nullptr) {
+    const int32_t *rg = a.mm_ranges + (int64_t)it.s * a.max_mm_ranges * 2;
+    const int clamp = a.window > 0 ? it.q_lo - a.window + 1 : INT_MIN;
+    for (int i = start; i < a.max_mm_ranges; i += step) {
+      const int s0 = __ldg(rg + 2 * i), e0 = __ldg(rg + 2 * i + 1);
+      if (s0 < e0 && s0 <= it.q_hi && e0 >= it.q_lo) {
+        emax = max(emax, e0);
+        smin = min(smin, max(s0, clamp));
+      }
+    }
+  }
+  if (warp_reduce) {
+    emax = __reduce_max_sync(0xffffffffu, emax);
+    smin = __reduce_min_sync(0xffffffffu, smin);
+  }
+  union_keys(a, it, emax, smin, kmin, kmax);
+}
+
+// Next valid item of this CTA's stream after `item` (false at the end).
+__device__ inline bool next_item(const AttnArgs &a, int &item, int stride, int n_items, int bq, Item &it) {
+  for (item += stride; item < n_items; item += stride) {
+    int32_t eb;
+    if (decode_item(a, item, bq, it, eb)) return true;
+  }
+  return false;
+}
+
+// What a softmax thread needs for one item: the item's tile range and its
+// row's visible interval [klo, khi] (empty for rows past the query length).
+struct RowSetup {
+  Item it;
+  int tile_lo, n_tiles;
+  int klo, khi;
+  int64_t out_row;
+  bool row_valid;
+};
+
+// One pass of the warp over the sequence's ranges yields both the block union
+// and every lane's own interval: a range is tested against the warp's 32 rows
+// only when it meets their span (ballot), which is rarely more than once.
+// Same rule as the visible interval of a single query: a valid range holding q
+// moves the right edge to its end and the left edge to its clamped start.
+template <int N>
+__device__ inline void row_setup(const AttnArgs &a, const Item &it, int row, int G, int lane, RowSetup &rs) {
+  rs.it = it;
+  const int wrow0 = row - lane;
+  const int wq_lo = it.ctx + it.qpos_lo + wrow0 / G;
+  const int wq_hi = it.ctx + it.qpos_lo + (wrow0 + 31) / G;
+  const int qpos = it.qpos_lo + row / G;
+  const int q = it.ctx + qpos;
+  int emax = -1, rhi = -1, smin = INT_MAX, rlo = INT_MAX;
+  if (a.mm_ranges != nullptr) {
+    const int32_t *rg = a.mm_ranges + (int64_t)it.s * a.max_mm_ranges * 2;
+    const int bclamp = a.window > 0 ? it.q_lo - a.window + 1 : INT_MIN;
+    const int rclamp = a.window > 0 ? q - a.window + 1 : INT_MIN;
+    for (int b = 0; b < a.max_mm_ranges; b += 32) {
+      int s0 = 0, e0 = -1;
+      if (b + lane < a.max_mm_ranges) {
+        s0 = __ldg(rg + 2 * (b + lane));
+        e0 = __ldg(rg + 2 * (b + lane) + 1);
+      }
+      const bool valid = s0 < e0;
+      if (valid && s0 <= it.q_hi && e0 >= it.q_lo) {
+        emax = max(emax, e0);
+        smin = min(smin, max(s0, bclamp));
+      }
+      uint32_t m = __ballot_sync(0xffffffffu, valid && s0 <= wq_hi && e0 >= wq_lo);
+      while (m != 0) {
+        const int src = __ffs(m) - 1;
+        m &= m - 1;
+        const int s1 = __shfl_sync(0xffffffffu, s0, src), e1 = __shfl_sync(0xffffffffu, e0, src);
+        if (s1 <= q && q <= e1) {
+          rhi = max(rhi, e1);
+          rlo = min(rlo, max(s1, rclamp));
+        }
+      }
+    }
+    emax = __reduce_max_sync(0xffffffffu, emax);
+    smin = __reduce_min_sync(0xffffffffu, smin);
+  }
+  int kmin, kmax;
+  union_keys(a, it, emax, smin, kmin, kmax);
+  rs.tile_lo = kmin / N;
+  rs.n_tiles = kmax / N - rs.tile_lo + 1;
+  rs.row_valid = qpos < it.qlen;
+  if (rs.row_valid) {
+    rs.klo = max(0, min(base_lo(q, a.window, a.chunk_size, a.chunk_lookback), rlo));
+    rs.khi = min(max(base_hi(q, a.window, it.causal, it.seq_len), rhi), it.seq_len - 1);
+    rs.out_row = (int64_t)(it.qstart + qpos) * a.hq + it.hk * G + row % G;
+  } else {
+    rs.klo = 1;
+    rs.khi = 0;
+    rs.out_row = 0;
+  }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+  static EncodeTiled fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiled>(nullptr);
+    return reinterpret_cast<EncodeTiled>(p);
+  }();
+  return fn;
+}
+
+bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+              uint32_t b0, uint32_t b1, uint32_t b2) {
+  EncodeTiled enc = encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess)
+    return 0;
+  return n;
+}
+
+}  // namespace
+}  // namespace swa

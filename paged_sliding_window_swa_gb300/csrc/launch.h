@@ -65,4 +65,8 @@ cudaError_t launch_attention_decode(const AttnArgs &a, cudaStream_t st);
 bool tc_supported(const AttnArgs &a);
 cudaError_t launch_attention_tc(const AttnArgs &a, cudaStream_t st);
 
+// The same for head_dim 128 with two query tiles per work item.
+bool tc_pair_supported(const AttnArgs &a);
+cudaError_t launch_attention_tc_pair(const AttnArgs &a, cudaStream_t st);
+
 }  // namespace swa
