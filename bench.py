@@ -14,6 +14,9 @@ bounded sample of the same workload instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 (N > 1: launched by torchrun, one independent replica per GPU.)
+``--workload chunked_prefill`` runs the causal chunked-prefill layout (head_dim
+128) as the step instead, for profiling that kernel; the default line is the
+Gemma-like one.
 """
 import os
 
@@ -228,7 +231,7 @@ def job_rate(units_per_rank, world, ms):
 def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    lay = W.gemma_like(num_requests=args.requests)
+    lay = W.gemma_like(num_requests=args.requests) if args.workload == "gemma_like" else W.chunked_prefill(True)
     step = PrefillStep(lay, dev)
     pairs = visible_pairs_per_head(lay)
     flops = 4.0 * lay.head_dim * lay.num_heads_q * pairs
@@ -377,6 +380,17 @@ def run_e2e(args, step, flops, barrier, stream, world, dev):
             "matches_device_step": same}
 
 
+def workload_text(lay):
+    if lay.name.startswith("gemma_like"):
+        return (f"{lay.name}: {lay.num_seqs} request(s) of {'/'.join(str(int(x)) for x in lay.seq_lens)} tokens, "
+                "60 images x 256 tokens each, causal SWA W=1024 with the window-clamped image mask, Hq=16, "
+                f"Hkv=8, D=256, bf16, paged KV block 16, slot mapping padded to {lay.max_num_tokens}")
+    return (f"{lay.name}: {lay.num_seqs} requests, cached context "
+            f"{'/'.join(str(int(x)) for x in lay.context_lens)} + 2048-token chunks, 0-40 images x 256 tokens, "
+            f"SWA W={lay.window} {'causal' if lay.causal else 'non-causal'}, Hq={lay.num_heads_q}, "
+            f"Hkv={lay.num_heads_kv}, D={lay.head_dim}, bf16, paged KV block {lay.block_size}")
+
+
 def l2_note(step):
     """How the timed region treats L2 (129 MB): the step's inputs are larger
     than it, so no flush is needed between steps."""
@@ -406,10 +420,7 @@ def report_line(args, lay, step, flops, pairs, ms_per_step, attn_ms, feed_ms, cl
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": f"{lay.name}: {lay.num_seqs} request(s) of "
-                        f"{'/'.join(str(int(x)) for x in lay.seq_lens)} tokens, 60 images x 256 "
-                        "tokens each, causal SWA W=1024 with the window-clamped image mask, Hq=16, "
-                        f"Hkv=8, D=256, bf16, paged KV block 16, slot mapping padded to {lay.max_num_tokens}",
+            "workload": workload_text(lay),
             "global_batch": lay.num_seqs * world,
             "seq_len": int(lay.seq_lens.mean()),
             "tokens_per_step": lay.num_tokens,
@@ -429,7 +440,7 @@ def report_line(args, lay, step, flops, pairs, ms_per_step, attn_ms, feed_ms, cl
             "peak": pk["bf16_tflops"],
             "unit": "TFLOP/s",
             "frac": round(achieved / pk["bf16_tflops"], 4),
-            "traffic": kernel_traffic(args.requests),
+            "traffic": kernel_traffic(args.requests) if args.workload == "gemma_like" else None,
             "peak_source": f"{pk['source']} bf16 dense (burst)",
             "avg_launch_ms": round(attn_avg, 4),
         },
@@ -655,6 +666,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads and bandwidth sweeps")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the step's kernels one by one instead of replaying CUDA graphs")
+    ap.add_argument("--workload", default="gemma_like", choices=["gemma_like", "chunked_prefill"],
+                    help="the step's layout (gemma_like = the benchmark; chunked_prefill = profiling case)")
     ap.add_argument("--requests", type=int, default=4, choices=[1, 2, 3, 4],
                     help="Gemma-like requests per step (4 = the benchmark; fewer = profiling case)")
     args = ap.parse_args()
