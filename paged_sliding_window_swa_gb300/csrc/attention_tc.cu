@@ -450,32 +450,38 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         uint32_t raw[NH];
+        float lred[NH / 32];                              // per 32 columns: max of S (min for NEG)
 #pragma unroll
         for (int c = 0; c < NH / 32; ++c)
-          tmem_ld32(tmem + lane_t + C::TM_S + (uint32_t)sb * C::N + h * NH + 32 * c,
-                    *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
+          tmem_ld32_red<NEG>(tmem + lane_t + C::TM_S + (uint32_t)sb * C::N + h * NH + 32 * c,
+                             *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c), lred[c]);
         tmem_wait_ld();
         float x[NH];
+        float mx;
         const bool full = klo <= kc0 && khi >= kc0 + NH - 1;
         if (__all_sync(0xffffffffu, full)) {
 #pragma unroll
           for (int c = 0; c < NH; ++c) x[c] = NEG ? -__uint_as_float(raw[c]) : __uint_as_float(raw[c]);
+          float r = lred[0];
+#pragma unroll
+          for (int c = 1; c < NH / 32; ++c) r = NEG ? fminf(r, lred[c]) : fmaxf(r, lred[c]);
+          mx = NEG ? -r : r;
         } else {
 #pragma unroll
           for (int c = 0; c < NH; ++c)
             x[c] = (kc0 + c >= klo && kc0 + c <= khi) ? (NEG ? -__uint_as_float(raw[c]) : __uint_as_float(raw[c]))
                                                       : -INFINITY;
+          float m4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) m4[i] = x[i];
+#pragma unroll
+          for (int c = 4; c + 8 <= NH; c += 8)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) m4[i] = fmax3(m4[i], x[c + 2 * i], x[c + 2 * i + 1]);
+#pragma unroll
+          for (int c = 4 + ((NH - 4) / 8) * 8; c < NH; ++c) m4[c & 3] = fmaxf(m4[c & 3], x[c]);
+          mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
         }
-        float m4[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) m4[i] = x[i];
-#pragma unroll
-        for (int c = 4; c + 8 <= NH; c += 8)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) m4[i] = fmax3(m4[i], x[c + 2 * i], x[c + 2 * i + 1]);
-#pragma unroll
-        for (int c = 4 + ((NH - 4) / 8) * 8; c < NH; ++c) m4[c & 3] = fmaxf(m4[c & 3], x[c]);
-        float mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
         mx = mx == -INFINITY ? -INFINITY : mx * asl2;
         ctl.red[xc & 1][h][row] = mx;
         mbar_arrive(smem_u32(&ctl.xch[xc & 1]));

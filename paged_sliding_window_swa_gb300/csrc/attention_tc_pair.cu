@@ -400,29 +400,36 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         uint32_t raw[N];
+        float lred[N / 32];                               // per 32 columns: max of S (min for NEG)
 #pragma unroll
-        for (int c = 0; c < N / 32; ++c) tmem_ld32(s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
+        for (int c = 0; c < N / 32; ++c)
+          tmem_ld32_red<NEG>(s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c), lred[c]);
         tmem_wait_ld();
         float xv[N];
+        float mx;
         if (__all_sync(0xffffffffu, klo <= kt0 && khi >= kt0 + N - 1)) {
 #pragma unroll
           for (int c = 0; c < N; ++c) xv[c] = NEG ? -__uint_as_float(raw[c]) : __uint_as_float(raw[c]);
+          float r = lred[0];
+#pragma unroll
+          for (int c = 1; c < N / 32; ++c) r = NEG ? fminf(r, lred[c]) : fmaxf(r, lred[c]);
+          mx = NEG ? -r : r;
         } else {
 #pragma unroll
           for (int c = 0; c < N; ++c)
             xv[c] = (kt0 + c >= klo && kt0 + c <= khi) ? (NEG ? -__uint_as_float(raw[c]) : __uint_as_float(raw[c]))
                                                       : -INFINITY;
+          float m4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) m4[i] = xv[i];
+#pragma unroll
+          for (int c = 4; c + 8 <= N; c += 8)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) m4[i] = fmax3(m4[i], xv[c + 2 * i], xv[c + 2 * i + 1]);
+#pragma unroll
+          for (int c = 4 + ((N - 4) / 8) * 8; c < N; ++c) m4[c & 3] = fmaxf(m4[c & 3], xv[c]);
+          mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
         }
-        float m4[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) m4[i] = xv[i];
-#pragma unroll
-        for (int c = 4; c + 8 <= N; c += 8)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) m4[i] = fmax3(m4[i], xv[c + 2 * i], xv[c + 2 * i + 1]);
-#pragma unroll
-        for (int c = 4 + ((N - 4) / 8) * 8; c < N; ++c) m4[c & 3] = fmaxf(m4[c & 3], xv[c]);
-        float mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
         mx = mx == -INFINITY ? -INFINITY : mx * asl2;
         const float m_new = fmaxf(m_used, mx);
         const bool need = m_new > m_used + 8.f;           // also true on the first visible tile
