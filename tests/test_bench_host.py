@@ -35,3 +35,17 @@ def test_visible_pair_count_with_chunks_and_flags_matches_oracle(seed):
                                seq_causal=lay.seq_causal, chunk_size=lay.chunk_size,
                                chunk_lookback=lay.chunk_lookback)
     assert bench.visible_pairs_per_head(lay) == ref
+
+
+def test_workload_text_names_each_layout():
+    g = bench.workload_text(W.gemma_like())
+    assert g.startswith("gemma_like") and "D=256" in g and "73728" in g
+    c = bench.workload_text(W.chunked_prefill(True))
+    assert c.startswith("chunked_prefill") and "D=128" in c and "causal" in c and "Hq=32" in c
+
+
+def test_traffic_is_reported_only_for_the_measured_workload():
+    # another request count than the one the counters were taken on: no traffic
+    assert bench.kernel_traffic(1) is None
+    t = bench.kernel_traffic(bench.MEASURED_TRAFFIC["requests"])
+    assert t is None or t == bench.MEASURED_TRAFFIC["bytes"]
