@@ -119,7 +119,12 @@ def peaks():
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples of the SM clock and the throttle reasons.  Only the
+    samples taken inside the timed region (host wall clock, a margin of one
+    interval) are kept; when the region is shorter than the interval, the
+    nearest samples stand in and `in_region` says so."""
+    INTERVAL_MS = 50
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -131,33 +136,46 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def stop(self, window=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        sm, smax, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 8:
-                continue
-            try:
-                sm.append(float(f[0]))
-                smax.append(float(f[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return summarise_clocks(out, window, self.INTERVAL_MS / 1e3)
+
+
+def summarise_clocks(out, window=None, margin_s=0.05):
+    """Median SM clock, maximum clock and throttle reasons from nvidia-smi CSV
+    lines (timestamp first); `window` = (t0, t1) host epoch seconds."""
+    import datetime
+    names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    rows = []
+    for line in out.strip().splitlines():
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            rows.append((ts, float(f[1]), float(f[2]), [n for n, v in zip(names, f[5:9]) if v.lower() == "active"]))
+        except ValueError:
+            continue
+    inside = rows
+    if window is not None and rows:
+        inside = [r for r in rows if window[0] - margin_s <= r[0] <= window[1] + margin_s]
+        if not inside:                      # region shorter than the interval: the nearest samples
+            mid = 0.5 * (window[0] + window[1])
+            inside = sorted(rows, key=lambda r: abs(r[0] - mid))[:2]
+    reasons = sorted({n for r in inside for n in r[3]})
+    return {"sm_mhz": statistics.median(r[1] for r in inside) if inside else None,
+            "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+            "reasons": reasons, "samples": len(inside),
+            "in_region": window is not None and bool(inside) and
+            all(window[0] - margin_s <= r[0] <= window[1] + margin_s for r in inside)}
 
 
 # ---------------------------------------------------------------------------
@@ -261,6 +279,7 @@ def run_gpu(args, rank, world, local_rank):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
+    wall0 = time.time()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -273,7 +292,7 @@ def run_gpu(args, rank, world, local_rank):
     t_end.record(stream)
     barrier()
     total_ms = t_start.elapsed_time(t_end)
-    clk = clocks.stop()
+    clk = clocks.stop(window=(wall0, time.time()))
     attn_ms = [a.elapsed_time(b) for _, a, b in ev]
     feed_ms = [a.elapsed_time(b) for a, b, _ in ev]
     total_ms = max_over_ranks(total_ms, world, dev)
@@ -657,7 +676,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

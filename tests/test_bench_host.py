@@ -49,3 +49,19 @@ def test_traffic_is_reported_only_for_the_measured_workload():
     assert bench.kernel_traffic(1) is None
     t = bench.kernel_traffic(bench.MEASURED_TRAFFIC["requests"])
     assert t is None or t == bench.MEASURED_TRAFFIC["bytes"]
+
+
+def test_clock_samples_are_taken_from_the_timed_region():
+    import datetime
+    base = datetime.datetime(2026, 1, 1, 12, 0, 0)
+    def line(ms, sm, sw_power="Not Active", hw="Not Active"):
+        ts = (base + datetime.timedelta(milliseconds=ms)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{ts}, {sm}, 2070, 900.00, 0x0, {hw}, Not Active, Not Active, {sw_power}"
+    out = "\n".join([line(0, 1200), line(50, 2070), line(100, 2070, sw_power="Active"), line(150, 2070),
+                     line(400, 990, hw="Active")])
+    t0 = base.timestamp()
+    c = bench.summarise_clocks(out, window=(t0 + 0.06, t0 + 0.14), margin_s=0.05)
+    assert c["samples"] == 3 and c["in_region"] and c["sm_mhz"] == 2070
+    assert c["reasons"] == ["sw_power_cap"]            # the idle and the late samples are left out
+    short = bench.summarise_clocks(out, window=(t0 + 0.3, t0 + 0.301), margin_s=0.01)
+    assert short["samples"] == 2 and not short["in_region"]
