@@ -27,8 +27,7 @@ Sources (page title, then the section):
   outputs merged with their LSE are equal to one softmax over the whole
   sequence.
 
-Readings where the pages are silent or ambiguous (each also listed in the
-design notes):
+Readings where the pages are silent or ambiguous:
 
 * softmax scale is an argument (default 1/sqrt(head_dim) in the workloads);
   LSE is in natural log;

@@ -179,6 +179,92 @@ def test_tile_bounds_padding_ranges_equal_no_ranges():
 
 
 # ---------------------------------------------------------------------------
+# tile bounds: the third field, max_seq_prefix_len
+# ---------------------------------------------------------------------------
+def _random_blocks(seed, with_ranges):
+    """Small random (sequence, query block) layouts with context and a ragged tail."""
+    rng = np.random.default_rng(900 + seed)
+    S = int(rng.integers(1, 4))
+    qlen = rng.integers(1, 70, size=S)
+    ctx = rng.integers(0, 70, size=S)
+    seq = ctx + qlen
+    mm = None
+    if with_ranges:
+        mm = np.zeros((S, 2, 2), dtype=np.int32)
+        for s in range(S):
+            a = int(rng.integers(0, seq[s]))
+            mm[s, 0] = (a, int(rng.integers(a, seq[s])))
+    qsl = np.concatenate([[0], np.cumsum(qlen)])
+    return rng, qsl, ctx, seq, mm
+
+
+def _max_visible_key_plus_one(ctx, seq_len, rows, window, causal, mm_row, **kw):
+    top = -1
+    for i in rows:
+        vis = np.nonzero(O.visible_keys(ctx + i, seq_len, window, causal, mm_row, **kw))[0]
+        if vis.size:
+            top = max(top, int(vis[-1]))
+    return top + 1
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_max_prefix_is_the_block_key_bound_when_causal_without_images(seed):
+    """Causal, no image ranges: the field is the exact bound on the keys the
+    block's rows can see, 1 + the largest visible key (brute force over the
+    per-pair rule), with and without chunked lookback, for every window."""
+    rng, qsl, ctx, seq, _ = _random_blocks(seed, with_ranges=False)
+    window = int(rng.choice([0, 1, 4, 9, 33, 500]))
+    bq = int(rng.choice([1, 3, 8, 16]))
+    tile = int(rng.choice([1, 4, 16]))
+    kw = {}
+    if window > 0 and rng.integers(0, 2):
+        kw = dict(chunk_size=int(rng.choice([4, 8, 32])), chunk_lookback=int(rng.integers(0, 3)))
+    maxb = int(-(-max(np.diff(qsl)) // bq))
+    tb = O.tile_bounds(qsl, seq, None, window, True, tile, bq, maxb, **kw)
+    for s in range(len(seq)):
+        for b in range(maxb):
+            rows = range(b * bq, min((b + 1) * bq, int(qsl[s + 1] - qsl[s])))
+            if not rows:
+                continue
+            bound = _max_visible_key_plus_one(int(ctx[s]), int(seq[s]), rows, window, True, None, **kw)
+            assert tb[s, b, 2] == bound, (s, b, tb[s, b].tolist(), bound)
+            # the tile range lies inside the prefix the field announces
+            assert tb[s, b, 1] <= -(-int(tb[s, b, 2]) // tile)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_max_prefix_is_the_sequence_length_with_images_or_noncausal(seed):
+    """With image ranges enabled, non-causal attention, or the per-sequence
+    causal mode, the field is seq_len: the printed [3, 72, 4096] case of the
+    PR #53147 geometry test generalised.  It still bounds every visible key."""
+    for with_ranges, causal, per_seq in ((True, True, False), (False, False, False),
+                                         (True, False, False), (False, True, True)):
+        rng, qsl, ctx, seq, mm = _random_blocks(seed, with_ranges)
+        window = int(rng.choice([0, 2, 9, 33]))
+        bq = int(rng.choice([1, 4, 8]))
+        maxb = int(-(-max(np.diff(qsl)) // bq))
+        tb = O.tile_bounds(qsl, seq, mm, window, causal, 4, bq, maxb, per_seq_causal=per_seq)
+        for s in range(len(seq)):
+            for b in range(maxb):
+                rows = range(b * bq, min((b + 1) * bq, int(qsl[s + 1] - qsl[s])))
+                if not rows:
+                    continue
+                assert tb[s, b, 2] == seq[s]
+                mm_row = None if mm is None else mm[s]
+                assert tb[s, b, 2] >= _max_visible_key_plus_one(int(ctx[s]), int(seq[s]), rows,
+                                                                window, causal, mm_row)
+
+
+def test_max_prefix_pages_geometry_without_images():
+    """The PR #53147 geometry (4096 tokens, W=1024, tile 32, block 8) without an
+    image: rows 1120..1127 see keys 97..1127, so the prefix is 1128 keys and the
+    tiles run [3, 36)."""
+    qsl, seq = np.array([0, 4096]), np.array([4096])
+    tb = O.tile_bounds(qsl, seq, None, 1024, True, 32, 8, 141)
+    assert tb[0, 140].tolist() == [3, 36, 1128]
+
+
+# ---------------------------------------------------------------------------
 # attention: reduction to torch's fp64 scaled-dot-product attention
 # ---------------------------------------------------------------------------
 def _dense(lay, q, k, v):
@@ -465,3 +551,16 @@ def test_planted_unclamped_image_mask_is_caught():
     right[lo:hi + 1] = True
     assert not np.array_equal(wrong, right)
     assert np.array_equal(O.visible_keys(q, seq_len, window, True, np.array(rngs)), right)
+
+
+def test_planted_max_prefix_seq_len_when_causal_is_caught():
+    """Reporting seq_len as the prefix of a causal block without images
+    overstates the keys the block can see; the brute-force pin catches it."""
+    qsl, seq = np.array([0, 40]), np.array([60])
+    tb = O.tile_bounds(qsl, seq, None, 8, True, 4, 8, 5)
+    wrong = tb.copy()
+    wrong[0, :, 2] = 60
+    rows = range(0, 8)
+    bound = _max_visible_key_plus_one(20, 60, rows, 8, True, None)
+    assert tb[0, 0, 2] == bound
+    assert wrong[0, 0, 2] != bound
