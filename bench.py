@@ -85,23 +85,41 @@ def visible_pairs_per_head(lay) -> int:
     return total
 
 
+# Every source the head_dim-256 attention kernel is compiled from: a change to
+# any of them makes the stored DRAM counters stale.
+TRAFFIC_SOURCES = ("paged_sliding_window_swa_gb300/csrc/attention_tc.cu",
+                   "paged_sliding_window_swa_gb300/csrc/attn_tc_common.cuh",
+                   "paged_sliding_window_swa_gb300/csrc/tc_ptx.cuh",
+                   "paged_sliding_window_swa_gb300/csrc/common.cuh",
+                   "paged_sliding_window_swa_gb300/csrc/launch.h",
+                   "include/swa.h")
+
+
+def kernel_source_sha():
+    """sha256 (16 hex digits) over the attention kernel's sources, in order."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def kernel_traffic(num_requests):
-    """DRAM bytes per attention launch on the 4-request workload from the committed ncu
-    launch list (profiles/attn_tc_gemma_like.md), or None for another workload or when
-    the kernel source has changed since those counters were taken."""
+    """DRAM bytes per attention launch on the 4-request workload, from the ncu
+    launch list taken of the kernel built from the sources whose hash is stored
+    with them; None for another workload or once any of those sources changed."""
     if num_requests != MEASURED_TRAFFIC["requests"]:
         return None
-    import hashlib
-    src = os.path.join(ROOT, "paged_sliding_window_swa_gb300", "csrc", "attention_tc.cu")
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        sha = kernel_source_sha()
     except OSError:
         return None
     return MEASURED_TRAFFIC["bytes"] if sha == MEASURED_TRAFFIC["kernel_sha"] else None
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one attention launch (ncu, 1 pass)
-MEASURED_TRAFFIC = {"kernel_sha": "69402b2a0724ae29", "requests": 4, "bytes": (1090.9 + 520.1) * 1e6}
+MEASURED_TRAFFIC = {"kernel_sha": "0000000000000000", "requests": 4, "bytes": (1090.9 + 520.1) * 1e6}
 
 
 def peaks():

@@ -11,7 +11,7 @@
  * Ownership.  Every array argument is a DEVICE pointer owned by the caller.
  *   The library allocates no memory and keeps no pointer after a call returns
  *   (swa_mm_paged_attention_split_static works in a fixed array of its own
- *   instead, allocated when the library is loaded; see there).
+ *   instead, placed on a device by the first call there; see there).
  * Streams.  `stream` is a cudaStream_t passed as void*; NULL means the legacy
  *   default stream.  Each call only enqueues work on `stream` and never
  *   synchronises the host.
@@ -317,15 +317,21 @@ int lse_combine(const void *partial_out, const float *partial_lse, int32_t num_s
  *   more than SWA_STATIC_SCRATCH_BYTES returns SWA_E_SCRATCH and launches
  *   nothing.
  * First call on a device: it looks up the array's device address with that
- *   device current and caches it; make that first call before any stream
- *   capture.  Later calls do no set-up.
+ *   device current and caches it.  CUDA loads device code lazily by default,
+ *   so that lookup is also when the array and this call's kernels are placed
+ *   on the device (with CUDA_MODULE_LOADING=EAGER: when the context is
+ *   created).  Make the first call on each device before reserving the rest
+ *   of its memory and before any stream capture.  Later calls do no set-up.
+ * Checks: every host-side check of swa_mm_paged_attention and lse_combine runs
+ *   before anything is launched or the array is touched.
  * Sharing: every call on a device uses the same array and leaves its contents
  *   behind.  Calls whose work overlaps on the GPU (two streams, or two host
  *   threads) race on it; serialise them.  The LSE part is reset to -inf at the
  *   start of each call.
  * Errors: those of swa_mm_paged_attention and lse_combine, plus
  *   SWA_E_SCRATCH; num_splits < 2 is SWA_E_SIZE.  Rows of a sequence rejected
- *   on the device come out as 0 with lse = -inf.
+ *   on the device, and tokens that no sequence covers, come out as 0 with
+ *   lse = -inf.
  */
 #define SWA_STATIC_SCRATCH_BYTES (16u << 20)
 int swa_mm_paged_attention_split_static(

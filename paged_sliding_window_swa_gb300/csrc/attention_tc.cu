@@ -13,8 +13,9 @@
 // every barrier phase simply continue from one item to the next: the next
 // item's Q copy and first two QK MMAs overlap the current item's tail.
 //
+// Built for head_dim 256 (head_dim 128 runs on attention_tc_pair.cu).
 // Shared memory: the Q tile (TMA, 128-byte swizzled, K-major) and two rings
-// of 32 KB units (for head_dim 256; 16 KB for 128): a K unit holds one half of
+// of 32 KB units: a K unit holds one half of
 // head_dim for all 128 keys of a tile, a V unit all of head_dim for one
 // 64-key half of a tile, so QK consumes two K units and PV two V units and
 // each is recycled as soon as its half of the MMA work is done.  TMEM (512
@@ -677,24 +678,15 @@ cudaError_t run(const AttnArgs &a, cudaStream_t st) {
 }
 
 using Cfg256 = Cfg<256, 3, 2, 2, 3, 2, 2>;    // 64 KB Q + 3 K + 2 V units of 32 KB; 2 softmax WGs, 2 S
-using Cfg128 = Cfg<128, 6, 6, 1, 3, 2, 2>;    // 32 KB Q + 6 K + 6 V units of 16 KB; 3 V producer warps; 2 softmax WGs, 2 S
 
 }  // namespace
 
-bool tc_supported(const AttnArgs &a) {
-  const int G = a.hq / a.hkv;
-  const int64_t items = (a.num_tokens / (128 / max(G, 1)) + a.num_seqs) * (int64_t)a.hkv;
-  return a.dtype == SWA_DTYPE_BF16 && (a.head_dim == 128 || a.head_dim == 256) && a.num_splits == 1 &&
-         (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) && a.max_query_len > 1 &&
-         a.num_blocks * a.block_size < (int64_t)INT32_MAX && a.num_tokens < (int64_t)INT32_MAX &&
-         items < (int64_t)INT32_MAX && encoder() != nullptr;
-}
+bool tc_supported(const AttnArgs &a) { return a.head_dim == 256 && tc_prefill_ok(a); }
 
 cudaError_t launch_attention_tc(const AttnArgs &a, cudaStream_t st) {
   // the sign of the scale is a template argument: a negative scale takes the
   // maximum of -S, without a per-score select
-  if (a.scale < 0.f) return a.head_dim == 256 ? run<Cfg256, true>(a, st) : run<Cfg128, true>(a, st);
-  return a.head_dim == 256 ? run<Cfg256, false>(a, st) : run<Cfg128, false>(a, st);
+  return a.scale < 0.f ? run<Cfg256, true>(a, st) : run<Cfg256, false>(a, st);
 }
 
 }  // namespace swa

@@ -599,10 +599,7 @@ cudaError_t run_pair(const AttnArgs &a, cudaStream_t st) {
 
 }  // namespace
 
-bool tc_pair_supported(const AttnArgs &a) {
-  const int G = a.hq / a.hkv;
-  return a.head_dim == 128 && tc_supported(a) && (G == 1 || G == 2 || G == 4 || G == 8 || G == 16);
-}
+bool tc_pair_supported(const AttnArgs &a) { return a.head_dim == 128 && tc_prefill_ok(a); }
 
 cudaError_t launch_attention_tc_pair(const AttnArgs &a, cudaStream_t st) {
   // the sign of the scale is a template argument, as in attention_tc.cu

@@ -198,6 +198,18 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// What both tensor-core prefill kernels need besides their head_dim: bf16, no
+// split, more than one query row per sequence somewhere, a GQA group that
+// divides the 128-row tile, 32-bit slot and token indices, and the TMA
+// descriptor encoder of the driver.
+inline bool tc_prefill_ok(const AttnArgs &a) {
+  const int G = a.hq / a.hkv;
+  const int64_t items = (a.num_tokens / (128 / max(G, 1)) + a.num_seqs) * (int64_t)a.hkv;
+  return a.dtype == SWA_DTYPE_BF16 && a.num_splits == 1 && (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) &&
+         a.max_query_len > 1 && a.num_blocks * a.block_size < (int64_t)INT32_MAX &&
+         a.num_tokens < (int64_t)INT32_MAX && items < (int64_t)INT32_MAX && encoder() != nullptr;
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=

@@ -28,6 +28,25 @@ struct AttnArgs {
   int32_t *err;
 };
 
+// Host-side checks of swa_mm_paged_attention.  Returns SWA_OK and fills `a`,
+// or a negative SWA_E_* code; an empty call (no tokens or no sequences) passes
+// with attention_is_empty(a).  Launches nothing.
+int prepare_attention(const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
+                      const int32_t *block_table, int64_t block_table_stride, const int32_t *query_start_loc,
+                      const int32_t *seq_lens, const int32_t *context_lens, const int32_t *mm_ranges,
+                      int32_t max_mm_ranges, int32_t num_seqs, int64_t num_tokens, int32_t max_query_len,
+                      int32_t num_heads_q, int32_t num_heads_kv, int32_t head_dim, int32_t block_size,
+                      int32_t window, int32_t causal, const int32_t *seq_causal, int32_t chunk_size,
+                      int32_t chunk_lookback, float scale, int32_t dtype, int32_t num_splits,
+                      const int32_t *splits_per_seq, void *out, float *lse, void *partial_out,
+                      float *partial_lse, int32_t *err, AttnArgs &a);
+bool attention_is_empty(const AttnArgs &a);
+// Picks the attention kernel for checked arguments and launches it.
+cudaError_t dispatch_attention(const AttnArgs &a, cudaStream_t st);
+// Host-side checks of lse_combine (SWA_OK or a negative code); launches nothing.
+int check_lse_combine(const void *partial_out, const float *partial_lse, int32_t num_splits,
+                      int64_t num_tokens, int32_t num_heads, int32_t head_dim, int32_t dtype, const void *out);
+
 // Context-parallel geometry of swa_slot_mapping_cp (validated by the caller).
 struct CpArgs {
   int32_t kv_cache_block_size, world, rank, interleave;
@@ -57,11 +76,11 @@ cudaError_t launch_lse_combine(const void *po, const float *pl, int32_t num_spli
 // General CUDA-core attention: any supported dtype / head_dim, split or not.
 cudaError_t launch_attention_simt(const AttnArgs &a, cudaStream_t st);
 
-// Split-KV decode: bf16, few query tokens per sequence, TMA-staged K/V.
+// Split-KV decode: bf16, few query tokens per sequence, K/V staged with cp.async.
 bool decode_supported(const AttnArgs &a);
 cudaError_t launch_attention_decode(const AttnArgs &a, cudaStream_t st);
 
-// tcgen05 / TMEM / TMA prefill: bf16, head_dim 128 or 256, no split.
+// tcgen05 / TMEM / TMA prefill: bf16, head_dim 256, no split.
 bool tc_supported(const AttnArgs &a);
 cudaError_t launch_attention_tc(const AttnArgs &a, cudaStream_t st);
 

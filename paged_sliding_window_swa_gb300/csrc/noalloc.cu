@@ -11,13 +11,21 @@
 // device-wide synchronisation cudaMalloc / cudaFree imply.  For them this entry
 // point keeps the partials in a file-scope __device__ array of
 // SWA_STATIC_SCRATCH_BYTES bytes.
+//
+// When the array is reserved: CUDA loads this library's device code lazily by
+// default, so the array (and this file's kernels) are placed on a device when
+// the first call on that device looks up the array's address.  That first
+// call must therefore come before the caller reserves the rest of the device,
+// and before any stream capture; with CUDA_MODULE_LOADING=EAGER the array is
+// placed when the CUDA context is created instead.
 #include <mutex>
 
 #include "common.cuh"
+#include "launch.h"
 
 namespace {
 
-// Every GPU that loads the library holds this array until the process exits.
+// Every GPU that loads this code holds the array until the process exits.
 static __device__ __align__(256) uint8_t g_split_scratch[SWA_STATIC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
@@ -46,6 +54,14 @@ __global__ void fill_neg_inf(float *x, int64_t n) {
 }
 
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess)
+    return 0;
+  return n;
+}
 
 }  // namespace
 
@@ -77,23 +93,31 @@ extern "C" int swa_mm_paged_attention_split_static(
   void *partial_out = base;
   float *partial_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(base) + po_bytes);
 
+  // Every host-side check of both steps runs before anything is launched.
+  swa::AttnArgs a;
+  rc = swa::prepare_attention(q, k_cache, v_cache, num_blocks, block_table, block_table_stride, query_start_loc,
+                              seq_lens, context_lens, mm_ranges, max_mm_ranges, num_seqs, num_tokens,
+                              max_query_len, num_heads_q, num_heads_kv, head_dim, block_size, window, causal,
+                              seq_causal, chunk_size, chunk_lookback, scale, dtype, num_splits, splits_per_seq,
+                              nullptr, nullptr, partial_out, partial_lse, err, a);
+  if (rc != SWA_OK) return rc;
+  rc = swa::check_lse_combine(partial_out, partial_lse, num_splits, num_tokens, num_heads_q, head_dim, dtype, out);
+  if (rc != SWA_OK) return rc;
+  const int sms = device_sm_count();
+  if (sms <= 0) return SWA_E_CUDA;
+
   // The array keeps the previous call's contents.  A partition row the
-  // attention kernel leaves unwritten (a sequence it rejects on the device)
-  // must read as "no keys" (-inf), so the LSE part is reset on every call;
-  // partial_out rows behind a -inf are never read.
+  // attention kernel leaves unwritten (a token no sequence covers, a sequence
+  // it rejects on the device) must read as "no keys" (-inf), so the LSE part
+  // is reset on every call; partial_out rows behind a -inf are never read.
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int64_t max_blocks = 152 * 8, want = swa::ceil_div(rows, 256);
+  const int64_t max_blocks = (int64_t)sms * 8, want = swa::ceil_div(rows, 256);
   const int64_t blocks = want < max_blocks ? want : max_blocks;
   fill_neg_inf<<<(unsigned)blocks, 256, 0, st>>>(partial_lse, rows);
   if (cudaGetLastError() != cudaSuccess) return SWA_E_CUDA;
-
-  rc = swa_mm_paged_attention(q, k_cache, v_cache, num_blocks, block_table, block_table_stride,
-                              query_start_loc, seq_lens, context_lens, mm_ranges, max_mm_ranges,
-                              num_seqs, num_tokens, max_query_len, num_heads_q, num_heads_kv, head_dim,
-                              block_size, window, causal, seq_causal, chunk_size, chunk_lookback, scale,
-                              dtype, num_splits, splits_per_seq, nullptr, nullptr, partial_out,
-                              partial_lse, err, stream);
-  if (rc != SWA_OK) return rc;
-  return lse_combine(partial_out, partial_lse, num_splits, num_tokens, num_heads_q, head_dim, dtype, out,
-                     lse, stream);
+  if (swa::dispatch_attention(a, st) != cudaSuccess) return SWA_E_CUDA;
+  if (swa::launch_lse_combine(partial_out, partial_lse, num_splits, num_tokens, num_heads_q, head_dim, dtype, out,
+                              lse, st) != cudaSuccess)
+    return SWA_E_CUDA;
+  return SWA_OK;
 }
