@@ -185,7 +185,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   volatile int *abort_flag = &ctl.abort;
-  const volatile int32_t *gerr = a.err;
   const int stride = gridDim.x;
 
   // Register split (warpgroup-wide, at the top of each side so every warp of a
@@ -211,6 +210,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int boxes = unit_keys / R;                    // boxes per unit (per chunk)
     const int uch = is_v ? C::CH : C::KU_CH;            // chunks per unit
     const int oob = (int)(a.num_blocks * a.block_size);
+    const int lg_bs = 31 - __clz(a.block_size);         // block sizes are powers of two
     int64_t u_base = 0;                                 // units issued by this warp before this item
     int ord = 0;                                        // valid items so far
     bool ok = true;
@@ -227,7 +227,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const int n_tiles = kmax / C::N - tile_lo + 1;
       if (warp == 0 && lane == 0) {
         // Q: the previous item's last QK has to be done with the buffer
-        if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, gerr, kWaitLimitNs);
+        if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, kWaitLimitNs);
         if (ok) {
           // the MMA warp learns the item's tile count from here once q_full completes
           ctl.sched_n[ord & 3] = n_tiles;
@@ -245,9 +245,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int k = tile_lo * C::N + b * R;
         int slot = oob;
         if (b < total_boxes && k < it.seq_len) {
-          const int page = k / a.block_size;
+          const int page = k >> lg_bs;
           const int32_t blk = page < a.bt_stride ? __ldg(bt + page) : -1;
-          if (blk >= 0 && blk < a.num_blocks) slot = blk * a.block_size + (k - page * a.block_size);
+          if (blk >= 0 && blk < a.num_blocks) slot = (blk << lg_bs) + (k & (a.block_size - 1));
           else if (warp == 0) report(a.err, SWA_ERR_BLOCK_ID);
         }
         return slot;
@@ -261,7 +261,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (u >= SU) {
           const uint32_t empty = smem_u32(is_v ? &ctl.v_empty[slot_i] : &ctl.k_empty[slot_i]);
           ok = __all_sync(0xffffffffu,
-                          mbar_wait(empty, (uint32_t)(((u / SU) - 1) & 1), abort_flag, gerr, kWaitLimitNs));
+                          mbar_wait(empty, (uint32_t)(((u / SU) - 1) & 1), abort_flag, kWaitLimitNs));
           if (!ok) break;
         }
         const int t = ul >> 1, half = ul & 1;
@@ -295,13 +295,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // drain: every load issued by this warp must have landed before the CTA exits
     if (lane == 0) {
       for (int64_t u = max((int64_t)0, u_base - SU); u < u_base; ++u)
-        mbar_wait(smem_u32(is_v ? &ctl.v_full[u % SU] : &ctl.k_full[u % SU]), (uint32_t)((u / SU) & 1), nullptr,
-                  nullptr, kWaitLimitNs);
-      if (warp == 0 && ord > 0) mbar_wait(smem_u32(&ctl.q_full), (ord - 1) & 1, nullptr, nullptr, kWaitLimitNs);
+        mbar_wait(smem_u32(is_v ? &ctl.v_full[u % SU] : &ctl.k_full[u % SU]), (uint32_t)((u / SU) & 1), nullptr, kWaitLimitNs);
+      if (warp == 0 && ord > 0) mbar_wait(smem_u32(&ctl.q_full), (ord - 1) & 1, nullptr, kWaitLimitNs);
       // end of stream for the MMA warp: one more q_full phase without data, once
       // the MMA warp is past the last real one (its last QK released q_empty)
       if (warp == 0 && ok &&
-          (ord == 0 || mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, gerr, kWaitLimitNs))) {
+          (ord == 0 || mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, kWaitLimitNs))) {
         ctl.sched_n[ord & 3] = 0;
         mbar_arrive(smem_u32(&ctl.q_full));
       }
@@ -316,10 +315,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (lane == 0 && warp == 1) {
       bool ok = true;
       int ord = 0;
-      int64_t t = 0;                                     // tiles of this CTA's stream
+      int t = 0;                                         // tiles of this CTA's stream
       while (ok) {
         // the next item's Q has landed (or the stream has ended: 0 tiles)
-        ok = mbar_wait(smem_u32(&ctl.q_full), (uint32_t)(ord & 1), abort_flag, gerr, kWaitLimitNs);
+        ok = mbar_wait(smem_u32(&ctl.q_full), (uint32_t)(ord & 1), abort_flag, kWaitLimitNs);
         if (!ok) break;
         const int n = ctl.sched_n[ord & 3];
         if (n == 0) break;
@@ -327,16 +326,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int j = 0; ok && j < n; ++j, ++t) {
           const int sb = (int)(t % C::NS);               // S buffer of tile t
           if (t >= C::NS) {
-            ok = mbar_wait(smem_u32(&ctl.pv_iss[sb]), (uint32_t)(((t / C::NS) - 1) & 1), abort_flag, gerr,
-                           kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.pv_iss[sb]), (uint32_t)(((t / C::NS) - 1) & 1), abort_flag, kWaitLimitNs);
             if (!ok) break;
             tc_fence_after();
           }
           const uint32_t d = tmem + C::TM_S + (uint32_t)sb * C::N;
           for (int half = 0; ok && half < 2; ++half) {
-            const int64_t u = 2 * t + half;
+            const uint32_t u = 2u * (uint32_t)t + half;
             const int slot = (int)(u % C::KSU);
-            ok = mbar_wait(smem_u32(&ctl.k_full[slot]), (uint32_t)((u / C::KSU) & 1), abort_flag, gerr, kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.k_full[slot]), (uint32_t)((u / C::KSU) & 1), abort_flag, kWaitLimitNs);
             if (!ok) break;
             tc_fence_after();
             const uint32_t qa = q_s + half * C::KU_CH * C::Q_CHUNK;
@@ -362,10 +360,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       // every MMA issued by this thread must finish before TMEM is released
       mma_commit(smem_u32(&ctl.drain));
-      mbar_wait(smem_u32(&ctl.drain), 0, nullptr, nullptr, kWaitLimitNs);
+      mbar_wait(smem_u32(&ctl.drain), 0, nullptr, kWaitLimitNs);
     } else if (lane == 0 && warp == 3) {
       bool ok = true;
-      int64_t t = 0;
+      int t = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += stride) {
         Item it;
         int32_t eb;
@@ -375,11 +373,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int n_tiles = kmax / C::N - kmin / C::N + 1;
         for (int j = 0; ok && j < n_tiles; ++j, ++t) {
           const int sb = (int)(t % C::NS);
-          ok = mbar_wait(smem_u32(&ctl.p_full[sb]), (uint32_t)((t / C::NS) & 1), abort_flag, gerr, kWaitLimitNs);
+          ok = mbar_wait(smem_u32(&ctl.p_full[sb]), (uint32_t)((t / C::NS) & 1), abort_flag, kWaitLimitNs);
           for (int half = 0; ok && half < 2; ++half) {
-            const int64_t u = 2 * t + half;
+            const uint32_t u = 2u * (uint32_t)t + half;
             const int slot = (int)(u % C::VSU);
-            ok = mbar_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1), abort_flag, gerr, kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1), abort_flag, kWaitLimitNs);
             if (!ok) break;
             tc_fence_after();
             const uint32_t p_t = tmem + C::TM_S + (uint32_t)sb * C::N + half * (C::VU_KEYS / 16) * 8;
@@ -402,7 +400,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         report(a.err, SWA_ERR_TIMEOUT);
       }
       mma_commit(smem_u32(&ctl.drain2));
-      mbar_wait(smem_u32(&ctl.drain2), 0, nullptr, nullptr, kWaitLimitNs);
+      mbar_wait(smem_u32(&ctl.drain2), 0, nullptr, kWaitLimitNs);
     }
   }
   // warp 7 has no role: it only gives its registers to the softmax
@@ -424,7 +422,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // the scale is folded into the exponent's FFMA: maxima are taken on the raw
     // scores (of -S for a negative scale, NEG) and scaled once
     const float asl2 = fmaxf(fabsf(a.scale * kLog2e), 1.17549435e-38f);
-    int64_t t = 0;                                       // global tile index
+    int t = 0;                                           // this CTA's tiles so far
     int64_t xc = 0;                                      // exchanges so far (buffer xc & 1)
     int n_done = 0;                                      // items finished
     bool ok = true;
@@ -447,7 +445,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int kt0 = (tile_lo + j) * C::N;
         const int kc0 = kt0 + h * NH;                    // key of this warpgroup's first column
         const int sb = (int)(t % C::NS);                 // S buffer of tile t
-        ok = mbar_wait(smem_u32(&ctl.s_full[sb]), (uint32_t)((t / C::NS) & 1), abort_flag, gerr, kWaitLimitNs);
+        ok = mbar_wait(smem_u32(&ctl.s_full[sb]), (uint32_t)((t / C::NS) & 1), abort_flag, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         uint32_t raw[NH];
@@ -486,7 +484,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mx = mx == -INFINITY ? -INFINITY : mx * asl2;
         ctl.red[xc & 1][h][row] = mx;
         mbar_arrive(smem_u32(&ctl.xch[xc & 1]));
-        ok = mbar_wait_spin(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag, gerr, kWaitLimitNs);
+        ok = mbar_wait_spin(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
 #pragma unroll
         for (int g = 0; g < NSW; ++g)
@@ -504,8 +502,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           const float m_next = need ? m_new : m_used;
           const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_next);
           if (j > 0) {
-            ok = mbar_wait(smem_u32(&ctl.o_full[(t - 1) & 1]), (uint32_t)(((t - 1) >> 1) & 1), abort_flag, gerr,
-                           kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.o_full[(t - 1) & 1]), (uint32_t)(((t - 1) >> 1) & 1), abort_flag, kWaitLimitNs);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll 1
@@ -547,25 +544,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           // them.  Once PV_{t-1} is done every earlier unit of each V slot has
           // been consumed, so the v_full parity below is unambiguous.
           if (j > 0) {
-            ok = mbar_wait(smem_u32(&ctl.o_full[(t - 1) & 1]), (uint32_t)(((t - 1) >> 1) & 1), abort_flag, gerr,
-                           kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.o_full[(t - 1) & 1]), (uint32_t)(((t - 1) >> 1) & 1), abort_flag, kWaitLimitNs);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           }
           for (int half = 0; half < 2 && ok; ++half) {
             const int k0 = kt0 + half * C::VU_KEYS;
             if (k0 + C::VU_KEYS <= it.seq_len) continue;
-            const int64_t u = 2 * t + half;
+            const uint32_t u = 2u * (uint32_t)t + half;
             const int slot = (int)(u % C::VSU);
             ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1),
-                                                   abort_flag, gerr, kWaitLimitNs));
+                                                   abort_flag, kWaitLimitNs));
             if (!ok) break;
-            const int r0 = max(0, it.seq_len - k0);
-            const int n16 = (C::VU_KEYS - r0) * 8 * C::CH;
-            for (int i = sid; i < n16; i += 128 * NSW) {
-              const int c = i / ((C::VU_KEYS - r0) * 8), rem = i % ((C::VU_KEYS - r0) * 8);
-              uint4 *dst = reinterpret_cast<uint4 *>(dsm_ptr + C::OFF_V + slot * C::UNIT + c * C::VU_CHUNK +
-                                                     (r0 + rem / 8) * 128 + (rem % 8) * 16);
-              *dst = make_uint4(0, 0, 0, 0);
+            const int r0 = max(0, it.seq_len - k0);       // first row to clear
+            uint8_t *unit = dsm_ptr + C::OFF_V + slot * C::UNIT;
+#pragma unroll 1
+            for (int i = sid; i < C::CH * C::VU_KEYS * 8; i += 128 * NSW) {   // 16-byte pieces: chunk, row, piece
+              const int r = (i >> 3) & (C::VU_KEYS - 1);
+              if (r >= r0)
+                *reinterpret_cast<uint4 *>(unit + (i / (C::VU_KEYS * 8)) * C::VU_CHUNK + r * 128 + (i & 7) * 16) =
+                    make_uint4(0, 0, 0, 0);
             }
           }
           if (!ok) break;
@@ -592,14 +589,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (have) row_setup<C::N>(a, nit, row, G, lane, cur);
       }
       // the item's last PV (one o_item phase per item), then the full row sum
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item), (uint32_t)(n_done & 1), abort_flag, gerr,
-                                             kWaitLimitNs));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item), (uint32_t)(n_done & 1), abort_flag, kWaitLimitNs));
       ++n_done;
       if (!ok) break;
       ctl.red[xc & 1][h][row] = l;
       mbar_arrive(smem_u32(&ctl.xch[xc & 1]));
-      ok = __all_sync(0xffffffffu, mbar_wait_spin(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag,
-                                             gerr, kWaitLimitNs));
+      ok = __all_sync(0xffffffffu, mbar_wait_spin(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag, kWaitLimitNs));
       if (!ok) break;
 #pragma unroll
       for (int g = 0; g < NSW; ++g)

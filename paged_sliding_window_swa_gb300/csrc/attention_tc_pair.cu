@@ -2,34 +2,42 @@
 // work item (same mask and pruning as attention_tc.cu: vLLM PR #53147
 // summary, implementation items 1-2 and the compute_tile_loop_bounds excerpt).
 //
-// At head_dim 128 the tensor memory holds two O accumulators and two S
-// buffers (4 x 128 columns), so an item is a PAIR of consecutive 128-row query
-// tiles A and B of one sequence and kv head (2 x 128/G positions x G heads).
-// Every K/V tile is staged once for both, and each query tile has its own
-// softmax warpgroup that owns whole rows: no max exchange between warpgroups,
-// and while one warpgroup works on its tile's scores the tensor pipe runs the
-// other tile's MMAs.  The key loop covers the 128-key tiles of the union of
-// the pair's rows.
+// At head_dim 128 the tensor memory holds the two O accumulators, one S
+// buffer and the two tiles' P, so an item is a PAIR of consecutive 128-row
+// query tiles A and B of one sequence and kv head (2 x 128/G positions x G
+// heads).  Every K/V tile is staged once for both, and each query tile has
+// its own softmax warpgroup that owns whole rows: no max exchange between
+// warpgroups.  The key loop covers the 128-key tiles of the union of the
+// pair's rows.
+//
+// The S buffer is shared: QK_A(t) and QK_B(t) take turns in it, and each QK
+// waits only until the other tile's softmax has LOADED the previous scores
+// (s_free).  P goes to a region of its own, so a tile's next QK never waits
+// for its softmax to finish or for its PV: while one softmax warpgroup works
+// on its scores the tensor pipe runs the other tile's QK and the PVs.
 //
 // Shared memory: Q_A and Q_B (32 KB each, TMA, 128-byte swizzle, K-major) and
 // two rings of 16 KB units: a K unit holds one 64-column half of head_dim for
 // the 128 keys of a tile, a V unit all 128 columns for one 64-key half.  TMEM
-// (512 columns): O_A [0,128), O_B [128,256), S_A [256,384), S_B [384,512); the
-// softmax writes P as bf16 pairs over the front of its S buffer.
+// (512 columns): O_A [0,128), O_B [128,256), S [256,384), P_A [384,448),
+// P_B [448,512) (P as bf16 pairs).
 //
 // Sixteen warps; setmaxnreg moves registers from warps 0-7 (64 each) to the
 // softmax warpgroups (192 each):
 //   warp 0      K producer and Q loads; warps 4-6 V producers (a unit's page
 //               boxes are dealt over them, one TMA box per page and chunk)
-//   warp 1      QK issuer and TMEM owner: QK_A(t), QK_B(t) per key tile;
-//               QK_X(t) waits until PV_X(t-1) has been issued (it reads
-//               P_X(t-1) from S_X)
+//   warp 1      QK issuer and TMEM owner: QK_A(t), QK_B(t) per key tile, each
+//               after the previous scores were loaded from S
 //   warp 3      PV issuer: PV_A(t) once P_A(t) is published, then PV_B(t)
 //   warps 2, 7  no role
 //   warps 8-11  softmax of tile A, warps 12-15 softmax of tile B: thread i of
 //               a warpgroup owns row i (TMEM lane i) of its tile.
-// Every mbarrier wait is bounded in time; on expiry the CTA sets
-// SWA_ERR_TIMEOUT, drains its own TMA loads and MMAs, frees TMEM and exits.
+// The code is kept small on purpose (32-bit counters, shifts for the
+// power-of-two page size, no runtime division in the loops): at this size the
+// SM's instruction cache decides how fast the rarely taken paths (item
+// boundaries, masked tiles) run.  Every mbarrier wait is bounded in time; on
+// expiry the CTA sets SWA_ERR_TIMEOUT, drains its own TMA loads and MMAs,
+// frees TMEM and exits.
 #include "attn_tc_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -60,22 +68,24 @@ struct PairCfg {
   static constexpr int OFF_V = OFF_K + KSU * UNIT;
   static constexpr int OFF_CTRL = OFF_V + VSU * UNIT;
   static constexpr int TM_O = 0;                     // O_X at X * D
-  static constexpr int TM_S = 2 * D;                 // S_X at TM_S + X * N
+  static constexpr int TM_S = 2 * D;                 // the shared S buffer
+  static constexpr int TM_P = 2 * D + N;             // P_X at TM_P + X * N / 2
   static constexpr uint32_t TM_COLS = 512;
   static constexpr uint32_t IDESC_QK = idesc_bf16(128, N, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
-  static_assert(2 * D + 2 * N <= 512, "TMEM budget");
+  static_assert(2 * D + N + 2 * (N / 2) <= 512, "TMEM budget");
   static_assert(LAUNCH_REGS * THREADS <= 65536 && (65536 / THREADS) >= LAUNCH_REGS, "launch registers");
   static_assert(256 * LOW_REGS + 256 * HIGH_REGS <= LAUNCH_REGS * THREADS,
                 "the register split can only hand over what the launch allocated");
   static_assert(KSU <= kMaxUnits && VSU <= kMaxUnits && KSU >= 2 && VSU >= 4, "ring sizes");
+  static_assert(KSU == VSU, "the producers share one ring walk");
 };
 
 struct PairCtrl {
   uint64_t q_full, q_empty;
   uint64_t k_full[kMaxUnits], k_empty[kMaxUnits], v_full[kMaxUnits], v_empty[kMaxUnits];
-  uint64_t s_full[2], p_full[2];         // per query tile X: S_X(t) complete, P_X(t) published
-  uint64_t pv_iss[2];                    // PV_X(t) issued: S_X may take QK_X(t+1)
+  uint64_t s_full[2], p_full[2];         // per query tile X: S holds QK_X(t), P_X(t) published
+  uint64_t s_free;                       // the last QK's scores were loaded: S may be overwritten
   uint64_t o_full[2], o_item[2];         // PV_X(t) complete; the item's last PV_X complete
   uint64_t drain, drain2;
   int32_t sched_n[4];                    // tile count of item ord at [ord & 3] (0: end of stream)
@@ -84,6 +94,18 @@ struct PairCtrl {
 };
 
 constexpr int pair_smem_bytes() { return PairCfg::OFF_CTRL + (int)sizeof(PairCtrl); }
+
+// A ring position: slot and the parity of its current fill.
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ void next(int size) {
+    if (++slot == size) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
 
 template <bool NEG>
 __global__ void __launch_bounds__(PairCfg::THREADS, 1)
@@ -119,10 +141,10 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&ctl.s_full[x]), 1);
       mbar_init(smem_u32(&ctl.p_full[x]), 128);
-      mbar_init(smem_u32(&ctl.pv_iss[x]), 1);
       mbar_init(smem_u32(&ctl.o_full[x]), 1);
       mbar_init(smem_u32(&ctl.o_item[x]), 1);
     }
+    mbar_init(smem_u32(&ctl.s_free), 128);
     mbar_init(smem_u32(&ctl.drain), 1);
     mbar_init(smem_u32(&ctl.drain2), 1);
     mbar_fence_init();
@@ -139,7 +161,6 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   volatile int *abort_flag = &ctl.abort;
-  const volatile int32_t *gerr = a.err;
   const int stride = gridDim.x;
 
   if (warp < 8) {
@@ -161,7 +182,8 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int boxes = unit_keys / R;                    // boxes per unit (per chunk)
     const int uch = is_v ? C::CH : 1;                   // chunks per unit
     const int oob = (int)(a.num_blocks * a.block_size);
-    int64_t u_base = 0;                                 // units issued by this warp before this item
+    const int lg_bs = 31 - __clz(a.block_size);
+    int u_base = 0;                                     // units issued by this warp before this item
     int ord = 0;                                        // valid items so far
     bool ok = true;
     for (int item = blockIdx.x; ok && item < n_items; item += stride) {
@@ -177,7 +199,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const int n_tiles = kmax / C::N - tile_lo + 1;
       if (warp == 0 && lane == 0) {
         // Q_A and Q_B: the previous item's last QK_B has to be done with them
-        if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, gerr, kWaitLimitNs);
+        if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, kWaitLimitNs);
         if (ok) {
           ctl.sched_n[ord & 3] = n_tiles;
           mbar_expect_tx(smem_u32(&ctl.q_full), 2 * C::Q_BYTES);
@@ -195,9 +217,9 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int k = tile_lo * C::N + b * R;
         int slot = oob;
         if (b < total_boxes && k < it.seq_len) {
-          const int page = k / a.block_size;
+          const int page = k >> lg_bs;
           const int32_t blk = page < a.bt_stride ? __ldg(bt + page) : -1;
-          if (blk >= 0 && blk < a.num_blocks) slot = blk * a.block_size + (k - page * a.block_size);
+          if (blk >= 0 && blk < a.num_blocks) slot = (blk << lg_bs) + (k & (a.block_size - 1));
           else if (warp == 0) report(a.err, SWA_ERR_BLOCK_ID);
         }
         return slot;
@@ -206,12 +228,12 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       int prv = oob, cur = resolve(lane), nxt = resolve(32 + lane);
       int ul = 0;
       for (; ul < 2 * n_tiles; ++ul) {                 // unit ul of this item: tile ul/2, half ul%2
-        const int64_t u = u_base + ul;
+        const int u = u_base + ul;
         const int slot_i = (int)(u % SU);
         if (u >= SU) {
           const uint32_t empty = smem_u32(is_v ? &ctl.v_empty[slot_i] : &ctl.k_empty[slot_i]);
           ok = __all_sync(0xffffffffu,
-                          mbar_wait(empty, (uint32_t)(((u / SU) - 1) & 1), abort_flag, gerr, kWaitLimitNs));
+                          mbar_wait(empty, (uint32_t)(((u / SU) - 1) & 1), abort_flag, kWaitLimitNs));
           if (!ok) break;
         }
         const int t = ul >> 1, half = ul & 1;
@@ -244,61 +266,63 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
     // drain: every load issued by this warp must have landed before the CTA exits
     if (lane == 0) {
-      for (int64_t u = max((int64_t)0, u_base - SU); u < u_base; ++u)
-        mbar_wait(smem_u32(is_v ? &ctl.v_full[u % SU] : &ctl.k_full[u % SU]), (uint32_t)((u / SU) & 1), nullptr,
-                  nullptr, kWaitLimitNs);
-      if (warp == 0 && ord > 0) mbar_wait(smem_u32(&ctl.q_full), (ord - 1) & 1, nullptr, nullptr, kWaitLimitNs);
+      for (int u = max(0, u_base - SU); u < u_base; ++u)
+        mbar_wait(smem_u32(is_v ? &ctl.v_full[u % SU] : &ctl.k_full[u % SU]), (uint32_t)((u / SU) & 1), nullptr, kWaitLimitNs);
+      if (warp == 0 && ord > 0) mbar_wait(smem_u32(&ctl.q_full), (ord - 1) & 1, nullptr, kWaitLimitNs);
       // end of stream for the QK issuer: one more q_full phase without data
       if (warp == 0 && ok &&
-          (ord == 0 || mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, gerr, kWaitLimitNs))) {
+          (ord == 0 || mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, kWaitLimitNs))) {
         ctl.sched_n[ord & 3] = 0;
         mbar_arrive(smem_u32(&ctl.q_full));
       }
     }
   } else if (warp == 1 || warp == 3) {
     // =============================== MMA issuers ================================
-    // Warp 1 issues QK_A(t), QK_B(t); warp 3 issues PV_A(t), PV_B(t).  QK_X(t)
-    // overwrites S_X, which holds P_X(t-1) until PV_X(t-1) has read it: it is
-    // issued after warp 3 has issued PV_X(t-1), fenced and arrived on
-    // pv_iss[X] (tcgen05 work ordered through a fence pair runs in that order).
+    // Warp 1 issues QK_A(t), QK_B(t) into the shared S buffer, each once the
+    // previous QK's scores have been loaded by their softmax (s_free); warp 3
+    // issues PV_A(t), PV_B(t) from P_A, P_B.
     if (lane == 0 && warp == 1) {
       bool ok = true;
       int ord = 0;
-      int64_t t = 0;                                     // key tiles of this CTA's stream
+      int n_qk = 0;                                     // QKs issued (both tiles)
+      RingPos kp;
       while (ok) {
-        ok = mbar_wait(smem_u32(&ctl.q_full), (uint32_t)(ord & 1), abort_flag, gerr, kWaitLimitNs);
+        ok = mbar_wait(smem_u32(&ctl.q_full), (uint32_t)(ord & 1), abort_flag, kWaitLimitNs);
         if (!ok) break;
         const int n = ctl.sched_n[ord & 3];
         if (n == 0) break;
         tc_fence_after();
-        for (int j = 0; ok && j < n; ++j, ++t) {
+        for (int j = 0; ok && j < n; ++j) {
+          const RingPos k0 = kp;                        // the tile's two K units
+          RingPos k1 = kp;
+          k1.next(C::KSU);
           for (int x = 0; ok && x < 2; ++x) {
-            if (t > 0) {
-              ok = mbar_wait(smem_u32(&ctl.pv_iss[x]), (uint32_t)((t - 1) & 1), abort_flag, gerr, kWaitLimitNs);
+            if (n_qk > 0) {
+              ok = mbar_wait(smem_u32(&ctl.s_free), (uint32_t)((n_qk - 1) & 1), abort_flag, kWaitLimitNs);
               if (!ok) break;
               tc_fence_after();
             }
-            const uint32_t d = tmem + C::TM_S + (uint32_t)x * C::N;
-            for (int half = 0; ok && half < 2; ++half) {    // K unit = 64-column half of head_dim
-              const int64_t u = 2 * t + half;
-              const int slot = (int)(u % C::KSU);
+            for (int half = 0; ok && half < 2; ++half) {  // K unit = 64-column half of head_dim
+              const RingPos &kh = half ? k1 : k0;
               if (x == 0) {
-                ok = mbar_wait(smem_u32(&ctl.k_full[slot]), (uint32_t)((u / C::KSU) & 1), abort_flag, gerr,
-                               kWaitLimitNs);
+                ok = mbar_wait(smem_u32(&ctl.k_full[kh.slot]), kh.phase, abort_flag, kWaitLimitNs);
                 if (!ok) break;
                 tc_fence_after();
               }
               const uint32_t qa = q_s + x * C::Q_BYTES + half * C::Q_CHUNK;
-              const uint32_t kb = k_s + slot * C::UNIT;
+              const uint32_t kb = k_s + kh.slot * C::UNIT;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)              // 16-column steps over the 64 columns
-                mma_ss(d, smem_desc_sw128(qa + kk * 32, 16, 1024), smem_desc_sw128(kb + kk * 32, 16, 1024),
-                       C::IDESC_QK, (half > 0 || kk > 0) ? 1u : 0u);
-              if (x == 1) mma_commit(smem_u32(&ctl.k_empty[slot]));
+                mma_ss(tmem + C::TM_S, smem_desc_sw128(qa + kk * 32, 16, 1024),
+                       smem_desc_sw128(kb + kk * 32, 16, 1024), C::IDESC_QK, (half > 0 || kk > 0) ? 1u : 0u);
+              if (x == 1) mma_commit(smem_u32(&ctl.k_empty[kh.slot]));
             }
             if (!ok) break;
             mma_commit(smem_u32(&ctl.s_full[x]));
+            ++n_qk;
           }
+          kp = k1;
+          kp.next(C::KSU);
           if (ok && j == n - 1) mma_commit(smem_u32(&ctl.q_empty));   // the item's Q is no longer read
         }
         ++ord;
@@ -309,10 +333,11 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       }
       // every MMA issued by this thread must finish before TMEM is released
       mma_commit(smem_u32(&ctl.drain));
-      mbar_wait(smem_u32(&ctl.drain), 0, nullptr, nullptr, kWaitLimitNs);
+      mbar_wait(smem_u32(&ctl.drain), 0, nullptr, kWaitLimitNs);
     } else if (lane == 0 && warp == 3) {
       bool ok = true;
-      int64_t t = 0;
+      uint32_t tpar = 0;                                // parity of this CTA's tile count
+      RingPos vp;
       for (int item = blockIdx.x; ok && item < n_items; item += stride) {
         Item it;
         int32_t eb;
@@ -320,35 +345,36 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         int kmin, kmax;
         block_keys(a, it, 0, 1, false, kmin, kmax);
         const int n_tiles = kmax / C::N - kmin / C::N + 1;
-        for (int j = 0; ok && j < n_tiles; ++j, ++t) {
+        for (int j = 0; ok && j < n_tiles; ++j, tpar ^= 1u) {
+          const RingPos v0 = vp;
+          RingPos v1 = vp;
+          v1.next(C::VSU);
           for (int x = 0; ok && x < 2; ++x) {
-            ok = mbar_wait(smem_u32(&ctl.p_full[x]), (uint32_t)(t & 1), abort_flag, gerr, kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.p_full[x]), tpar, abort_flag, kWaitLimitNs);
             if (!ok) break;
             tc_fence_after();
-            for (int half = 0; ok && half < 2; ++half) {    // V unit = 64-key half of the tile
-              const int64_t u = 2 * t + half;
-              const int slot = (int)(u % C::VSU);
+            for (int half = 0; ok && half < 2; ++half) {  // V unit = 64-key half of the tile
+              const RingPos &vh = half ? v1 : v0;
               if (x == 0) {
-                ok = mbar_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1), abort_flag, gerr,
-                               kWaitLimitNs);
+                ok = mbar_wait(smem_u32(&ctl.v_full[vh.slot]), vh.phase, abort_flag, kWaitLimitNs);
                 if (!ok) break;
                 tc_fence_after();
               }
-              const uint32_t p_t = tmem + C::TM_S + (uint32_t)x * C::N + half * (C::VU_KEYS / 16) * 8;
-              const uint32_t vb = v_s + slot * C::UNIT;
+              const uint32_t p_t = tmem + C::TM_P + (uint32_t)x * (C::N / 2) + half * (C::VU_KEYS / 16) * 8;
+              const uint32_t vb = v_s + vh.slot * C::UNIT;
 #pragma unroll
               for (int kk = 0; kk < C::VU_KEYS / 16; ++kk)
                 mma_ts(tmem + C::TM_O + (uint32_t)x * C::D, p_t + kk * 8,
                        smem_desc_sw128(vb + kk * 16 * 128, C::VU_CHUNK, 1024), C::IDESC_PV,
                        (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
-              if (x == 1) mma_commit(smem_u32(&ctl.v_empty[slot]));
+              if (x == 1) mma_commit(smem_u32(&ctl.v_empty[vh.slot]));
             }
             if (!ok) break;
             mma_commit(smem_u32(&ctl.o_full[x]));
             if (j == n_tiles - 1) mma_commit(smem_u32(&ctl.o_item[x]));   // the item's O_X is final
-            tc_fence_before();
-            mbar_arrive(smem_u32(&ctl.pv_iss[x]));
           }
+          vp = v1;
+          vp.next(C::VSU);
         }
       }
       if (!ok) {
@@ -356,7 +382,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         report(a.err, SWA_ERR_TIMEOUT);
       }
       mma_commit(smem_u32(&ctl.drain2));
-      mbar_wait(smem_u32(&ctl.drain2), 0, nullptr, nullptr, kWaitLimitNs);
+      mbar_wait(smem_u32(&ctl.drain2), 0, nullptr, kWaitLimitNs);
     }
   }
   // warps 2 and 7 have no role: they only give their registers to the softmax
@@ -372,10 +398,11 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int sid = threadIdx.x - 256 - 128 * x;         // 0 .. 127 within the warpgroup
     const int row = 32 * (warp & 3) + lane;              // TMEM lane of this thread
     const uint32_t lane_t = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t s_col = tmem + lane_t + C::TM_S + (uint32_t)x * N;
+    const uint32_t s_col = tmem + lane_t + C::TM_S;
+    const uint32_t p_col = tmem + lane_t + C::TM_P + (uint32_t)x * (N / 2);
     const uint32_t o_col = tmem + lane_t + C::TM_O + (uint32_t)x * C::D;
     const float asl2 = fmaxf(fabsf(a.scale * kLog2e), 1.17549435e-38f);
-    int64_t t = 0;                                       // global tile index
+    int t = 0;                                           // this CTA's tiles so far
     int n_done = 0;                                      // items finished
     bool ok = true;
     int item = blockIdx.x - stride;
@@ -396,7 +423,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < n_tiles; ++j, ++t) {
         const int kt0 = (tile_lo + j) * N;
-        ok = mbar_wait(smem_u32(&ctl.s_full[x]), (uint32_t)(t & 1), abort_flag, gerr, kWaitLimitNs);
+        ok = mbar_wait(smem_u32(&ctl.s_full[x]), (uint32_t)(t & 1), abort_flag, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         uint32_t raw[N];
@@ -405,6 +432,8 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         for (int c = 0; c < N / 32; ++c)
           tmem_ld32_red<NEG>(s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c), lred[c]);
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&ctl.s_free));             // S may take the other tile's next QK
         float xv[N];
         float mx;
         if (__all_sync(0xffffffffu, klo <= kt0 && khi >= kt0 + N - 1)) {
@@ -437,10 +466,10 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           const float m_next = need ? m_new : m_used;
           const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_next);
           if (j > 0) {
-            // PV_x(t-1) must be complete before O_x is rescaled (S_x(t), seen
-            // complete, was issued after it, so its o_full phase is the only
-            // one that can still be open)
-            ok = mbar_wait(smem_u32(&ctl.o_full[x]), (uint32_t)((t - 1) & 1), abort_flag, gerr, kWaitLimitNs);
+            // PV_x(t-1) must be complete before O_x is rescaled.  The P store
+            // of tile t-1 waited for PV_x(t-2), so the o_full phase of
+            // PV_x(t-1) is the only one that can still be open.
+            ok = mbar_wait(smem_u32(&ctl.o_full[x]), (uint32_t)((t - 1) & 1), abort_flag, kWaitLimitNs);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll 1
@@ -464,29 +493,36 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         uint64_t s2[2] = {0, 0};                         // two paired partial sums (0.0f bits)
         if (x == 0 && kt0 + N > it.seq_len) {
           // keys past the sequence end: their V rows may hold anything; zero
-          // them before P_A(t) is published (PV_B(t) follows PV_A(t)).  The
-          // V units of tile t sit in other ring slots than tile t-1's, which
-          // PV_B(t-1) may still read, and their fill is the latest one of
-          // their slots, so the v_full parity is unambiguous.
+          // them before P_A(t) is published (PV_B(t) follows PV_A(t)).  V unit
+          // 2t + half is the latest fill of its slot (tile t-1's units sit in
+          // other slots, which PV_B(t-1) may still read), so its v_full parity
+          // is unambiguous.
           for (int half = 0; half < 2 && ok; ++half) {
             const int k0 = kt0 + half * C::VU_KEYS;
             if (k0 + C::VU_KEYS <= it.seq_len) continue;
-            const int64_t u = 2 * t + half;
+            const uint32_t u = 2u * (uint32_t)t + half;
             const int slot = (int)(u % C::VSU);
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1),
-                                                   abort_flag, gerr, kWaitLimitNs));
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.v_full[slot]), (u / C::VSU) & 1u, abort_flag,
+                                                   kWaitLimitNs));
             if (!ok) break;
-            const int r0 = max(0, it.seq_len - k0);
-            const int n16 = (C::VU_KEYS - r0) * 8 * C::CH;
-            for (int i = sid; i < n16; i += 128) {
-              const int c = i / ((C::VU_KEYS - r0) * 8), rem = i % ((C::VU_KEYS - r0) * 8);
-              uint4 *dst = reinterpret_cast<uint4 *>(dsm_ptr + C::OFF_V + slot * C::UNIT + c * C::VU_CHUNK +
-                                                     (r0 + rem / 8) * 128 + (rem % 8) * 16);
-              *dst = make_uint4(0, 0, 0, 0);
+            const int r0 = max(0, it.seq_len - k0);       // first row to clear
+            uint8_t *unit = dsm_ptr + C::OFF_V + slot * C::UNIT;
+#pragma unroll 1
+            for (int i = sid; i < C::CH * C::VU_KEYS * 8; i += 128) {   // 16-byte pieces: chunk, row, piece
+              const int r = (i >> 3) & (C::VU_KEYS - 1);
+              if (r >= r0)
+                *reinterpret_cast<uint4 *>(unit + (i >> 9) * C::VU_CHUNK + r * 128 + (i & 7) * 16) =
+                    make_uint4(0, 0, 0, 0);
             }
           }
           if (!ok) break;
           fence_proxy_async_smem();
+        }
+        if (t > 0) {
+          // P_x(t) overwrites P_x(t-1): PV_x(t-1) must have read it
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_full[x]), (uint32_t)((t - 1) & 1), abort_flag, kWaitLimitNs));
+          if (!ok) break;
+          tc_fence_after();
         }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {                 // P in two stores of 32 columns (64 keys each)
@@ -499,7 +535,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             s2[c & 1] = f2_add(s2[c & 1], f2_pack(p0, p1));
             pk[c] = pack_bf16(p0, p1);
           }
-          tmem_st32(s_col + 32 * hh, pk);
+          tmem_st32(p_col + 32 * hh, pk);
         }
         {
           float a0, a1, b0, b1;
@@ -523,8 +559,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
       }
       // the item's last PV_x (one o_item phase per item)
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item[x]), (uint32_t)(n_done & 1), abort_flag, gerr,
-                                             kWaitLimitNs));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item[x]), (uint32_t)(n_done & 1), abort_flag, kWaitLimitNs));
       ++n_done;
       if (!ok) break;
       // epilogue: O / l -> bf16, 64 columns per pass, 32-byte stores.  The

@@ -50,38 +50,29 @@ __device__ inline bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Gives up (returns
-// false) after `limit_ns`, or early when the CTA-local flag *abort is set or
-// the launch-wide error word already carries SWA_ERR_TIMEOUT (so one stalled
-// CTA makes the others quit quickly).  Either pointer may be null: drain
-// waits pass nulls so they only stop at the time limit.  Inlined: a kernel
-// that splits its registers with setmaxnreg cannot call one function from
-// both sides of the split.
-__device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const volatile int *abort,
-                                            const volatile int32_t *err, uint64_t limit_ns) {
-  uint64_t t0 = 0;     // the clock is read only once a wait has really stalled
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0) {
-      if (abort != nullptr && *abort) return false;
-      if (err != nullptr && (*err & SWA_ERR_TIMEOUT)) return false;
-      const uint64_t now = global_ns();
-      if (t0 == 0) t0 = now;
-      else if (now - t0 > limit_ns) return false;
-    }
-  }
-}
-__device__ inline bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int *abort,
-                                 const volatile int32_t *err, uint64_t limit_ns) {
+// false) after `limit_ns`, or early once the CTA-local flag *abort is set (so
+// the other roles of a CTA whose pipeline stalled quit quickly).  `abort` may
+// be null: drain waits pass null so they only stop at the time limit.  Each
+// try_wait suspends the thread for a while when the phase is still open, so
+// the loop is not hot.  Inlined: a kernel that splits its registers with
+// setmaxnreg cannot call one function from both sides of the split.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int *abort,
+                                          uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort, err, limit_ns);
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if ((abort != nullptr && *abort) || global_ns() - t0 > limit_ns) return false;
+  }
+  return true;
 }
+
 // For waits that are usually short (a partner warpgroup at the same point):
 // poll without suspending first, then wait as above.
-__device__ inline bool mbar_wait_spin(uint32_t bar, uint32_t parity, const volatile int *abort,
-                                      const volatile int32_t *err, uint64_t limit_ns) {
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, const volatile int *abort,
+                                               uint64_t limit_ns) {
   for (int i = 0; i < 64; ++i)
     if (mbar_test_wait(bar, parity)) return true;
-  return mbar_wait(bar, parity, abort, err, limit_ns);
+  return mbar_wait(bar, parity, abort, limit_ns);
 }
 
 // ---------------------------------------------------------------- TMA
