@@ -344,6 +344,32 @@ int swa_mm_paged_attention_split_static(
     int32_t dtype, int32_t num_splits, const int32_t *splits_per_seq, void *out, float *lse,
     int32_t *err, void *stream);
 
+/*
+ * swa_set_watchdog -- bound of the pipeline waits in the tensor-core
+ * attention kernels, and a switch that makes those waits run out on purpose.
+ *
+ * The pages have no counterpart of this call.  Every wait of the tcgen05
+ * prefill kernels (a TMA copy landing, an MMA completing, a softmax warpgroup
+ * publishing its probabilities) is bounded in time; when a bound runs out the
+ * kernel sets SWA_ERR_TIMEOUT in `err`, lets its own copies and MMAs finish,
+ * frees its tensor memory and returns, so the CUDA context stays usable.
+ *   wait_limit_ns  bound of each such wait for the attention calls made after
+ *                  this one; 0 restores the default (200 ms); otherwise it must
+ *                  lie in [1 us, 10 s] (else SWA_E_SIZE, nothing changes).
+ *                  The final drains always keep the default bound.
+ *   stall          nonzero: in every later tensor-core attention call the PV
+ *                  issuer first waits on a barrier that nothing signals, so
+ *                  that wait runs out after wait_limit_ns and the whole
+ *                  pipeline of every CTA stops through the timeout path (the
+ *                  call returns SWA_OK, `err` gets SWA_ERR_TIMEOUT, the
+ *                  outputs are unspecified).  0: normal operation.  This is
+ *                  for failure-detection tests of callers and of this library.
+ * Settings are process-wide (all devices, all host threads) and apply to
+ * calls enqueued after this one; the CUDA-core and decode kernels have no
+ * pipeline waits and ignore them.  Returns SWA_OK or SWA_E_SIZE.
+ */
+int swa_set_watchdog(uint64_t wait_limit_ns, int32_t stall);
+
 /* Library version string, e.g. "swa-gb300 0.1 sm_103a". */
 const char *swa_version(void);
 

@@ -14,6 +14,8 @@ Entry points (same names as the C ABI):
 * ``lse_combine``            merge of split-KV partials by their LSE
 * ``swa_mm_paged_attention_split_static``  split-KV attention and merge with
   the partials in a library-owned array, for callers that cannot allocate
+* ``swa_set_watchdog``       bound of the tensor-core kernels' pipeline waits,
+  and a switch that makes them run out (failure-detection tests)
 """
 from __future__ import annotations
 
@@ -25,7 +27,8 @@ import torch
 from .build_lib import LIB_PATH
 
 __all__ = ["swa_slot_mapping", "swa_slot_mapping_cp", "swa_kv_cache_write", "swa_tile_bounds",
-           "swa_mm_paged_attention", "lse_combine", "swa_mm_paged_attention_split_static", "lib", "SwaError", "DTYPE_BF16", "DTYPE_FP32", "ERR_BITS"]
+           "swa_mm_paged_attention", "lse_combine", "swa_mm_paged_attention_split_static", "swa_set_watchdog",
+           "lib", "SwaError", "DTYPE_BF16", "DTYPE_FP32", "ERR_BITS"]
 
 DTYPE_BF16 = 0
 DTYPE_FP32 = 1
@@ -55,7 +58,7 @@ _SIGS = {
 }
 # Bytes of the library-owned array behind swa_mm_paged_attention_split_static.
 STATIC_SCRATCH_BYTES = 16 << 20
-EXPORTED = tuple(_SIGS) + ("swa_version",)
+EXPORTED = tuple(_SIGS) + ("swa_version", "swa_set_watchdog")
 
 
 class SwaError(RuntimeError):
@@ -79,6 +82,8 @@ def lib() -> ctypes.CDLL:
             fn.restype = ctypes.c_int
         handle.swa_version.restype = ctypes.c_char_p
         handle.swa_version.argtypes = []
+        handle.swa_set_watchdog.restype = ctypes.c_int
+        handle.swa_set_watchdog.argtypes = [ctypes.c_uint64, ctypes.c_int32]
         _LIB = handle
     return _LIB
 
@@ -315,3 +320,10 @@ def swa_mm_paged_attention_split_static(q, k_cache, v_cache, block_table, query_
         _ptr(splits_per_seq), _ptr(out), _ptr(lse), _ptr(err), _stream(stream))
     _check(rc, "swa_mm_paged_attention_split_static")
     return out, lse
+
+
+def swa_set_watchdog(wait_limit_ns: int = 0, stall: bool = False):
+    """Bound of every pipeline wait in the tensor-core attention kernels for
+    later calls (0 = the default 200 ms) and, with ``stall``, a wait that can
+    only run out, so those calls report SWA_ERR_TIMEOUT.  Process-wide."""
+    _check(lib().swa_set_watchdog(int(wait_limit_ns), int(bool(stall))), "swa_set_watchdog")

@@ -1,5 +1,6 @@
 // The C ABI (include/swa.h): host-side argument checks, then one launch per
 // call on the caller's stream.  Nothing here allocates device memory.
+#include <atomic>
 #include <cmath>
 
 #include "common.cuh"
@@ -16,6 +17,10 @@ inline int finish(cudaError_t e) { return e == cudaSuccess ? SWA_OK : SWA_E_CUDA
 inline bool chunk_ok(int window, int chunk_size, int chunk_lookback) {
   return chunk_lookback < 0 || (window > 0 && chunk_size > 0);
 }
+
+// swa_set_watchdog: process-wide settings read by every later attention call.
+std::atomic<uint64_t> g_wait_ns{0};      // 0: the default bound
+std::atomic<int32_t> g_stall{0};
 
 }  // namespace
 
@@ -66,6 +71,9 @@ int prepare_attention(const void *q, const void *k_cache, const void *v_cache, i
   a.chunk_size = chunk_size; a.chunk_lookback = chunk_lookback < 0 ? -1 : chunk_lookback;
   a.num_splits = num_splits; a.splits_per_seq = (num_splits > 1) ? splits_per_seq : nullptr;
   a.out = out; a.lse = lse; a.partial_out = partial_out; a.partial_lse = partial_lse; a.err = err;
+  const uint64_t wait_ns = g_wait_ns.load();
+  a.wait_ns = wait_ns != 0 ? wait_ns : kDefaultWaitNs;
+  a.stall = g_stall.load();
   return SWA_OK;
 }
 
@@ -94,6 +102,13 @@ int check_lse_combine(const void *partial_out, const float *partial_lse, int32_t
 extern "C" {
 
 const char *swa_version(void) { return "swa-gb300 0.1 sm_103a"; }
+
+int swa_set_watchdog(uint64_t wait_limit_ns, int32_t stall) {
+  if (wait_limit_ns != 0 && (wait_limit_ns < 1000ull || wait_limit_ns > 10000000000ull)) return SWA_E_SIZE;
+  g_wait_ns.store(wait_limit_ns);
+  g_stall.store(stall != 0 ? 1 : 0);
+  return SWA_OK;
+}
 
 int swa_slot_mapping(const int32_t *query_start_loc, const int64_t *positions,
                      const int32_t *context_lens, const int32_t *block_table, int64_t block_table_stride,

@@ -118,6 +118,7 @@ struct Ctrl {
   uint64_t pv_iss[NS];                   // PV of the tile issued (its S buffer may be overwritten)
   uint64_t o_full[2];                    // PV of tile t complete, alternating by t & 1
   uint64_t o_item, drain, drain2;
+  uint64_t stall;                        // never signalled: the watchdog test's stalled wait
   uint64_t xch[2];                       // exchanges between the softmax warpgroups
   int32_t sched_n[4];                    // tile count of item ord at [ord & 3] (0: end of stream)
   uint32_t tmem_base;
@@ -170,6 +171,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     mbar_init(smem_u32(&ctl.o_item), 1);
     mbar_init(smem_u32(&ctl.drain), 1);
+    mbar_init(smem_u32(&ctl.stall), 1);                 // nothing ever arrives here
     mbar_init(smem_u32(&ctl.drain2), 1);
     mbar_fence_init();
     tma_prefetch_map(&tm_q);
@@ -185,6 +187,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   volatile int *abort_flag = &ctl.abort;
+  const uint64_t wl = a.wait_ns;                      // bound of every pipeline wait (drains: kWaitLimitNs)
   const int stride = gridDim.x;
 
   // Register split (warpgroup-wide, at the top of each side so every warp of a
@@ -227,7 +230,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const int n_tiles = kmax / C::N - tile_lo + 1;
       if (warp == 0 && lane == 0) {
         // Q: the previous item's last QK has to be done with the buffer
-        if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, kWaitLimitNs);
+        if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, wl);
         if (ok) {
           // the MMA warp learns the item's tile count from here once q_full completes
           ctl.sched_n[ord & 3] = n_tiles;
@@ -261,7 +264,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (u >= SU) {
           const uint32_t empty = smem_u32(is_v ? &ctl.v_empty[slot_i] : &ctl.k_empty[slot_i]);
           ok = __all_sync(0xffffffffu,
-                          mbar_wait(empty, (uint32_t)(((u / SU) - 1) & 1), abort_flag, kWaitLimitNs));
+                          mbar_wait(empty, (uint32_t)(((u / SU) - 1) & 1), abort_flag, wl));
           if (!ok) break;
         }
         const int t = ul >> 1, half = ul & 1;
@@ -300,7 +303,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       // end of stream for the MMA warp: one more q_full phase without data, once
       // the MMA warp is past the last real one (its last QK released q_empty)
       if (warp == 0 && ok &&
-          (ord == 0 || mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, kWaitLimitNs))) {
+          (ord == 0 || mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, wl))) {
         ctl.sched_n[ord & 3] = 0;
         mbar_arrive(smem_u32(&ctl.q_full));
       }
@@ -318,7 +321,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       int t = 0;                                         // tiles of this CTA's stream
       while (ok) {
         // the next item's Q has landed (or the stream has ended: 0 tiles)
-        ok = mbar_wait(smem_u32(&ctl.q_full), (uint32_t)(ord & 1), abort_flag, kWaitLimitNs);
+        ok = mbar_wait(smem_u32(&ctl.q_full), (uint32_t)(ord & 1), abort_flag, wl);
         if (!ok) break;
         const int n = ctl.sched_n[ord & 3];
         if (n == 0) break;
@@ -326,7 +329,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int j = 0; ok && j < n; ++j, ++t) {
           const int sb = (int)(t % C::NS);               // S buffer of tile t
           if (t >= C::NS) {
-            ok = mbar_wait(smem_u32(&ctl.pv_iss[sb]), (uint32_t)(((t / C::NS) - 1) & 1), abort_flag, kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.pv_iss[sb]), (uint32_t)(((t / C::NS) - 1) & 1), abort_flag, wl);
             if (!ok) break;
             tc_fence_after();
           }
@@ -334,7 +337,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           for (int half = 0; ok && half < 2; ++half) {
             const uint32_t u = 2u * (uint32_t)t + half;
             const int slot = (int)(u % C::KSU);
-            ok = mbar_wait(smem_u32(&ctl.k_full[slot]), (uint32_t)((u / C::KSU) & 1), abort_flag, kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.k_full[slot]), (uint32_t)((u / C::KSU) & 1), abort_flag, wl);
             if (!ok) break;
             tc_fence_after();
             const uint32_t qa = q_s + half * C::KU_CH * C::Q_CHUNK;
@@ -363,6 +366,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_wait(smem_u32(&ctl.drain), 0, nullptr, kWaitLimitNs);
     } else if (lane == 0 && warp == 3) {
       bool ok = true;
+      // watchdog test: a wait that can only run out (a.stall, set by swa_set_watchdog)
+      if (a.stall) ok = mbar_wait(smem_u32(&ctl.stall), 0, abort_flag, wl);
       int t = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += stride) {
         Item it;
@@ -373,11 +378,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int n_tiles = kmax / C::N - kmin / C::N + 1;
         for (int j = 0; ok && j < n_tiles; ++j, ++t) {
           const int sb = (int)(t % C::NS);
-          ok = mbar_wait(smem_u32(&ctl.p_full[sb]), (uint32_t)((t / C::NS) & 1), abort_flag, kWaitLimitNs);
+          ok = mbar_wait(smem_u32(&ctl.p_full[sb]), (uint32_t)((t / C::NS) & 1), abort_flag, wl);
           for (int half = 0; ok && half < 2; ++half) {
             const uint32_t u = 2u * (uint32_t)t + half;
             const int slot = (int)(u % C::VSU);
-            ok = mbar_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1), abort_flag, kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1), abort_flag, wl);
             if (!ok) break;
             tc_fence_after();
             const uint32_t p_t = tmem + C::TM_S + (uint32_t)sb * C::N + half * (C::VU_KEYS / 16) * 8;
@@ -445,7 +450,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int kt0 = (tile_lo + j) * C::N;
         const int kc0 = kt0 + h * NH;                    // key of this warpgroup's first column
         const int sb = (int)(t % C::NS);                 // S buffer of tile t
-        ok = mbar_wait(smem_u32(&ctl.s_full[sb]), (uint32_t)((t / C::NS) & 1), abort_flag, kWaitLimitNs);
+        ok = mbar_wait(smem_u32(&ctl.s_full[sb]), (uint32_t)((t / C::NS) & 1), abort_flag, wl);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         uint32_t raw[NH];
@@ -484,7 +489,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mx = mx == -INFINITY ? -INFINITY : mx * asl2;
         ctl.red[xc & 1][h][row] = mx;
         mbar_arrive(smem_u32(&ctl.xch[xc & 1]));
-        ok = mbar_wait_spin(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag, kWaitLimitNs);
+        ok = mbar_wait_spin(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag, wl);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
 #pragma unroll
         for (int g = 0; g < NSW; ++g)
@@ -502,7 +507,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           const float m_next = need ? m_new : m_used;
           const float alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_next);
           if (j > 0) {
-            ok = mbar_wait(smem_u32(&ctl.o_full[(t - 1) & 1]), (uint32_t)(((t - 1) >> 1) & 1), abort_flag, kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.o_full[(t - 1) & 1]), (uint32_t)(((t - 1) >> 1) & 1), abort_flag, wl);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll 1
@@ -544,7 +549,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           // them.  Once PV_{t-1} is done every earlier unit of each V slot has
           // been consumed, so the v_full parity below is unambiguous.
           if (j > 0) {
-            ok = mbar_wait(smem_u32(&ctl.o_full[(t - 1) & 1]), (uint32_t)(((t - 1) >> 1) & 1), abort_flag, kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.o_full[(t - 1) & 1]), (uint32_t)(((t - 1) >> 1) & 1), abort_flag, wl);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           }
           for (int half = 0; half < 2 && ok; ++half) {
@@ -553,7 +558,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint32_t u = 2u * (uint32_t)t + half;
             const int slot = (int)(u % C::VSU);
             ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.v_full[slot]), (uint32_t)((u / C::VSU) & 1),
-                                                   abort_flag, kWaitLimitNs));
+                                                   abort_flag, wl));
             if (!ok) break;
             const int r0 = max(0, it.seq_len - k0);       // first row to clear
             uint8_t *unit = dsm_ptr + C::OFF_V + slot * C::UNIT;
@@ -589,12 +594,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (have) row_setup<C::N>(a, nit, row, G, lane, cur);
       }
       // the item's last PV (one o_item phase per item), then the full row sum
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item), (uint32_t)(n_done & 1), abort_flag, kWaitLimitNs));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item), (uint32_t)(n_done & 1), abort_flag, wl));
       ++n_done;
       if (!ok) break;
       ctl.red[xc & 1][h][row] = l;
       mbar_arrive(smem_u32(&ctl.xch[xc & 1]));
-      ok = __all_sync(0xffffffffu, mbar_wait_spin(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag, kWaitLimitNs));
+      ok = __all_sync(0xffffffffu, mbar_wait_spin(smem_u32(&ctl.xch[xc & 1]), (uint32_t)((xc >> 1) & 1), abort_flag, wl));
       if (!ok) break;
 #pragma unroll
       for (int g = 0; g < NSW; ++g)

@@ -88,6 +88,7 @@ struct PairCtrl {
   uint64_t s_free;                       // the last QK's scores were loaded: S may be overwritten
   uint64_t o_full[2], o_item[2];         // PV_X(t) complete; the item's last PV_X complete
   uint64_t drain, drain2;
+  uint64_t stall;                        // never signalled: the watchdog test's stalled wait
   int32_t sched_n[4];                    // tile count of item ord at [ord & 3] (0: end of stream)
   uint32_t tmem_base;
   int abort;
@@ -146,6 +147,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
     mbar_init(smem_u32(&ctl.s_free), 128);
     mbar_init(smem_u32(&ctl.drain), 1);
+    mbar_init(smem_u32(&ctl.stall), 1);                 // nothing ever arrives here
     mbar_init(smem_u32(&ctl.drain2), 1);
     mbar_fence_init();
     tma_prefetch_map(&tm_q);
@@ -161,6 +163,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   volatile int *abort_flag = &ctl.abort;
+  const uint64_t wl = a.wait_ns;                      // bound of every pipeline wait (drains: kWaitLimitNs)
   const int stride = gridDim.x;
 
   if (warp < 8) {
@@ -199,7 +202,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const int n_tiles = kmax / C::N - tile_lo + 1;
       if (warp == 0 && lane == 0) {
         // Q_A and Q_B: the previous item's last QK_B has to be done with them
-        if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, kWaitLimitNs);
+        if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, wl);
         if (ok) {
           ctl.sched_n[ord & 3] = n_tiles;
           mbar_expect_tx(smem_u32(&ctl.q_full), 2 * C::Q_BYTES);
@@ -233,7 +236,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (u >= SU) {
           const uint32_t empty = smem_u32(is_v ? &ctl.v_empty[slot_i] : &ctl.k_empty[slot_i]);
           ok = __all_sync(0xffffffffu,
-                          mbar_wait(empty, (uint32_t)(((u / SU) - 1) & 1), abort_flag, kWaitLimitNs));
+                          mbar_wait(empty, (uint32_t)(((u / SU) - 1) & 1), abort_flag, wl));
           if (!ok) break;
         }
         const int t = ul >> 1, half = ul & 1;
@@ -271,7 +274,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       if (warp == 0 && ord > 0) mbar_wait(smem_u32(&ctl.q_full), (ord - 1) & 1, nullptr, kWaitLimitNs);
       // end of stream for the QK issuer: one more q_full phase without data
       if (warp == 0 && ok &&
-          (ord == 0 || mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, kWaitLimitNs))) {
+          (ord == 0 || mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, wl))) {
         ctl.sched_n[ord & 3] = 0;
         mbar_arrive(smem_u32(&ctl.q_full));
       }
@@ -287,7 +290,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       int n_qk = 0;                                     // QKs issued (both tiles)
       RingPos kp;
       while (ok) {
-        ok = mbar_wait(smem_u32(&ctl.q_full), (uint32_t)(ord & 1), abort_flag, kWaitLimitNs);
+        ok = mbar_wait(smem_u32(&ctl.q_full), (uint32_t)(ord & 1), abort_flag, wl);
         if (!ok) break;
         const int n = ctl.sched_n[ord & 3];
         if (n == 0) break;
@@ -298,14 +301,14 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           k1.next(C::KSU);
           for (int x = 0; ok && x < 2; ++x) {
             if (n_qk > 0) {
-              ok = mbar_wait(smem_u32(&ctl.s_free), (uint32_t)((n_qk - 1) & 1), abort_flag, kWaitLimitNs);
+              ok = mbar_wait(smem_u32(&ctl.s_free), (uint32_t)((n_qk - 1) & 1), abort_flag, wl);
               if (!ok) break;
               tc_fence_after();
             }
             for (int half = 0; ok && half < 2; ++half) {  // K unit = 64-column half of head_dim
               const RingPos &kh = half ? k1 : k0;
               if (x == 0) {
-                ok = mbar_wait(smem_u32(&ctl.k_full[kh.slot]), kh.phase, abort_flag, kWaitLimitNs);
+                ok = mbar_wait(smem_u32(&ctl.k_full[kh.slot]), kh.phase, abort_flag, wl);
                 if (!ok) break;
                 tc_fence_after();
               }
@@ -336,6 +339,8 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       mbar_wait(smem_u32(&ctl.drain), 0, nullptr, kWaitLimitNs);
     } else if (lane == 0 && warp == 3) {
       bool ok = true;
+      // watchdog test: a wait that can only run out (a.stall, set by swa_set_watchdog)
+      if (a.stall) ok = mbar_wait(smem_u32(&ctl.stall), 0, abort_flag, wl);
       uint32_t tpar = 0;                                // parity of this CTA's tile count
       RingPos vp;
       for (int item = blockIdx.x; ok && item < n_items; item += stride) {
@@ -350,13 +355,13 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           RingPos v1 = vp;
           v1.next(C::VSU);
           for (int x = 0; ok && x < 2; ++x) {
-            ok = mbar_wait(smem_u32(&ctl.p_full[x]), tpar, abort_flag, kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.p_full[x]), tpar, abort_flag, wl);
             if (!ok) break;
             tc_fence_after();
             for (int half = 0; ok && half < 2; ++half) {  // V unit = 64-key half of the tile
               const RingPos &vh = half ? v1 : v0;
               if (x == 0) {
-                ok = mbar_wait(smem_u32(&ctl.v_full[vh.slot]), vh.phase, abort_flag, kWaitLimitNs);
+                ok = mbar_wait(smem_u32(&ctl.v_full[vh.slot]), vh.phase, abort_flag, wl);
                 if (!ok) break;
                 tc_fence_after();
               }
@@ -423,7 +428,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < n_tiles; ++j, ++t) {
         const int kt0 = (tile_lo + j) * N;
-        ok = mbar_wait(smem_u32(&ctl.s_full[x]), (uint32_t)(t & 1), abort_flag, kWaitLimitNs);
+        ok = mbar_wait(smem_u32(&ctl.s_full[x]), (uint32_t)(t & 1), abort_flag, wl);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         uint32_t raw[N];
@@ -469,7 +474,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             // PV_x(t-1) must be complete before O_x is rescaled.  The P store
             // of tile t-1 waited for PV_x(t-2), so the o_full phase of
             // PV_x(t-1) is the only one that can still be open.
-            ok = mbar_wait(smem_u32(&ctl.o_full[x]), (uint32_t)((t - 1) & 1), abort_flag, kWaitLimitNs);
+            ok = mbar_wait(smem_u32(&ctl.o_full[x]), (uint32_t)((t - 1) & 1), abort_flag, wl);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll 1
@@ -503,7 +508,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const uint32_t u = 2u * (uint32_t)t + half;
             const int slot = (int)(u % C::VSU);
             ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.v_full[slot]), (u / C::VSU) & 1u, abort_flag,
-                                                   kWaitLimitNs));
+                                                   wl));
             if (!ok) break;
             const int r0 = max(0, it.seq_len - k0);       // first row to clear
             uint8_t *unit = dsm_ptr + C::OFF_V + slot * C::UNIT;
@@ -520,7 +525,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         if (t > 0) {
           // P_x(t) overwrites P_x(t-1): PV_x(t-1) must have read it
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_full[x]), (uint32_t)((t - 1) & 1), abort_flag, kWaitLimitNs));
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_full[x]), (uint32_t)((t - 1) & 1), abort_flag, wl));
           if (!ok) break;
           tc_fence_after();
         }
@@ -559,7 +564,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
       }
       // the item's last PV_x (one o_item phase per item)
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item[x]), (uint32_t)(n_done & 1), abort_flag, kWaitLimitNs));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item[x]), (uint32_t)(n_done & 1), abort_flag, wl));
       ++n_done;
       if (!ok) break;
       // epilogue: O / l -> bf16, 64 columns per pass, 32-byte stores.  The

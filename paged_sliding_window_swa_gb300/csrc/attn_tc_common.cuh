@@ -15,7 +15,7 @@
 namespace swa {
 namespace {
 
-constexpr uint64_t kWaitLimitNs = 200000000ull;    // 200 ms per wait: far above any real stall
+constexpr uint64_t kWaitLimitNs = kDefaultWaitNs;  // drain waits: every copy and MMA must land before exit
 constexpr int kMaxUnits = 8;                       // ring slots per operand
 
 struct Item {

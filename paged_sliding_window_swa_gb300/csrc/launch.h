@@ -26,7 +26,12 @@ struct AttnArgs {
   void *partial_out;
   float *partial_lse;
   int32_t *err;
+  uint64_t wait_ns;                     // bound of each pipeline wait in the tensor-core kernels
+  int32_t stall;                        // watchdog test: the PV issuer waits on a barrier nothing signals
 };
+
+// Default bound of a pipeline wait: far above any real stall.
+constexpr uint64_t kDefaultWaitNs = 200000000ull;
 
 // Host-side checks of swa_mm_paged_attention.  Returns SWA_OK and fills `a`,
 // or a negative SWA_E_* code; an empty call (no tokens or no sequences) passes

@@ -137,3 +137,11 @@ def test_kv_cache_write_rejects_bad_arguments(lib):
     assert call(dtype=5) == -3
     assert call() == -1
     assert call(T=0) == 0
+
+
+def test_watchdog_rejects_out_of_range_bounds(lib):
+    """The bound must be 0 (default) or within [1 us, 10 s]; a refused call changes nothing."""
+    assert lib.swa_set_watchdog(999, 0) == -2
+    assert lib.swa_set_watchdog(10_000_000_001, 0) == -2
+    assert lib.swa_set_watchdog(1000, 0) == 0
+    assert lib.swa_set_watchdog(0, 0) == 0
