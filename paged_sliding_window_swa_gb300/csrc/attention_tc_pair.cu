@@ -449,10 +449,15 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           for (int c = 1; c < N / 32; ++c) r = NEG ? fminf(r, lred[c]) : fmaxf(r, lred[c]);
           mx = NEG ? -r : r;
         } else {
+          // column c is visible when c_lo <= c <= c_lo + span: one unsigned compare
+          // (an empty interval puts c_lo past the tile, so c - c_lo wraps above span)
+          const bool empty = khi < klo;
+          const int c_lo = empty ? 2 * N : klo - kt0;
+          const uint32_t c_span = empty ? 0u : (uint32_t)(khi - klo);
 #pragma unroll
           for (int c = 0; c < N; ++c)
-            xv[c] = (kt0 + c >= klo && kt0 + c <= khi) ? (NEG ? -__uint_as_float(raw[c]) : __uint_as_float(raw[c]))
-                                                      : -INFINITY;
+            xv[c] = (uint32_t)(c - c_lo) <= c_span ? (NEG ? -__uint_as_float(raw[c]) : __uint_as_float(raw[c]))
+                                                   : -INFINITY;
           float m4[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) m4[i] = xv[i];

@@ -2,11 +2,12 @@
 // notes, section 1.1: partials merged by LSE equal one softmax over the whole
 // sequence).
 //
-// A group of LPR lanes owns one (token, head) row; every lane moves 16-byte
-// vectors, so a row of D bf16 values is read with D*2/16 lanes in one
-// coalesced sweep per partition, two partitions' loads in flight at once.
-// Partitions whose LSE is -inf are skipped before their output is touched, so
-// their (unwritten) rows are never read.
+// Many rows: a group of LPR lanes owns one (token, head) row; every lane moves
+// 16-byte vectors, so a row of D bf16 values is read with D*2/16 lanes in one
+// coalesced sweep per partition, two partitions' loads in flight at once.  Few
+// rows: one warp per row with all partitions in flight (below).  Partitions
+// whose LSE is -inf are skipped before their output is touched, so their
+// (unwritten) rows are never read.
 #include "common.cuh"
 #include "launch.h"
 
@@ -117,13 +118,105 @@ lse_combine_kernel(const T *__restrict__ po, const float *__restrict__ pl, int32
   if (out_lse != nullptr && gl == 0) out_lse[row] = (wsum > 0.f) ? L + logf(wsum) : -INFINITY;
 }
 
+// Few rows (a decode step: tokens x heads in the thousands) leave too little
+// work in flight for the kernel above, whose partitions follow one another.
+// Here one warp owns a row: lane p loads partition p's LSE (one load for up to
+// 32 partitions), the warp reduces the maximum, and the lanes split into
+// kGroups groups that each take every kGroups-th partition; every live
+// partition's vectors are requested before the first multiply-add, and the
+// groups' sums meet through shuffles.
+template <typename T, int D>
+struct RowWarpShape {
+  static constexpr int kVecElems = 16 / sizeof(T);
+  static constexpr int kVecs = D / kVecElems;                 // 16-byte vectors per row
+  static constexpr int kLanes = kVecs < 32 ? kVecs : 32;      // lanes per partition group
+  static constexpr int kGroups = 32 / kLanes;
+  static constexpr int kVpl = kVecs / kLanes;                 // vectors per lane and partition
+  // partitions per lane per batch: up to 32 partitions per batch, at most 16
+  // vectors (64 registers) in flight per lane
+  static constexpr int kInFlight = 32 / kGroups < 16 / kVpl ? 32 / kGroups : 16 / kVpl;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads)
+lse_combine_rowwarp_kernel(const T *__restrict__ po, const float *__restrict__ pl, int32_t num_splits,
+                           int64_t rows, T *__restrict__ out, float *__restrict__ out_lse) {
+  using Sh = RowWarpShape<T, D>;
+  constexpr int E = Sh::kVecElems;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  if (row >= rows) return;                                   // warp-uniform
+  const int g = lane / Sh::kLanes, gl = lane % Sh::kLanes;
+  // lane p holds partition p's LSE; with up to 32 partitions the weights then
+  // come from the lanes by shuffle, with no second load
+  const float l0 = lane < num_splits ? __ldg(pl + (int64_t)lane * rows + row) : -INFINITY;
+  float L = l0;
+  for (int p = lane + 32; p < num_splits; p += 32) L = fmaxf(L, __ldg(pl + (int64_t)p * rows + row));
+  L = warp_max(L);
+  const float w0 = l0 == -INFINITY ? 0.f : __expf(l0 - L);
+  float acc[Sh::kVpl * E];
+#pragma unroll
+  for (int i = 0; i < Sh::kVpl * E; ++i) acc[i] = 0.f;
+  float wsum = 0.f;
+  if (L != -INFINITY) {
+    for (int p0 = 0; p0 < num_splits; p0 += Sh::kGroups * Sh::kInFlight) {
+      float w[Sh::kInFlight];
+      uint4 v[Sh::kInFlight][Sh::kVpl];
+#pragma unroll
+      for (int i = 0; i < Sh::kInFlight; ++i) {
+        const int p = p0 + g + i * Sh::kGroups;
+        const float wp = __shfl_sync(0xffffffffu, w0, p & 31);
+        if (p < 32) {
+          w[i] = p < num_splits ? wp : 0.f;
+        } else {
+          const float lp = p < num_splits ? __ldg(pl + (int64_t)p * rows + row) : -INFINITY;
+          w[i] = lp == -INFINITY ? 0.f : __expf(lp - L);
+        }
+        const uint4 *src = reinterpret_cast<const uint4 *>(po + ((int64_t)p * rows + row) * D);
+#pragma unroll
+        for (int j = 0; j < Sh::kVpl; ++j)
+          v[i][j] = w[i] > 0.f ? __ldg(src + gl + j * Sh::kLanes) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < Sh::kInFlight; ++i) {
+        wsum += w[i];
+#pragma unroll
+        for (int j = 0; j < Sh::kVpl; ++j) accum<T>(acc + j * E, v[i][j], w[i]);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = Sh::kLanes; o < 32; o <<= 1) {                // the groups' partial sums meet
+    wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+#pragma unroll
+    for (int i = 0; i < Sh::kVpl * E; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+  }
+  if (g != 0) return;
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+  for (int i = 0; i < Sh::kVpl * E; ++i) acc[i] *= inv;
+  uint4 *dst = reinterpret_cast<uint4 *>(out + row * D);
+#pragma unroll
+  for (int v = 0; v < Sh::kVpl; ++v) dst[gl + v * Sh::kLanes] = pack<T>(acc + v * E);
+  if (out_lse != nullptr && gl == 0) out_lse[row] = (wsum > 0.f) ? L + logf(wsum) : -INFINITY;
+}
+
+// Below this many rows the warp-per-row kernel is used.
+constexpr int64_t kRowWarpMaxRows = 32768;
+
 template <typename T, int D>
 cudaError_t run(const void *po, const float *pl, int32_t P, int64_t rows, void *out, float *ol,
                 cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  if (rows < kRowWarpMaxRows) {
+    const int64_t grid = ceil_div(rows, kThreads / 32);
+    lse_combine_rowwarp_kernel<T, D><<<(unsigned)grid, kThreads, 0, st>>>(
+        static_cast<const T *>(po), pl, P, rows, static_cast<T *>(out), ol);
+    return cudaGetLastError();
+  }
   using Sh = CombineShape<T, D>;
   const int64_t rows_per_block = (kThreads / 32) * Sh::kRowsPerWarp;
   const int64_t grid = ceil_div(rows, rows_per_block);
-  if (grid == 0) return cudaSuccess;
   lse_combine_kernel<T, D><<<(unsigned)grid, kThreads, 0, st>>>(
       static_cast<const T *>(po), pl, P, rows, static_cast<T *>(out), ol);
   return cudaGetLastError();
