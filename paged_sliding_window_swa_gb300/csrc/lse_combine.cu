@@ -120,11 +120,10 @@ lse_combine_kernel(const T *__restrict__ po, const float *__restrict__ pl, int32
 
 // Few rows (a decode step: tokens x heads in the thousands) leave too little
 // work in flight for the kernel above, whose partitions follow one another.
-// Here one warp owns a row: lane p loads partition p's LSE (one load for up to
-// 32 partitions), the warp reduces the maximum, and the lanes split into
-// kGroups groups that each take every kGroups-th partition; every live
-// partition's vectors are requested before the first multiply-add, and the
-// groups' sums meet through shuffles.
+// Here one warp owns a row: the lanes read the partitions' LSEs for the
+// maximum, then split into kGroups groups that each take every kGroups-th
+// partition, a batch of partitions' vectors in flight before the first
+// multiply-add; the groups' sums meet through shuffles.
 template <typename T, int D>
 struct RowWarpShape {
   static constexpr int kVecElems = 16 / sizeof(T);
@@ -132,9 +131,9 @@ struct RowWarpShape {
   static constexpr int kLanes = kVecs < 32 ? kVecs : 32;      // lanes per partition group
   static constexpr int kGroups = 32 / kLanes;
   static constexpr int kVpl = kVecs / kLanes;                 // vectors per lane and partition
-  // partitions per lane per batch: up to 32 partitions per batch, at most 16
-  // vectors (64 registers) in flight per lane
-  static constexpr int kInFlight = 32 / kGroups < 16 / kVpl ? 32 / kGroups : 16 / kVpl;
+  // partitions per lane per batch: up to 32 partitions per batch, at most 8
+  // vectors per lane in flight (more measured slower at the decode size)
+  static constexpr int kInFlight = 32 / kGroups < 8 / kVpl ? 32 / kGroups : 8 / kVpl;
 };
 
 template <typename T, int D>
@@ -147,13 +146,9 @@ lse_combine_rowwarp_kernel(const T *__restrict__ po, const float *__restrict__ p
   const int64_t row = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   if (row >= rows) return;                                   // warp-uniform
   const int g = lane / Sh::kLanes, gl = lane % Sh::kLanes;
-  // lane p holds partition p's LSE; with up to 32 partitions the weights then
-  // come from the lanes by shuffle, with no second load
-  const float l0 = lane < num_splits ? __ldg(pl + (int64_t)lane * rows + row) : -INFINITY;
-  float L = l0;
-  for (int p = lane + 32; p < num_splits; p += 32) L = fmaxf(L, __ldg(pl + (int64_t)p * rows + row));
+  float L = -INFINITY;
+  for (int p = lane; p < num_splits; p += 32) L = fmaxf(L, __ldg(pl + (int64_t)p * rows + row));
   L = warp_max(L);
-  const float w0 = l0 == -INFINITY ? 0.f : __expf(l0 - L);
   float acc[Sh::kVpl * E];
 #pragma unroll
   for (int i = 0; i < Sh::kVpl * E; ++i) acc[i] = 0.f;
@@ -165,13 +160,8 @@ lse_combine_rowwarp_kernel(const T *__restrict__ po, const float *__restrict__ p
 #pragma unroll
       for (int i = 0; i < Sh::kInFlight; ++i) {
         const int p = p0 + g + i * Sh::kGroups;
-        const float wp = __shfl_sync(0xffffffffu, w0, p & 31);
-        if (p < 32) {
-          w[i] = p < num_splits ? wp : 0.f;
-        } else {
-          const float lp = p < num_splits ? __ldg(pl + (int64_t)p * rows + row) : -INFINITY;
-          w[i] = lp == -INFINITY ? 0.f : __expf(lp - L);
-        }
+        const float lp = p < num_splits ? __ldg(pl + (int64_t)p * rows + row) : -INFINITY;
+        w[i] = lp == -INFINITY ? 0.f : __expf(lp - L);
         const uint4 *src = reinterpret_cast<const uint4 *>(po + ((int64_t)p * rows + row) * D);
 #pragma unroll
         for (int j = 0; j < Sh::kVpl; ++j)

@@ -65,7 +65,7 @@ slot_mapping_kernel(const int32_t *__restrict__ qsl, const int64_t *__restrict__
     for (int i = 0; i < kTokPerThread; ++i) res[i] = pad_id;
   } else {
     // positions: given, or (kDerive) the request's context length plus the
-    // token's index in the request
+    // token's index in the request (filled below, once the request is known)
     int64_t p[kTokPerThread];
     if (kDerive) {
 #pragma unroll
@@ -85,10 +85,70 @@ slot_mapping_kernel(const int32_t *__restrict__ qsl, const int64_t *__restrict__
     int r = find_req(qsl, num_reqs, t0);
     int32_t r_start = __ldg(qsl + r), r_end = __ldg(qsl + r + 1);
     int32_t r_ctx = kDerive ? __ldg(ctx + r) : 0;
+    if (kDerive) {
+#pragma unroll
+      for (int i = 0; i < kTokPerThread; ++i) p[i] = (int64_t)r_ctx + (t0 + i - r_start);
+    }
+    // Fast path: the 8 tokens are consecutive positions of one request that
+    // stay inside one page (and, for a CP cache, one interleave run of one
+    // rank): one ownership test and one block-table read serve all of them.
+    bool done = false;
+    if (t0 >= r_start && t0 + kTokPerThread <= r_end && p[0] >= 0 && p[kTokPerThread - 1] - p[0] == kTokPerThread - 1) {
+      bool consecutive = true;
+#pragma unroll
+      for (int i = 1; i < kTokPerThread - 1; ++i) consecutive &= p[i] == p[0] + i;
+      if (consecutive) {
+        const int64_t ps = p[0];
+        int64_t page = -1, off = 0;
+        bool mine = true, one_page = false;
+        if (kMode == kCpPow2) {
+          const int64_t v_idx = ps >> g.vbs_shift;
+          const int32_t v_off = (int32_t)(ps & (g.vbs - 1));
+          if ((v_off & (g.interleave - 1)) + kTokPerThread <= g.interleave) {
+            mine = ((v_off >> g.inter_shift) & (g.world - 1)) == g.rank;
+            const int32_t local = ((v_off >> g.wi_shift) << g.inter_shift) | (v_off & (g.interleave - 1));
+            page = v_idx * g.blocks_per_kv_block + (local >> g.shift);
+            off = local & (block_size - 1);
+            one_page = off + kTokPerThread <= block_size;
+          }
+        } else if (kMode == kCp) {
+          if (ps <= INT32_MAX) {
+            const uint32_t v_idx = (uint32_t)ps / (uint32_t)g.vbs;
+            const uint32_t v_off = (uint32_t)ps - v_idx * (uint32_t)g.vbs;
+            const uint32_t I = (uint32_t)g.interleave, Wd = (uint32_t)g.world;
+            if (v_off % I + kTokPerThread <= I) {
+              mine = (v_off / I) % Wd == (uint32_t)g.rank;
+              const uint32_t local = (v_off / (Wd * I)) * I + v_off % I;
+              page = (int64_t)v_idx * g.blocks_per_kv_block + local / (uint32_t)block_size;
+              off = local % (uint32_t)block_size;
+              one_page = off + kTokPerThread <= block_size;
+            }
+          }
+        } else if (kMode == kPlainPow2) {
+          page = ps >> g.shift;
+          off = ps & (block_size - 1);
+          one_page = off + kTokPerThread <= block_size;
+        } else {
+          page = ps / block_size;
+          off = ps - page * block_size;
+          one_page = off + kTokPerThread <= block_size;
+        }
+        if (!mine) {                                         // another rank's tokens
+#pragma unroll
+          for (int i = 0; i < kTokPerThread; ++i) res[i] = pad_id;
+          done = true;
+        } else if (one_page && page < stride) {
+          const int32_t base = (int32_t)((int64_t)__ldg(bt + (int64_t)r * stride + page) * block_size + off);
+#pragma unroll
+          for (int i = 0; i < kTokPerThread; ++i) res[i] = base + i;
+          done = true;
+        }
+      }
+    }
     int64_t last = -1;                                       // (request, page) of the last lookup
     int32_t blk = 0;
 #pragma unroll
-    for (int i = 0; i < kTokPerThread; ++i) {
+    for (int i = 0; i < kTokPerThread && !done; ++i) {
       const int64_t t = t0 + i;
       res[i] = pad_id;
       if (t >= num_tokens) continue;
@@ -99,7 +159,7 @@ slot_mapping_kernel(const int32_t *__restrict__ qsl, const int64_t *__restrict__
         if (kDerive) r_ctx = __ldg(ctx + r);
       }
       if (t < r_start || t >= r_end) continue;              // outside every request
-      const int64_t ps = kDerive ? (int64_t)r_ctx + (t - r_start) : p[i];
+      const int64_t ps = kDerive ? (int64_t)r_ctx + (t - r_start) : p[i];   // (p[] of the fast path is r's)
       if (ps < 0) { report(err, SWA_ERR_POSITION); continue; }
       int64_t page, off;
       if (kMode == kCpPow2) {
