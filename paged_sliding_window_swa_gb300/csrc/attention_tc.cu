@@ -95,6 +95,7 @@ struct Cfg {
   static constexpr int OFF_K = Q_BYTES;
   static constexpr int OFF_V = OFF_K + KSU * UNIT;
   static constexpr int OFF_CTRL = OFF_V + VSU * UNIT;
+  static constexpr int O_CHUNK = M * 128;            // bytes of one staged 64-column chunk of O (bf16)
   static constexpr int TM_O = 0;        // TMEM columns: O [0, D), S buffer b at [D + b*N, D + (b+1)*N)
   static constexpr int TM_S = D;
   static constexpr uint32_t TM_COLS = 512;
@@ -107,6 +108,7 @@ struct Cfg {
   static_assert(KSU <= kMaxUnits && VSU <= kMaxUnits && KSU >= 2 && VSU >= 2, "ring sizes");
   static_assert(KW >= 1 && KW <= 2 && VW >= 1 && VW <= 4, "producer warps");
   static_assert((N / 16) * KU_CH <= 32 && (VU_KEYS / 16) * CH <= 32, "one warp instruction per unit");
+  static_assert(CH * O_CHUNK <= VSU * UNIT, "the item's O (bf16) is staged in the V ring");
 };
 
 template <int NSW, int NS>
@@ -120,10 +122,42 @@ struct Ctrl {
   uint64_t o_item, drain, drain2;
   uint64_t stall;                        // never signalled: the watchdog test's stalled wait
   uint64_t xch[2];                       // exchanges between the softmax warpgroups
-  int32_t sched_n[4];                    // tile count of item ord at [ord & 3] (0: end of stream)
+  uint64_t rec_full[kRecSlots];          // item record ord published at [ord % kRecSlots]
+  uint64_t ostage_full;                  // the item's O staged in the V ring (or stored directly)
+  uint64_t ostage_free;                  // the staged O was read by its TMA store: the V ring is free
+  ItemRec rec[kRecSlots];
   uint32_t tmem_base;
   int abort;
 };
+
+// V warp 4: an item's O, staged in the V ring by the softmax (bf16, boxes of
+// 64 columns x 128 rows, 128-byte swizzle), to the output.  A tile whose rows
+// all lie inside the sequence goes out as TMA stores issued by lane 0 (which
+// waits until they have read the ring, unless it is the CTA's last); any other
+// tile is copied by the warp, one 512-byte row per instruction, for the rows
+// of the sequence only.  `tok`: the tile's first token, `ntok`: its tokens
+// inside the sequence.
+template <class C>
+__device__ inline void store_staged_o(const CUtensorMap *tm_o, int o_tma, const AttnArgs &a, uint32_t v_s, int G,
+                                      int bq, int hk, int tok, int ntok, int lane, bool last) {
+  static_assert(C::CH * 8 == 32, "one lane per 16-byte piece of a row");
+  if (o_tma && ntok == bq) {
+    if (lane == 0) {
+      for (int c = 0; c < C::CH; ++c) tma_store_3d(tm_o, v_s + c * C::O_CHUNK, c * 64, hk * G, tok);
+      bulk_commit();
+      if (!last) bulk_wait_read_all();
+    }
+    return;
+  }
+  const int lg = 31 - __clz(G);                         // G is a power of two
+  const int chunk = lane >> 3, j = lane & 7;
+  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+  for (int r = 0; r < (ntok << lg); ++r) {
+    const uint4 v = ld_shared_v4(v_s + (uint32_t)(chunk * C::O_CHUNK + r * 128 + ((j ^ (r & 7)) << 4)));
+    const int64_t orow = (int64_t)(tok + (r >> lg)) * a.hq + hk * G + (r & (G - 1));
+    *reinterpret_cast<uint4 *>(out + orow * C::D + lane * 8) = v;
+  }
+}
 
 template <class C>
 constexpr int smem_bytes() { return C::OFF_CTRL + (int)sizeof(Ctrl<C::NSW, C::NS>); }
@@ -131,7 +165,8 @@ constexpr int smem_bytes() { return C::OFF_CTRL + (int)sizeof(Ctrl<C::NSW, C::NS
 template <class C, bool NEG>
 __global__ void __launch_bounds__(C::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const int G, const int n_items) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+               const AttnArgs a, const int G, const int n_items, const int o_tma) {
   // Everything lives in dynamic shared memory, which starts 1024-byte aligned
   // when a kernel has no static shared data (checked below): the 128-byte
   // swizzled tiles need that alignment and there is no room for slack.
@@ -170,6 +205,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(smem_u32(&ctl.o_full[i]), 1);
     }
     mbar_init(smem_u32(&ctl.o_item), 1);
+    for (int i = 0; i < kRecSlots; ++i) mbar_init(smem_u32(&ctl.rec_full[i]), 1);
+    mbar_init(smem_u32(&ctl.ostage_full), 128 * C::NSW);
+    mbar_init(smem_u32(&ctl.ostage_free), 1);
     mbar_init(smem_u32(&ctl.drain), 1);
     mbar_init(smem_u32(&ctl.stall), 1);                 // nothing ever arrives here
     mbar_init(smem_u32(&ctl.drain2), 1);
@@ -177,6 +215,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tma_prefetch_map(&tm_q);
     tma_prefetch_map(&tm_k);
     tma_prefetch_map(&tm_v);
+    if (o_tma) tma_prefetch_map(&tm_o);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl.tmem_base), C::TM_COLS);
@@ -217,6 +256,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     int64_t u_base = 0;                                 // units issued by this warp before this item
     int ord = 0;                                        // valid items so far
     bool ok = true;
+    // V warps: the previous item's output tile (kv head, first token, tokens inside the sequence)
+    int prev_hk = 0, prev_tok = 0, prev_ntok = 0;
     for (int item = blockIdx.x; ok && item < n_items; item += stride) {
       Item it;
       int32_t eb;
@@ -224,24 +265,44 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (eb != 0 && warp == 0 && lane == 0) report(a.err, eb);
         continue;
       }
-      int kmin, kmax;
-      block_keys(a, it, lane, 32, true, kmin, kmax);
-      const int tile_lo = kmin / C::N;
-      const int n_tiles = kmax / C::N - tile_lo + 1;
-      if (warp == 0 && lane == 0) {
-        // Q: the previous item's last QK has to be done with the buffer
-        if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, wl);
+      int tile_lo, n_tiles, nr, rrs, rre;
+      block_keys_rec<C::N>(a, it, lane, tile_lo, n_tiles, nr, rrs, rre);
+      if (warp == 0) {
+        // Q: the previous item's last QK has to be done with the buffer.  The
+        // item's record goes out first: the MMA warps and the softmax read it
+        // instead of decoding the item themselves.  (The slot's previous
+        // record, kRecSlots items back, has been read: this QK stream could
+        // not have got here before the softmax and the PV warp had started a
+        // later item.)
+        if (ord > 0 && lane == 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, wl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
         if (ok) {
-          // the MMA warp learns the item's tile count from here once q_full completes
-          ctl.sched_n[ord & 3] = n_tiles;
-          mbar_expect_tx(smem_u32(&ctl.q_full), C::Q_BYTES);
-          for (int c = 0; c < C::CH; ++c)
-            tma_load_3d(q_s + c * C::Q_CHUNK, &tm_q, c * 64, it.hk * G, it.qstart + it.qpos_lo,
-                        smem_u32(&ctl.q_full));
+          write_rec(ctl.rec[ord % kRecSlots], it, tile_lo, n_tiles, nr, rrs, rre, lane);
+          if (lane == 0) {
+            mbar_arrive(smem_u32(&ctl.rec_full[ord % kRecSlots]));
+            mbar_expect_tx(smem_u32(&ctl.q_full), C::Q_BYTES);
+            for (int c = 0; c < C::CH; ++c)
+              tma_load_3d(q_s + c * C::Q_CHUNK, &tm_q, c * 64, it.hk * G, it.qstart + it.qpos_lo,
+                          smem_u32(&ctl.q_full));
+          }
         }
       }
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       ++ord;                                            // items whose Q copy was issued
+      if (is_v && ord > 1) {
+        // The previous item's O is staged in the V ring once its last PV is
+        // done (so are its V units): V warp 4 stores it and frees the ring.
+        const uint32_t par = (uint32_t)((ord - 2) & 1);
+        if (share == 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.ostage_full), par, abort_flag, wl));
+          if (!ok) break;
+          store_staged_o<C>(&tm_o, o_tma, a, v_s, G, bq, prev_hk, prev_tok, prev_ntok, lane, false);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctl.ostage_free));
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.ostage_free), par, abort_flag, wl));
+        if (!ok) break;
+      }
       const int total_boxes = (n_tiles * C::N) / R;
       const int32_t *bt = a.block_table + (int64_t)it.s * a.bt_stride;
       auto resolve = [&](int b) -> int {                // slot of the first key of box b
@@ -290,6 +351,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (lane < boxes * uch && lane % nsh == share) tma_load_3d(d, map, x, it.hk, slot, full);
       }
       u_base += ul;                                     // units issued (all of them unless aborted)
+      prev_hk = it.hk;
+      prev_tok = it.qstart + it.qpos_lo;
+      prev_ntok = min(bq, it.qlen - it.qpos_lo);
+    }
+    if (is_v && share == 0) {
+      // the last item's O
+      if (ok && ord > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.ostage_full), (uint32_t)((ord - 1) & 1), abort_flag, wl));
+        if (ok) store_staged_o<C>(&tm_o, o_tma, a, v_s, G, bq, prev_hk, prev_tok, prev_ntok, lane, true);
+      }
+      if (lane == 0) bulk_wait_all();                   // every store has landed before the CTA exits
     }
     if (!ok && lane == 0) {
       *abort_flag = 1;
@@ -304,7 +376,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       // the MMA warp is past the last real one (its last QK released q_empty)
       if (warp == 0 && ok &&
           (ord == 0 || mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, wl))) {
-        ctl.sched_n[ord & 3] = 0;
+        ctl.rec[ord % kRecSlots].n_tiles = 0;
+        __threadfence_block();
+        mbar_arrive(smem_u32(&ctl.rec_full[ord % kRecSlots]));
         mbar_arrive(smem_u32(&ctl.q_full));
       }
     }
@@ -323,7 +397,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // the next item's Q has landed (or the stream has ended: 0 tiles)
         ok = mbar_wait(smem_u32(&ctl.q_full), (uint32_t)(ord & 1), abort_flag, wl);
         if (!ok) break;
-        const int n = ctl.sched_n[ord & 3];
+        const int n = ctl.rec[ord % kRecSlots].n_tiles;
         if (n == 0) break;
         tc_fence_after();
         for (int j = 0; ok && j < n; ++j, ++t) {
@@ -369,13 +443,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       // watchdog test: a wait that can only run out (a.stall, set by swa_set_watchdog)
       if (a.stall) ok = mbar_wait(smem_u32(&ctl.stall), 0, abort_flag, wl);
       int t = 0;
-      for (int item = blockIdx.x; ok && item < n_items; item += stride) {
-        Item it;
-        int32_t eb;
-        if (!decode_item(a, item, bq, it, eb)) continue;
-        int kmin, kmax;
-        block_keys(a, it, 0, 1, false, kmin, kmax);
-        const int n_tiles = kmax / C::N - kmin / C::N + 1;
+      for (int ord = 0; ok; ++ord) {
+        // the item's record (n_tiles 0: the end of the stream)
+        ok = mbar_wait(smem_u32(&ctl.rec_full[ord % kRecSlots]), (uint32_t)((ord / kRecSlots) & 1), abort_flag, wl);
+        if (!ok) break;
+        const int n_tiles = ctl.rec[ord % kRecSlots].n_tiles;
+        if (n_tiles == 0) break;
         for (int j = 0; ok && j < n_tiles; ++j, ++t) {
           const int sb = (int)(t % C::NS);
           ok = mbar_wait(smem_u32(&ctl.p_full[sb]), (uint32_t)((t / C::NS) & 1), abort_flag, wl);
@@ -430,17 +503,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     int t = 0;                                           // this CTA's tiles so far
     int64_t xc = 0;                                      // exchanges so far (buffer xc & 1)
     int n_done = 0;                                      // items finished
-    bool ok = true;
-    // The next item's setup (a few dependent global loads) is done while the
-    // current item's last PV runs.
-    int item = blockIdx.x - stride;
+    // Items come from the records the Q producer publishes; the next one is
+    // set up while the current item's last PV runs.
     RowSetup cur;
-    bool have;
-    {
-      Item it;
-      have = next_item(a, item, stride, n_items, bq, it);
-      if (have) row_setup<C::N>(a, it, row, G, lane, cur);
-    }
+    bool have = false;
+    auto next_rec = [&]() -> bool {                      // false: the wait ran out
+      const int slot = n_done % kRecSlots;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.rec_full[slot]),
+                                             (uint32_t)((n_done / kRecSlots) & 1), abort_flag, wl)))
+        return false;
+      have = ctl.rec[slot].n_tiles > 0;
+      if (have) row_setup_rec(a, ctl.rec[slot], row, G, lane, cur);
+      return true;
+    };
+    bool ok = next_rec();
     while (ok && have) {
       const Item &it = cur.it;
       const int tile_lo = cur.tile_lo, n_tiles = cur.n_tiles;
@@ -593,14 +669,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       if (!ok) break;
       const bool row_valid = cur.row_valid;
       const int64_t out_row = cur.out_row;
-      {
-        Item nit;
-        have = next_item(a, item, stride, n_items, bq, nit);
-        if (have) row_setup<C::N>(a, nit, row, G, lane, cur);
-      }
-      // the item's last PV (one o_item phase per item), then the full row sum
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item), (uint32_t)(n_done & 1), abort_flag, wl));
       ++n_done;
+      if (!next_rec()) { ok = false; break; }
+      // the item's last PV (one o_item phase per item), then the full row sum
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item), (uint32_t)((n_done - 1) & 1), abort_flag, wl));
       if (!ok) break;
       ctl.red[xc & 1][h][row] = l;
       mbar_arrive(smem_u32(&ctl.xch[xc & 1]));
@@ -610,28 +682,33 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       for (int g = 0; g < NSW; ++g)
         if (g != h) l += ctl.red[xc & 1][g][row];
       ++xc;
-      // epilogue: O / l -> bf16, 64 columns per pass, 32-byte stores.  The
+      // epilogue: O / l -> bf16 rows in the V ring (free: the item's PVs are
+      // done and the V producers wait for ostage_free), laid out as the output
+      // map's boxes of 64 columns x 128 rows with the 128-byte swizzle, so that
+      // the 16-byte pieces of 8 rows hit all banks; V warp 4 stores them.  The
       // next item's first PV overwrites O only after this thread's P for it
       // (published after these loads completed).
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + out_row * C::D + h * DH;
 #pragma unroll 1
-      for (int c = 0; c < DH / EPW; ++c) {
-        uint32_t r[EPW];
-#pragma unroll
-        for (int k = 0; k < EPW / 32; ++k)
-          tmem_ld32(tmem + lane_t + C::TM_O + h * DH + EPW * c + 32 * k, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * k));
+      for (int c = 0; c < DH / 32; ++c) {                  // 32 columns: half of a staged 64-column chunk
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_t + C::TM_O + h * DH + 32 * c, r);
         tmem_wait_ld();
-        if (row_valid) {
-          uint32_t w[EPW / 2];
+        const int col = h * DH + 32 * c;
+        const uint32_t rb = v_s + (uint32_t)((col >> 6) * C::O_CHUNK + row * 128);
 #pragma unroll
-          for (int e = 0; e < EPW / 2; ++e)
-            w[e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
-#pragma unroll
-          for (int e = 0; e < EPW / 16; ++e) st_global_v8(o + EPW * c + 16 * e, w + 8 * e);
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = ((col & 63) >> 3) + jj;            // 16-byte piece of the 128-byte row
+          st_shared_v4(rb + ((uint32_t)(j ^ (row & 7)) << 4),
+                       pack_bf16(__uint_as_float(r[8 * jj]) * inv, __uint_as_float(r[8 * jj + 1]) * inv),
+                       pack_bf16(__uint_as_float(r[8 * jj + 2]) * inv, __uint_as_float(r[8 * jj + 3]) * inv),
+                       pack_bf16(__uint_as_float(r[8 * jj + 4]) * inv, __uint_as_float(r[8 * jj + 5]) * inv),
+                       pack_bf16(__uint_as_float(r[8 * jj + 6]) * inv, __uint_as_float(r[8 * jj + 7]) * inv));
         }
       }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&ctl.ostage_full));
       if (row_valid && h == 0 && a.lse != nullptr)
         a.lse[out_row] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
       tc_fence_before();
@@ -665,6 +742,12 @@ cudaError_t run(const AttnArgs &a, cudaStream_t st) {
       !make_map(&mv, a.v_cache, C::D, a.hkv, slots, C::D * esz, (uint64_t)a.hkv * C::D * esz, 64, 1,
                 (uint32_t)min(a.block_size, C::VU_KEYS)))
     return cudaErrorInvalidValue;
+  // the output through the same box shape as Q (TMA stores of whole tiles);
+  // an output the map cannot describe is written with plain stores
+  CUtensorMap mo;
+  memset(&mo, 0, sizeof(mo));
+  const int o_tma = make_map(&mo, a.out, C::D, a.hq, a.num_tokens, C::D * esz, (uint64_t)a.hq * C::D * esz, 64, G, bq)
+                        ? 1 : 0;
   constexpr int smem = smem_bytes<C>();
   static_assert(smem <= 227 * 1024, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<C, NEG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -678,7 +761,7 @@ cudaError_t run(const AttnArgs &a, cudaStream_t st) {
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, attn_tc_kernel<C, NEG>) != cudaSuccess || fa.numRegs != C::LAUNCH_REGS)
     return cudaErrorInvalidConfiguration;
-  attn_tc_kernel<C, NEG><<<grid, C::THREADS, smem, st>>>(mq, mk, mv, a, G, (int)items);
+  attn_tc_kernel<C, NEG><<<grid, C::THREADS, smem, st>>>(mq, mk, mv, mo, a, G, (int)items, o_tma);
   return cudaGetLastError();
 }
 

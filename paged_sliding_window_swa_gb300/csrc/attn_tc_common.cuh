@@ -167,6 +167,142 @@ __device__ inline void row_setup(const AttnArgs &a, const Item &it, int row, int
   }
 }
 
+// An item as the Q-loading producer decoded it, published in a ring of
+// kRecSlots records in shared memory for the MMA issuers and the softmax, so
+// that they do not repeat the decode (a chain of dependent global loads) at
+// every item boundary.  n_tiles 0 marks the end of the CTA's stream.  The
+// record also holds the image ranges that meet the item's rows (nr of them;
+// -1 when more than kRecRanges do, and the softmax scans them itself).
+constexpr int kRecSlots = 4;
+constexpr int kRecRanges = 4;
+struct ItemRec {
+  Item it;
+  int tile_lo, n_tiles;
+  int nr;
+  int rs[kRecRanges], re[kRecRanges];
+};
+
+// Whole warp, warp-uniform item: the item's tile range (the union of
+// block_keys) and the image ranges that meet its rows, the i-th of them kept
+// by lane i < kRecRanges in (rs, re); nr counts all of them.
+template <int N>
+__device__ inline void block_keys_rec(const AttnArgs &a, const Item &it, int lane, int &tile_lo, int &n_tiles,
+                                      int &nr, int &rs, int &re) {
+  int emax = -1, smin = INT_MAX;
+  nr = 0;
+  rs = 0;
+  re = -1;
+  if (a.mm_ranges != nullptr) {
+    const int32_t *rg = a.mm_ranges + (int64_t)it.s * a.max_mm_ranges * 2;
+    const int clamp = a.window > 0 ? it.q_lo - a.window + 1 : INT_MIN;
+    for (int b = 0; b < a.max_mm_ranges; b += 32) {
+      int s0 = 0, e0 = -1;
+      if (b + lane < a.max_mm_ranges) {
+        s0 = __ldg(rg + 2 * (b + lane));
+        e0 = __ldg(rg + 2 * (b + lane) + 1);
+      }
+      const bool meets = s0 < e0 && s0 <= it.q_hi && e0 >= it.q_lo;
+      if (meets) {
+        emax = max(emax, e0);
+        smin = min(smin, max(s0, clamp));
+      }
+      uint32_t m = __ballot_sync(0xffffffffu, meets);
+      while (m != 0 && nr < kRecRanges) {              // warp-uniform
+        const int src = __ffs(m) - 1;
+        m &= m - 1;
+        const int s1 = __shfl_sync(0xffffffffu, s0, src), e1 = __shfl_sync(0xffffffffu, e0, src);
+        if (lane == nr) {
+          rs = s1;
+          re = e1;
+        }
+        ++nr;
+      }
+      nr += __popc(m);                                 // the ones past kRecRanges are only counted
+    }
+    emax = __reduce_max_sync(0xffffffffu, emax);
+    smin = __reduce_min_sync(0xffffffffu, smin);
+  }
+  int kmin, kmax;
+  union_keys(a, it, emax, smin, kmin, kmax);
+  tile_lo = kmin / N;
+  n_tiles = kmax / N - tile_lo + 1;
+}
+
+// Whole warp: writes the record (n_tiles 0: the end of the stream).  The
+// caller publishes it afterwards with one release (an mbarrier arrive).
+__device__ inline void write_rec(ItemRec &r, const Item &it, int tile_lo, int n_tiles, int nr, int rs, int re,
+                                 int lane) {
+  if (lane < nr && lane < kRecRanges) {
+    r.rs[lane] = rs;
+    r.re[lane] = re;
+  }
+  if (lane == 0) {
+    r.it = it;
+    r.tile_lo = tile_lo;
+    r.n_tiles = n_tiles;
+    r.nr = nr <= kRecRanges ? nr : -1;
+  }
+  __threadfence_block();
+  __syncwarp();
+}
+
+// A softmax thread's RowSetup from a record: its row's interval from the
+// record's ranges, or, for a record that could not hold them all, from a scan
+// of the sequence's ranges by the warp (same rule as row_setup).
+__device__ inline void row_setup_rec(const AttnArgs &a, const ItemRec &r, int row, int G, int lane,
+                                     RowSetup &rs) {
+  rs.it = r.it;
+  rs.tile_lo = r.tile_lo;
+  rs.n_tiles = r.n_tiles;
+  const Item &it = rs.it;
+  const int qpos = it.qpos_lo + row / G;
+  const int q = it.ctx + qpos;
+  const int rclamp = a.window > 0 ? q - a.window + 1 : INT_MIN;
+  int rhi = -1, rlo = INT_MAX;
+  const int nr = r.nr;
+  if (nr >= 0) {
+    for (int i = 0; i < nr; ++i) {
+      const int s1 = r.rs[i], e1 = r.re[i];
+      if (s1 <= q && q <= e1) {
+        rhi = max(rhi, e1);
+        rlo = min(rlo, max(s1, rclamp));
+      }
+    }
+  } else {
+    const int32_t *rg = a.mm_ranges + (int64_t)it.s * a.max_mm_ranges * 2;
+    const int wrow0 = row - lane;
+    const int wq_lo = it.ctx + it.qpos_lo + wrow0 / G;
+    const int wq_hi = it.ctx + it.qpos_lo + (wrow0 + 31) / G;
+    for (int b = 0; b < a.max_mm_ranges; b += 32) {
+      int s0 = 0, e0 = -1;
+      if (b + lane < a.max_mm_ranges) {
+        s0 = __ldg(rg + 2 * (b + lane));
+        e0 = __ldg(rg + 2 * (b + lane) + 1);
+      }
+      uint32_t m = __ballot_sync(0xffffffffu, s0 < e0 && s0 <= wq_hi && e0 >= wq_lo);
+      while (m != 0) {
+        const int src = __ffs(m) - 1;
+        m &= m - 1;
+        const int s1 = __shfl_sync(0xffffffffu, s0, src), e1 = __shfl_sync(0xffffffffu, e0, src);
+        if (s1 <= q && q <= e1) {
+          rhi = max(rhi, e1);
+          rlo = min(rlo, max(s1, rclamp));
+        }
+      }
+    }
+  }
+  rs.row_valid = qpos < it.qlen;
+  if (rs.row_valid) {
+    rs.klo = max(0, min(base_lo(q, a.window, a.chunk_size, a.chunk_lookback), rlo));
+    rs.khi = min(max(base_hi(q, a.window, it.causal, it.seq_len), rhi), it.seq_len - 1);
+    rs.out_row = (int64_t)(it.qstart + qpos) * a.hq + it.hk * G + row % G;
+  } else {
+    rs.klo = 1;
+    rs.khi = 0;
+    rs.out_row = 0;
+  }
+}
+
 // ------------------------------------------------------------------ host side
 using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,

@@ -90,6 +90,31 @@ def test_shapes_all_rows(D, B, G, err):
     _check(lay, _all_rows(lay), err=err)
 
 
+@pytest.mark.parametrize("D,G,window,causal", [(256, 2, 48, True), (256, 1, 300, False), (128, 2, 300, True),
+                                              (128, 4, 48, False)])
+def test_many_image_ranges_per_tile_all_rows(D, G, window, causal, err):
+    """Dozens of short, partly overlapping image ranges: a 128-row tile meets more of
+    them than an item record holds, so the softmax scans the sequence's ranges itself."""
+    rng = np.random.default_rng(7 * D + G)
+    qlen = np.array([333, 517], dtype=np.int32)
+    ctx = np.array([150, 41], dtype=np.int32)
+    seq = (ctx + qlen).astype(np.int32)
+    per = []
+    for s in range(2):
+        lst = []
+        for a in range(3, int(seq[s]) - 12, 13):
+            b = a + int(rng.integers(0, 12))          # 1 to 12 tokens, every 13th start
+            lst.append((a, b))
+        lst.append((int(seq[s]) // 3, int(seq[s]) // 3 + 90))   # one that overlaps several
+        per.append(lst)
+    bt, nb = W._block_table(rng, seq, 32, spare_blocks=5)
+    lay = W.Layout(f"many_ranges_d{D}_g{G}", query_lens=qlen, seq_lens=seq, mm_ranges=W._pad_ranges(per),
+                   block_table=bt, num_blocks=nb, num_heads_q=2 * G, num_heads_kv=2, head_dim=D,
+                   block_size=32, window=window, causal=causal, dtype="bf16",
+                   max_num_tokens=int(qlen.sum()) + 9)
+    _check(lay, _all_rows(lay), err=err)
+
+
 def test_unused_cache_rows_never_reach_the_output(err):
     """Spare blocks and page tails hold NaN; the output must stay finite and exact."""
     for seed in range(4):
