@@ -7,42 +7,50 @@
 // one 128-row query tile -- 128 / G query positions x the G query heads of one
 // kv head (GQA packing: every K/V tile is staged once for the whole group) --
 // and its key loop covers the 128-key tiles of the union of its rows' visible
-// intervals (the pruned tile range of the union formula).  All roles walk the
-// same item sequence, compute each item's tile range themselves, and count
-// tiles, K/V units and exchanges globally, so the rings, the S buffers and
-// every barrier phase simply continue from one item to the next: the next
-// item's Q copy and first two QK MMAs overlap the current item's tail.
+// intervals (the pruned tile range of the union formula).  A scheduler warp
+// decodes the items and publishes them as records in a small ring (the item,
+// its tile range and the image ranges meeting its rows); every role reads
+// them and counts tiles, K/V units and exchanges globally, so the rings, the
+// S buffers and every barrier phase simply continue from one item to the
+// next: the next item's Q copy and first two QK MMAs overlap the current
+// item's tail.
 //
 // Built for head_dim 256 (head_dim 128 runs on attention_tc_pair.cu).
 // Shared memory: the Q tile (TMA, 128-byte swizzled, K-major) and two rings
 // of 32 KB units: a K unit holds one half of
 // head_dim for all 128 keys of a tile, a V unit all of head_dim for one
 // 64-key half of a tile, so QK consumes two K units and PV two V units and
-// each is recycled as soon as its half of the MMA work is done.  TMEM (512
-// columns): O [0, D) and two S buffers of 128 fp32 columns; the softmax
-// overwrites the front of S with P as bf16 pairs, the A operand of PV.
+// each is recycled as soon as its half of the MMA work is done.  At the end
+// of an item, once its PVs are done, the V ring holds its normalised O (bf16,
+// in the output map's swizzled boxes) until the TMA stores have read it.
+// TMEM (512 columns): O [0, D) and two S buffers of 128 fp32 columns; the
+// softmax overwrites the front of S with P as bf16 pairs, the A operand of PV.
 //
 // Sixteen warps; setmaxnreg moves registers from the first two warpgroups
 // (64 each) to the softmax warpgroups (192 each):
-//   warps 0, 2  K producers (warp 0 also loads Q), warps 4-6 V producers:
+//   warps 0, 2  K producers, warps 4-6 V producers:
 //              every lane resolves the cache slot of one page box through the
 //              block table (32 boxes per batch, one batch ahead); a unit's
 //              boxes (one per page and 64-column chunk) are dealt round-robin
 //              over the operand's producer warps, since one warp issues TMA
 //              boxes one after another; pages past the sequence or with a bad
 //              block id are read from outside the tensor, which the TMA fills
-//              with 0.
-//   warp 1     QK issuer and TMEM owner, warp 3 PV issuer: two tcgen05
+//              with 0.  Warp 4 also writes each item's staged O out.
+//   warp 1     QK issuer, Q loads and TMEM owner (the Q copy of an item can
+//              only start once the previous item's last QK is done, when
+//              this thread would wait for it anyway; the K producers never
+//              wait for it), warp 3 PV issuer: two tcgen05
 //              streams, so a ready PV never waits behind a QK issue that the
 //              tensor pipe holds up; QK runs two tiles ahead of PV along the
 //              CTA's flat tile stream (QK_t waits until PV_{t-2} is issued).
-//   warp 7     no role (its registers go to the softmax).
+//   warp 7     scheduler: decodes the items (dependent global loads) ahead
+//              of the other roles and publishes their records.
 //   warps 8-15 softmax, two warpgroups: thread i of each owns row i (TMEM lane
 //              i) and one half of the tile's columns; half-row maxima meet in
 //              shared memory once per tile.  Masks only tiles not fully inside
 //              the row's interval, keeps the running max in the log2 domain,
 //              rescales O in TMEM only when the max grows by more than 2^8, and
-//              at the end of an item normalises and stores its half of O.
+//              at the end of an item normalises its half of O into the V ring.
 // Every mbarrier wait is bounded in time; on expiry the CTA sets
 // SWA_ERR_TIMEOUT, drains its own TMA loads and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -72,7 +80,7 @@ struct Cfg {
   static constexpr int VSU = VSU_;      // V ring slots (units)
   // TMA issue from one warp is serial (about one 2 KB page box per 90 cycles),
   // so each K and V unit's boxes are shared between KW and VW producer warps:
-  // K warps 0 (which also loads Q) and 2; V warps 4 .. 4 + VW - 1.
+  // K warps 0 and 2; V warps 4 .. 4 + VW - 1.
   static constexpr int KW = KW_;
   static constexpr int VW = VW_;
   // NSW softmax warpgroups share every row (each owns N / NSW columns of S and
@@ -80,6 +88,7 @@ struct Cfg {
   static constexpr int NSW = NSW_;
   static constexpr int NS = NS_;
   static constexpr int THREADS = 32 * (kFirstSoftmaxWarp + 4 * NSW);
+  static constexpr int REC_READERS = KW + VW + 2 + 4 * NSW;   // warps that read every item record
   static constexpr int LAUNCH_REGS = (65536 / THREADS) & ~7;   // what the launch allocates per thread
   static constexpr int LOW_REGS = 64;                           // producers and MMA issuers
   static constexpr int HIGH_REGS =                             // softmax: all that the others free
@@ -123,29 +132,34 @@ struct Ctrl {
   uint64_t stall;                        // never signalled: the watchdog test's stalled wait
   uint64_t xch[2];                       // exchanges between the softmax warpgroups
   uint64_t rec_full[kRecSlots];          // item record ord published at [ord % kRecSlots]
+  uint64_t rec_empty[kRecSlots];         // ... and read by every consumer warp
   uint64_t ostage_full;                  // the item's O staged in the V ring (or stored directly)
-  uint64_t ostage_free;                  // the staged O was read by its TMA store: the V ring is free
+  uint64_t ostage_free;                  // the staged O has been read: the V ring may be refilled
   ItemRec rec[kRecSlots];
   uint32_t tmem_base;
   int abort;
 };
 
 // V warp 4: an item's O, staged in the V ring by the softmax (bf16, boxes of
-// 64 columns x 128 rows, 128-byte swizzle), to the output.  A tile whose rows
-// all lie inside the sequence goes out as TMA stores issued by lane 0 (which
-// waits until they have read the ring, unless it is the CTA's last); any other
-// tile is copied by the warp, one 512-byte row per instruction, for the rows
-// of the sequence only.  `tok`: the tile's first token, `ntok`: its tokens
-// inside the sequence.
+// 64 columns x 128 rows, 128-byte swizzle), to the output; the V ring is
+// released (`free_bar`) once the staged O has been read, unless this is the
+// CTA's last item.  A tile whose rows all lie inside the sequence goes out as
+// TMA stores issued by lane 0; any other tile is copied by the warp, one
+// 512-byte row per instruction, for the rows of the sequence only.  `tok`:
+// the tile's first token, `ntok`: its tokens inside the sequence.  (Freeing
+// the two V slots one at a time, as each half is read, measured slower.)
 template <class C>
 __device__ inline void store_staged_o(const CUtensorMap *tm_o, int o_tma, const AttnArgs &a, uint32_t v_s, int G,
-                                      int bq, int hk, int tok, int ntok, int lane, bool last) {
+                                      int bq, int hk, int tok, int ntok, int lane, bool last, uint32_t free_bar) {
   static_assert(C::CH * 8 == 32, "one lane per 16-byte piece of a row");
   if (o_tma && ntok == bq) {
     if (lane == 0) {
       for (int c = 0; c < C::CH; ++c) tma_store_3d(tm_o, v_s + c * C::O_CHUNK, c * 64, hk * G, tok);
       bulk_commit();
-      if (!last) bulk_wait_read_all();
+      if (!last) {
+        bulk_wait_read<0>();
+        mbar_arrive(free_bar);
+      }
     }
     return;
   }
@@ -157,6 +171,8 @@ __device__ inline void store_staged_o(const CUtensorMap *tm_o, int o_tma, const 
     const int64_t orow = (int64_t)(tok + (r >> lg)) * a.hq + hk * G + (r & (G - 1));
     *reinterpret_cast<uint4 *>(out + orow * C::D + lane * 8) = v;
   }
+  __syncwarp();
+  if (lane == 0 && !last) mbar_arrive(free_bar);
 }
 
 template <class C>
@@ -205,7 +221,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(smem_u32(&ctl.o_full[i]), 1);
     }
     mbar_init(smem_u32(&ctl.o_item), 1);
-    for (int i = 0; i < kRecSlots; ++i) mbar_init(smem_u32(&ctl.rec_full[i]), 1);
+    for (int i = 0; i < kRecSlots; ++i) {
+      mbar_init(smem_u32(&ctl.rec_full[i]), 1);
+      mbar_init(smem_u32(&ctl.rec_empty[i]), C::REC_READERS);
+    }
     mbar_init(smem_u32(&ctl.ostage_full), 128 * C::NSW);
     mbar_init(smem_u32(&ctl.ostage_free), 1);
     mbar_init(smem_u32(&ctl.drain), 1);
@@ -254,53 +273,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int oob = (int)(a.num_blocks * a.block_size);
     const int lg_bs = 31 - __clz(a.block_size);         // block sizes are powers of two
     int64_t u_base = 0;                                 // units issued by this warp before this item
-    int ord = 0;                                        // valid items so far
+    int ord = 0;                                        // items so far
     bool ok = true;
     // V warps: the previous item's output tile (kv head, first token, tokens inside the sequence)
     int prev_hk = 0, prev_tok = 0, prev_ntok = 0;
-    for (int item = blockIdx.x; ok && item < n_items; item += stride) {
-      Item it;
-      int32_t eb;
-      if (!decode_item(a, item, bq, it, eb)) {
-        if (eb != 0 && warp == 0 && lane == 0) report(a.err, eb);
-        continue;
-      }
-      int tile_lo, n_tiles, nr, rrs, rre;
-      block_keys_rec<C::N>(a, it, lane, tile_lo, n_tiles, nr, rrs, rre);
-      if (warp == 0) {
-        // Q: the previous item's last QK has to be done with the buffer.  The
-        // item's record goes out first: the MMA warps and the softmax read it
-        // instead of decoding the item themselves.  (The slot's previous
-        // record, kRecSlots items back, has been read: this QK stream could
-        // not have got here before the softmax and the PV warp had started a
-        // later item.)
-        if (ord > 0 && lane == 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, wl);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) {
-          write_rec(ctl.rec[ord % kRecSlots], it, tile_lo, n_tiles, nr, rrs, rre, lane);
-          if (lane == 0) {
-            mbar_arrive(smem_u32(&ctl.rec_full[ord % kRecSlots]));
-            mbar_expect_tx(smem_u32(&ctl.q_full), C::Q_BYTES);
-            for (int c = 0; c < C::CH; ++c)
-              tma_load_3d(q_s + c * C::Q_CHUNK, &tm_q, c * 64, it.hk * G, it.qstart + it.qpos_lo,
-                          smem_u32(&ctl.q_full));
-          }
-        }
-      }
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      ++ord;                                            // items whose Q copy was issued
-      if (is_v && ord > 1) {
+    for (;; ++ord) {
+      // the item's record (n_tiles 0: the end of the stream)
+      const int rs = ord % kRecSlots;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.rec_full[rs]), (uint32_t)((ord / kRecSlots) & 1),
+                                             abort_flag, wl));
+      if (!ok) break;
+      const Item it = ctl.rec[rs].it;
+      const int tile_lo = ctl.rec[rs].tile_lo, n_tiles = ctl.rec[rs].n_tiles;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl.rec_empty[rs]));
+      if (n_tiles == 0) break;
+      if (is_v && share == 0 && ord > 0) {
         // The previous item's O is staged in the V ring once its last PV is
-        // done (so are its V units): V warp 4 stores it and frees the ring.
-        const uint32_t par = (uint32_t)((ord - 2) & 1);
-        if (share == 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.ostage_full), par, abort_flag, wl));
-          if (!ok) break;
-          store_staged_o<C>(&tm_o, o_tma, a, v_s, G, bq, prev_hk, prev_tok, prev_ntok, lane, false);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ctl.ostage_free));
-        }
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.ostage_free), par, abort_flag, wl));
+        // done (so are its V units): V warp 4 stores it and frees the slots.
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.ostage_full), (uint32_t)((ord - 1) & 1), abort_flag, wl));
+        if (!ok) break;
+        store_staged_o<C>(&tm_o, o_tma, a, v_s, G, bq, prev_hk, prev_tok, prev_ntok, lane, false,
+                          smem_u32(&ctl.ostage_free));
+      }
+      if (is_v && ord > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.ostage_free), (uint32_t)((ord - 1) & 1), abort_flag, wl));
         if (!ok) break;
       }
       const int total_boxes = (n_tiles * C::N) / R;
@@ -351,6 +348,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (lane < boxes * uch && lane % nsh == share) tma_load_3d(d, map, x, it.hk, slot, full);
       }
       u_base += ul;                                     // units issued (all of them unless aborted)
+      if (!ok) break;
       prev_hk = it.hk;
       prev_tok = it.qstart + it.qpos_lo;
       prev_ntok = min(bq, it.qlen - it.qpos_lo);
@@ -359,7 +357,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       // the last item's O
       if (ok && ord > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.ostage_full), (uint32_t)((ord - 1) & 1), abort_flag, wl));
-        if (ok) store_staged_o<C>(&tm_o, o_tma, a, v_s, G, bq, prev_hk, prev_tok, prev_ntok, lane, true);
+        if (ok)
+          store_staged_o<C>(&tm_o, o_tma, a, v_s, G, bq, prev_hk, prev_tok, prev_ntok, lane, true, 0u);
       }
       if (lane == 0) bulk_wait_all();                   // every store has landed before the CTA exits
     }
@@ -371,16 +370,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (lane == 0) {
       for (int64_t u = max((int64_t)0, u_base - SU); u < u_base; ++u)
         mbar_wait(smem_u32(is_v ? &ctl.v_full[u % SU] : &ctl.k_full[u % SU]), (uint32_t)((u / SU) & 1), nullptr, kWaitLimitNs);
-      if (warp == 0 && ord > 0) mbar_wait(smem_u32(&ctl.q_full), (ord - 1) & 1, nullptr, kWaitLimitNs);
-      // end of stream for the MMA warp: one more q_full phase without data, once
-      // the MMA warp is past the last real one (its last QK released q_empty)
-      if (warp == 0 && ok &&
-          (ord == 0 || mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, wl))) {
-        ctl.rec[ord % kRecSlots].n_tiles = 0;
-        __threadfence_block();
-        mbar_arrive(smem_u32(&ctl.rec_full[ord % kRecSlots]));
-        mbar_arrive(smem_u32(&ctl.q_full));
-      }
     }
   } else if (warp == 1 || warp == 3) {
     // =============================== MMA issuers ================================
@@ -392,13 +381,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (lane == 0 && warp == 1) {
       bool ok = true;
       int ord = 0;
+      int n_q = 0;                                       // Q copies issued
       int t = 0;                                         // tiles of this CTA's stream
       while (ok) {
-        // the next item's Q has landed (or the stream has ended: 0 tiles)
+        // the item's record (n_tiles 0: the end of the stream), then its Q
+        const int rs = ord % kRecSlots;
+        ok = mbar_wait(smem_u32(&ctl.rec_full[rs]), (uint32_t)((ord / kRecSlots) & 1), abort_flag, wl);
+        if (!ok) break;
+        const int n = ctl.rec[rs].n_tiles;
+        const int q_hk = ctl.rec[rs].it.hk, q_tok = ctl.rec[rs].it.qstart + ctl.rec[rs].it.qpos_lo;
+        mbar_arrive(smem_u32(&ctl.rec_empty[rs]));
+        if (n == 0) break;
+        // Q: once the previous item's last QK is done with the buffer (this
+        // thread would wait for the copy before its next MMA anyway)
+        if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (uint32_t)((ord - 1) & 1), abort_flag, wl);
+        if (!ok) break;
+        mbar_expect_tx(smem_u32(&ctl.q_full), C::Q_BYTES);
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_3d(q_s + c * C::Q_CHUNK, &tm_q, c * 64, q_hk * G, q_tok, smem_u32(&ctl.q_full));
+        ++n_q;
         ok = mbar_wait(smem_u32(&ctl.q_full), (uint32_t)(ord & 1), abort_flag, wl);
         if (!ok) break;
-        const int n = ctl.rec[ord % kRecSlots].n_tiles;
-        if (n == 0) break;
         tc_fence_after();
         for (int j = 0; ok && j < n; ++j, ++t) {
           const int sb = (int)(t % C::NS);               // S buffer of tile t
@@ -435,9 +438,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         *abort_flag = 1;
         report(a.err, SWA_ERR_TIMEOUT);
       }
-      // every MMA issued by this thread must finish before TMEM is released
+      // every MMA issued by this thread must finish before TMEM is released,
+      // and every Q copy must have landed
       mma_commit(smem_u32(&ctl.drain));
       mbar_wait(smem_u32(&ctl.drain), 0, nullptr, kWaitLimitNs);
+      if (n_q > 0) mbar_wait(smem_u32(&ctl.q_full), (uint32_t)((n_q - 1) & 1), nullptr, kWaitLimitNs);
     } else if (lane == 0 && warp == 3) {
       bool ok = true;
       // watchdog test: a wait that can only run out (a.stall, set by swa_set_watchdog)
@@ -448,6 +453,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         ok = mbar_wait(smem_u32(&ctl.rec_full[ord % kRecSlots]), (uint32_t)((ord / kRecSlots) & 1), abort_flag, wl);
         if (!ok) break;
         const int n_tiles = ctl.rec[ord % kRecSlots].n_tiles;
+        mbar_arrive(smem_u32(&ctl.rec_empty[ord % kRecSlots]));
         if (n_tiles == 0) break;
         for (int j = 0; ok && j < n_tiles; ++j, ++t) {
           const int sb = (int)(t % C::NS);
@@ -480,8 +486,41 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mma_commit(smem_u32(&ctl.drain2));
       mbar_wait(smem_u32(&ctl.drain2), 0, nullptr, kWaitLimitNs);
     }
+  } else if (warp == 7) {
+    // =============================== scheduler ==================================
+    // Decodes the CTA's items (a chain of dependent global loads) ahead of
+    // every other role and publishes them as records, up to kRecSlots ahead
+    // of the slowest reader.
+    bool ok = true;
+    int ord = 0;
+    auto publish = [&](const Item &it, int tile_lo, int n_tiles, int nr, int rrs, int rre) -> bool {
+      const int rs = ord % kRecSlots;
+      if (ord >= kRecSlots &&
+          !__all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(&ctl.rec_empty[rs]), (uint32_t)(((ord / kRecSlots) - 1) & 1),
+                                             abort_flag, wl)))
+        return false;
+      write_rec(ctl.rec[rs], it, tile_lo, n_tiles, nr, rrs, rre, lane);
+      if (lane == 0) mbar_arrive(smem_u32(&ctl.rec_full[rs]));
+      ++ord;
+      return true;
+    };
+    for (int item = blockIdx.x; ok && item < n_items; item += stride) {
+      Item it;
+      int32_t eb;
+      if (!decode_item(a, item, bq, it, eb)) {
+        if (eb != 0 && lane == 0) report(a.err, eb);
+        continue;
+      }
+      int tile_lo, n_tiles, nr, rrs, rre;
+      block_keys_rec<C::N>(a, it, lane, tile_lo, n_tiles, nr, rrs, rre);
+      ok = publish(it, tile_lo, n_tiles, nr, rrs, rre);
+    }
+    if (ok) ok = publish(Item{}, 0, 0, 0, 0, -1);         // the end of the stream
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      report(a.err, SWA_ERR_TIMEOUT);
+    }
   }
-  // warp 7 has no role: it only gives its registers to the softmax
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::HIGH_REGS));
     // =============================== softmax ====================================
@@ -492,7 +531,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     constexpr int NSW = C::NSW;
     constexpr int NH = C::N / NSW;                       // S columns of one warpgroup
     constexpr int DH = C::D / NSW;                       // O columns of one warpgroup
-    constexpr int EPW = DH < 64 ? DH : 64;               // O columns per epilogue pass
     const int h = (warp - kFirstSoftmaxWarp) >> 2;
     const int sid = threadIdx.x - 32 * kFirstSoftmaxWarp;   // 0 .. 128 * NSW - 1
     const int row = 32 * (warp & 3) + lane;              // TMEM lane of this thread
@@ -514,6 +552,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         return false;
       have = ctl.rec[slot].n_tiles > 0;
       if (have) row_setup_rec(a, ctl.rec[slot], row, G, lane, cur);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl.rec_empty[slot]));
       return true;
     };
     bool ok = next_rec();
@@ -691,21 +731,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-      for (int c = 0; c < DH / 32; ++c) {                  // 32 columns: half of a staged 64-column chunk
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_t + C::TM_O + h * DH + 32 * c, r);
+      for (int c = 0; c < DH / 64; ++c) {                  // one staged 64-column chunk per pass
+        uint32_t r[64];
+        tmem_ld32(tmem + lane_t + C::TM_O + h * DH + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(r));
+        tmem_ld32(tmem + lane_t + C::TM_O + h * DH + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
         tmem_wait_ld();
-        const int col = h * DH + 32 * c;
-        const uint32_t rb = v_s + (uint32_t)((col >> 6) * C::O_CHUNK + row * 128);
+        const uint32_t rb = v_s + (uint32_t)((h * (DH / 64) + c) * C::O_CHUNK + row * 128);
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int j = ((col & 63) >> 3) + jj;            // 16-byte piece of the 128-byte row
+        for (int j = 0; j < 8; ++j)                        // 16-byte piece j of the 128-byte row
           st_shared_v4(rb + ((uint32_t)(j ^ (row & 7)) << 4),
-                       pack_bf16(__uint_as_float(r[8 * jj]) * inv, __uint_as_float(r[8 * jj + 1]) * inv),
-                       pack_bf16(__uint_as_float(r[8 * jj + 2]) * inv, __uint_as_float(r[8 * jj + 3]) * inv),
-                       pack_bf16(__uint_as_float(r[8 * jj + 4]) * inv, __uint_as_float(r[8 * jj + 5]) * inv),
-                       pack_bf16(__uint_as_float(r[8 * jj + 6]) * inv, __uint_as_float(r[8 * jj + 7]) * inv));
-        }
+                       pack_bf16(__uint_as_float(r[8 * j]) * inv, __uint_as_float(r[8 * j + 1]) * inv),
+                       pack_bf16(__uint_as_float(r[8 * j + 2]) * inv, __uint_as_float(r[8 * j + 3]) * inv),
+                       pack_bf16(__uint_as_float(r[8 * j + 4]) * inv, __uint_as_float(r[8 * j + 5]) * inv),
+                       pack_bf16(__uint_as_float(r[8 * j + 6]) * inv, __uint_as_float(r[8 * j + 7]) * inv));
       }
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&ctl.ostage_full));

@@ -75,6 +75,19 @@ __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, co
   return mbar_wait(bar, parity, abort, limit_ns);
 }
 
+// For a role that runs well ahead and need not react quickly (the item
+// scheduler): poll with a back-off sleep, so its wait takes no issue slots
+// from the warps that share its SM sub-partition.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const volatile int *abort,
+                                                uint64_t limit_ns) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_test_wait(bar, parity)) {
+    if ((abort != nullptr && *abort) || global_ns() - t0 > limit_ns) return false;
+    __nanosleep(1000);
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ inline void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
                                    uint32_t bar) {
@@ -208,7 +221,8 @@ __device__ inline void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0
                : "memory");
 }
 __device__ inline void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ inline void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+template <int N>
+__device__ inline void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 __device__ inline void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ inline void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
