@@ -24,12 +24,15 @@
 //
 // Sixteen warps; setmaxnreg moves registers from warps 0-7 (64 each) to the
 // softmax warpgroups (192 each):
-//   warp 0      K producer and Q loads; warps 4-6 V producers (a unit's page
-//               boxes are dealt over them, one TMA box per page and chunk)
-//   warp 1      QK issuer and TMEM owner: QK_A(t), QK_B(t) per key tile, each
-//               after the previous scores were loaded from S
+//   warp 0      K producer; warps 4-6 V producers (a unit's page boxes are
+//               dealt over them, one TMA box per page and chunk)
+//   warp 1      QK issuer, Q loads and TMEM owner: QK_A(t), QK_B(t) per key
+//               tile, each after the previous scores were loaded from S; an
+//               item's Q copy once the previous item's last QK is done
 //   warp 3      PV issuer: PV_A(t) once P_A(t) is published, then PV_B(t)
-//   warps 2, 7  no role
+//   warp 7      scheduler: decodes the items ahead of the other roles and
+//               publishes them as records (as in attention_tc.cu)
+//   warp 2      no role
 //   warps 8-11  softmax of tile A, warps 12-15 softmax of tile B: thread i of
 //               a warpgroup owns row i (TMEM lane i) of its tile.
 // The code is kept small on purpose (32-bit counters, shifts for the
@@ -57,6 +60,7 @@ struct PairCfg {
   static constexpr int LAUNCH_REGS = 128;
   static constexpr int LOW_REGS = 64;
   static constexpr int HIGH_REGS = 192;
+  static constexpr int REC_READERS = 1 + VW + 2 + 8;   // warps that read every item record
   static constexpr int Q_CHUNK = M * 128;            // bytes of one 64-column chunk of a Q tile
   static constexpr int Q_BYTES = M * D * 2;
   static constexpr int UNIT = 16384;                 // bytes of a K or V unit
@@ -89,7 +93,9 @@ struct PairCtrl {
   uint64_t o_full[2], o_item[2];         // PV_X(t) complete; the item's last PV_X complete
   uint64_t drain, drain2;
   uint64_t stall;                        // never signalled: the watchdog test's stalled wait
-  int32_t sched_n[4];                    // tile count of item ord at [ord & 3] (0: end of stream)
+  uint64_t rec_full[kRecSlots];          // item record ord published at [ord % kRecSlots]
+  uint64_t rec_empty[kRecSlots];         // ... and read by every consumer warp
+  ItemRec rec[kRecSlots];
   uint32_t tmem_base;
   int abort;
 };
@@ -146,6 +152,10 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       mbar_init(smem_u32(&ctl.o_item[x]), 1);
     }
     mbar_init(smem_u32(&ctl.s_free), 128);
+    for (int i = 0; i < kRecSlots; ++i) {
+      mbar_init(smem_u32(&ctl.rec_full[i]), 1);
+      mbar_init(smem_u32(&ctl.rec_empty[i]), C::REC_READERS);
+    }
     mbar_init(smem_u32(&ctl.drain), 1);
     mbar_init(smem_u32(&ctl.stall), 1);                 // nothing ever arrives here
     mbar_init(smem_u32(&ctl.drain2), 1);
@@ -187,33 +197,18 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int oob = (int)(a.num_blocks * a.block_size);
     const int lg_bs = 31 - __clz(a.block_size);
     int u_base = 0;                                     // units issued by this warp before this item
-    int ord = 0;                                        // valid items so far
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < n_items; item += stride) {
-      Item it;
-      int32_t eb;
-      if (!decode_item(a, item, bq2, it, eb)) {
-        if (eb != 0 && warp == 0 && lane == 0) report(a.err, eb);
-        continue;
-      }
-      int kmin, kmax;
-      block_keys(a, it, lane, 32, true, kmin, kmax);
-      const int tile_lo = kmin / C::N;
-      const int n_tiles = kmax / C::N - tile_lo + 1;
-      if (warp == 0 && lane == 0) {
-        // Q_A and Q_B: the previous item's last QK_B has to be done with them
-        if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, wl);
-        if (ok) {
-          ctl.sched_n[ord & 3] = n_tiles;
-          mbar_expect_tx(smem_u32(&ctl.q_full), 2 * C::Q_BYTES);
-          for (int x = 0; x < 2; ++x)
-            for (int c = 0; c < C::CH; ++c)
-              tma_load_3d(q_s + x * C::Q_BYTES + c * C::Q_CHUNK, &tm_q, c * 64, it.hk * G,
-                          it.qstart + it.qpos_lo + x * bq, smem_u32(&ctl.q_full));
-        }
-      }
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      ++ord;
+    for (int ord = 0;; ++ord) {
+      // the item's record (n_tiles 0: the end of the stream)
+      const int rs = ord % kRecSlots;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.rec_full[rs]), (uint32_t)((ord / kRecSlots) & 1),
+                                             abort_flag, wl));
+      if (!ok) break;
+      const Item it = ctl.rec[rs].it;
+      const int tile_lo = ctl.rec[rs].tile_lo, n_tiles = ctl.rec[rs].n_tiles;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl.rec_empty[rs]));
+      if (n_tiles == 0) break;
       const int total_boxes = (n_tiles * C::N) / R;
       const int32_t *bt = a.block_table + (int64_t)it.s * a.bt_stride;
       auto resolve = [&](int b) -> int {                // slot of the first key of box b
@@ -262,6 +257,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (lane < boxes * uch && lane % nsh == share) tma_load_3d(d, map, x, it.hk, slot, full);
       }
       u_base += ul;
+      if (!ok) break;
     }
     if (!ok && lane == 0) {
       *abort_flag = 1;
@@ -271,13 +267,6 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (lane == 0) {
       for (int u = max(0, u_base - SU); u < u_base; ++u)
         mbar_wait(smem_u32(is_v ? &ctl.v_full[u % SU] : &ctl.k_full[u % SU]), (uint32_t)((u / SU) & 1), nullptr, kWaitLimitNs);
-      if (warp == 0 && ord > 0) mbar_wait(smem_u32(&ctl.q_full), (ord - 1) & 1, nullptr, kWaitLimitNs);
-      // end of stream for the QK issuer: one more q_full phase without data
-      if (warp == 0 && ok &&
-          (ord == 0 || mbar_wait(smem_u32(&ctl.q_empty), (ord - 1) & 1, abort_flag, wl))) {
-        ctl.sched_n[ord & 3] = 0;
-        mbar_arrive(smem_u32(&ctl.q_full));
-      }
     }
   } else if (warp == 1 || warp == 3) {
     // =============================== MMA issuers ================================
@@ -287,13 +276,30 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (lane == 0 && warp == 1) {
       bool ok = true;
       int ord = 0;
+      int n_q = 0;                                      // Q copies issued
       int n_qk = 0;                                     // QKs issued (both tiles)
       RingPos kp;
       while (ok) {
+        // the item's record (n_tiles 0: the end of the stream), then Q_A and
+        // Q_B, once the previous item's last QK_B is done with them (this
+        // thread would wait for the copy before its next MMA anyway)
+        const int rs = ord % kRecSlots;
+        ok = mbar_wait(smem_u32(&ctl.rec_full[rs]), (uint32_t)((ord / kRecSlots) & 1), abort_flag, wl);
+        if (!ok) break;
+        const int n = ctl.rec[rs].n_tiles;
+        const int q_hk = ctl.rec[rs].it.hk, q_tok = ctl.rec[rs].it.qstart + ctl.rec[rs].it.qpos_lo;
+        mbar_arrive(smem_u32(&ctl.rec_empty[rs]));
+        if (n == 0) break;
+        if (ord > 0) ok = mbar_wait(smem_u32(&ctl.q_empty), (uint32_t)((ord - 1) & 1), abort_flag, wl);
+        if (!ok) break;
+        mbar_expect_tx(smem_u32(&ctl.q_full), 2 * C::Q_BYTES);
+        for (int x = 0; x < 2; ++x)
+          for (int c = 0; c < C::CH; ++c)
+            tma_load_3d(q_s + x * C::Q_BYTES + c * C::Q_CHUNK, &tm_q, c * 64, q_hk * G, q_tok + x * bq,
+                        smem_u32(&ctl.q_full));
+        ++n_q;
         ok = mbar_wait(smem_u32(&ctl.q_full), (uint32_t)(ord & 1), abort_flag, wl);
         if (!ok) break;
-        const int n = ctl.sched_n[ord & 3];
-        if (n == 0) break;
         tc_fence_after();
         for (int j = 0; ok && j < n; ++j) {
           const RingPos k0 = kp;                        // the tile's two K units
@@ -334,22 +340,25 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         *abort_flag = 1;
         report(a.err, SWA_ERR_TIMEOUT);
       }
-      // every MMA issued by this thread must finish before TMEM is released
+      // every MMA issued by this thread must finish before TMEM is released,
+      // and every Q copy must have landed
       mma_commit(smem_u32(&ctl.drain));
       mbar_wait(smem_u32(&ctl.drain), 0, nullptr, kWaitLimitNs);
+      if (n_q > 0) mbar_wait(smem_u32(&ctl.q_full), (uint32_t)((n_q - 1) & 1), nullptr, kWaitLimitNs);
     } else if (lane == 0 && warp == 3) {
       bool ok = true;
       // watchdog test: a wait that can only run out (a.stall, set by swa_set_watchdog)
       if (a.stall) ok = mbar_wait(smem_u32(&ctl.stall), 0, abort_flag, wl);
       uint32_t tpar = 0;                                // parity of this CTA's tile count
       RingPos vp;
-      for (int item = blockIdx.x; ok && item < n_items; item += stride) {
-        Item it;
-        int32_t eb;
-        if (!decode_item(a, item, bq2, it, eb)) continue;
-        int kmin, kmax;
-        block_keys(a, it, 0, 1, false, kmin, kmax);
-        const int n_tiles = kmax / C::N - kmin / C::N + 1;
+      for (int ord = 0; ok; ++ord) {
+        // the item's record (n_tiles 0: the end of the stream)
+        const int rs = ord % kRecSlots;
+        ok = mbar_wait(smem_u32(&ctl.rec_full[rs]), (uint32_t)((ord / kRecSlots) & 1), abort_flag, wl);
+        if (!ok) break;
+        const int n_tiles = ctl.rec[rs].n_tiles;
+        mbar_arrive(smem_u32(&ctl.rec_empty[rs]));
+        if (n_tiles == 0) break;
         for (int j = 0; ok && j < n_tiles; ++j, tpar ^= 1u) {
           const RingPos v0 = vp;
           RingPos v1 = vp;
@@ -389,8 +398,42 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       mma_commit(smem_u32(&ctl.drain2));
       mbar_wait(smem_u32(&ctl.drain2), 0, nullptr, kWaitLimitNs);
     }
+  } else if (warp == 7) {
+    // =============================== scheduler ==================================
+    // Decodes the CTA's items (a chain of dependent global loads) ahead of
+    // every other role and publishes them as records, up to kRecSlots ahead
+    // of the slowest reader.
+    bool ok = true;
+    int ord = 0;
+    auto publish = [&](const Item &it, int tile_lo, int n_tiles, int nr, int rrs, int rre) -> bool {
+      const int rs = ord % kRecSlots;
+      if (ord >= kRecSlots &&
+          !__all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(&ctl.rec_empty[rs]),
+                                                   (uint32_t)(((ord / kRecSlots) - 1) & 1), abort_flag, wl)))
+        return false;
+      write_rec(ctl.rec[rs], it, tile_lo, n_tiles, nr, rrs, rre, lane);
+      if (lane == 0) mbar_arrive(smem_u32(&ctl.rec_full[rs]));
+      ++ord;
+      return true;
+    };
+    for (int item = blockIdx.x; ok && item < n_items; item += stride) {
+      Item it;
+      int32_t eb;
+      if (!decode_item(a, item, bq2, it, eb)) {
+        if (eb != 0 && lane == 0) report(a.err, eb);
+        continue;
+      }
+      int tile_lo, n_tiles, nr, rrs, rre;
+      block_keys_rec<C::N>(a, it, lane, tile_lo, n_tiles, nr, rrs, rre);
+      ok = publish(it, tile_lo, n_tiles, nr, rrs, rre);
+    }
+    if (ok) ok = publish(Item{}, 0, 0, 0, 0, -1);         // the end of the stream
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      report(a.err, SWA_ERR_TIMEOUT);
+    }
   }
-  // warps 2 and 7 have no role: they only give their registers to the softmax
+  // warp 2 has no role: it only gives its registers to the softmax
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::HIGH_REGS));
     // =============================== softmax ====================================
@@ -409,18 +452,22 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const float asl2 = fmaxf(fabsf(a.scale * kLog2e), 1.17549435e-38f);
     int t = 0;                                           // this CTA's tiles so far
     int n_done = 0;                                      // items finished
-    bool ok = true;
-    int item = blockIdx.x - stride;
+    // Items come from the scheduler's records; the next one is set up while
+    // the current item's last PV runs.
     RowSetup cur;
-    bool have;
-    {
-      Item it;
-      have = next_item(a, item, stride, n_items, bq2, it);
-      if (have) {
-        it.qpos_lo += x * bq;                            // this warpgroup's tile of the pair
-        row_setup<N>(a, it, row, G, lane, cur);
-      }
-    }
+    bool have = false;
+    auto next_rec = [&]() -> bool {                      // false: the wait ran out
+      const int slot = n_done % kRecSlots;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.rec_full[slot]),
+                                             (uint32_t)((n_done / kRecSlots) & 1), abort_flag, wl)))
+        return false;
+      have = ctl.rec[slot].n_tiles > 0;
+      if (have) row_setup_rec(a, ctl.rec[slot], row, G, lane, cur, x * bq);   // this warpgroup's tile of the pair
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl.rec_empty[slot]));
+      return true;
+    };
+    bool ok = next_rec();
     while (ok && have) {
       const Item &it = cur.it;
       const int tile_lo = cur.tile_lo, n_tiles = cur.n_tiles;
@@ -560,17 +607,10 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       if (!ok) break;
       const bool row_valid = cur.row_valid;
       const int64_t out_row = cur.out_row;
-      {
-        Item nit;
-        have = next_item(a, item, stride, n_items, bq2, nit);
-        if (have) {
-          nit.qpos_lo += x * bq;
-          row_setup<N>(a, nit, row, G, lane, cur);
-        }
-      }
-      // the item's last PV_x (one o_item phase per item)
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item[x]), (uint32_t)(n_done & 1), abort_flag, wl));
       ++n_done;
+      if (!next_rec()) { ok = false; break; }
+      // the item's last PV_x (one o_item phase per item)
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item[x]), (uint32_t)((n_done - 1) & 1), abort_flag, wl));
       if (!ok) break;
       // epilogue: O / l -> bf16, 64 columns per pass, 32-byte stores.  The
       // next item's first PV_x overwrites O_x only after this thread's P for
@@ -644,7 +684,11 @@ cudaError_t run_pair(const AttnArgs &a, cudaStream_t st) {
 
 }  // namespace
 
-bool tc_pair_supported(const AttnArgs &a) { return a.head_dim == 128 && tc_prefill_ok(a); }
+// The epilogue's 32-byte stores want a 32-byte aligned output (the library
+// only asks for 16); other outputs take the CUDA-core path.
+bool tc_pair_supported(const AttnArgs &a) {
+  return a.head_dim == 128 && (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 && tc_prefill_ok(a);
+}
 
 cudaError_t launch_attention_tc_pair(const AttnArgs &a, cudaStream_t st) {
   // the sign of the scale is a template argument, as in attention_tc.cu

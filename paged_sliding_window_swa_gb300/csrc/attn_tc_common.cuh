@@ -248,10 +248,13 @@ __device__ inline void write_rec(ItemRec &r, const Item &it, int tile_lo, int n_
 
 // A softmax thread's RowSetup from a record: its row's interval from the
 // record's ranges, or, for a record that could not hold them all, from a scan
-// of the sequence's ranges by the warp (same rule as row_setup).
+// of the sequence's ranges by the warp (same rule as row_setup).  `qoff`: the
+// position of the thread's query tile within the item (0, or bq for the
+// second tile of a pair).
 __device__ inline void row_setup_rec(const AttnArgs &a, const ItemRec &r, int row, int G, int lane,
-                                     RowSetup &rs) {
+                                     RowSetup &rs, int qoff = 0) {
   rs.it = r.it;
+  rs.it.qpos_lo += qoff;
   rs.tile_lo = r.tile_lo;
   rs.n_tiles = r.n_tiles;
   const Item &it = rs.it;

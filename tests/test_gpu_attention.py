@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import paged_sliding_window_swa_gb300 as swa
 import workloads as W
 from _gpu_helpers import (LSE_ATOL, atol_for, gpu_inputs, max_errors, oracle_rows, run_attention,
                           sample_rows)
@@ -113,6 +114,30 @@ def test_many_image_ranges_per_tile_all_rows(D, G, window, causal, err):
                    block_size=32, window=window, causal=causal, dtype="bf16",
                    max_num_tokens=int(qlen.sum()) + 9)
     _check(lay, _all_rows(lay), err=err)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_output_aligned_to_16_bytes_only(D, err):
+    """The library asks for 16-byte aligned outputs; one that is not 32-byte aligned
+    must give the same rows as the oracle (the head_dim-128 tensor-core kernel's
+    32-byte stores are not used for it)."""
+    lay = W.random_small(300 + D, head_dim=D, block_size=32, group=2, max_seqs=3, max_ctx=400, max_q=300,
+                         window=200, with_ranges=True)
+    q, k, v, d = gpu_inputs(lay, data_seed=3)
+    big = torch.empty(q.numel() + 8, dtype=q.dtype, device=q.device)
+    out = big[8:].view(q.shape)
+    assert out.data_ptr() % 32 == 16
+    o, lse = swa.swa_mm_paged_attention(
+        q, k, v, d["block_table"], d["query_start_loc"], d["seq_lens"], context_lens=d["context_lens"],
+        mm_ranges=d["mm_ranges"], max_query_len=lay.max_query_len, window=lay.window, causal=lay.causal,
+        scale=lay.scale, out=out, err=err)
+    assert o.data_ptr() == out.data_ptr()
+    rows = _all_rows(lay)
+    ro, rl = oracle_rows(lay, q, k, v, rows)
+    e_out, e_lse = max_errors(out, lse, ro, rl, rows)
+    assert e_out <= atol_for(lay) and e_lse <= LSE_ATOL, (e_out, e_lse)
+    torch.cuda.synchronize()
+    assert err.item() == 0
 
 
 def test_unused_cache_rows_never_reach_the_output(err):
