@@ -113,6 +113,9 @@ attn_decode_kernel(AttnArgs a) {
     if (split >= parts) live = false;
     else part = split_span(seq_len, parts, split);
   }
+  // a dependent kernel (the LSE merge of the partials) may be launched now; it
+  // waits for this grid to complete before it reads anything
+  pdl_launch_dependents();
   // rows' visible intervals inside the partition (rows >= `rows` see nothing)
   if (threadIdx.x < kMaxRows) {
     int lo = 1, hi = 0;

@@ -25,6 +25,14 @@ __device__ inline uint64_t global_ns() {
   return t;
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while the kernel before it in the
+// stream is still running; pdl_wait() blocks until that kernel has completed
+// and its writes are visible (a no-op without the attribute).  The earlier
+// kernel lets it start early with pdl_launch_dependents().
+__device__ inline void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ inline void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 template <typename T> struct Elem;
 template <> struct Elem<float> {
   static __device__ inline float to_f(float x) { return x; }

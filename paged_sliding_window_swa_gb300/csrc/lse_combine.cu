@@ -66,6 +66,7 @@ lse_combine_kernel(const T *__restrict__ po, const float *__restrict__ pl, int32
                    int64_t rows, T *__restrict__ out, float *__restrict__ out_lse) {
   using Sh = CombineShape<T, D>;
   constexpr int E = Sh::kVecElems;
+  pdl_wait();                                                // the partials' producer is done
   const int lane = threadIdx.x & 31;
   const int sub = lane / Sh::kLpr;              // row within the warp
   const int gl = lane % Sh::kLpr;               // lane within the row group
@@ -142,6 +143,7 @@ lse_combine_rowwarp_kernel(const T *__restrict__ po, const float *__restrict__ p
                            int64_t rows, T *__restrict__ out, float *__restrict__ out_lse) {
   using Sh = RowWarpShape<T, D>;
   constexpr int E = Sh::kVecElems;
+  pdl_wait();                                                // the partials' producer is done
   const int lane = threadIdx.x & 31;
   const int64_t row = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   if (row >= rows) return;                                   // warp-uniform
@@ -194,22 +196,35 @@ lse_combine_rowwarp_kernel(const T *__restrict__ po, const float *__restrict__ p
 // Below this many rows the warp-per-row kernel is used.
 constexpr int64_t kRowWarpMaxRows = 32768;
 
+// Launched as a programmatic dependent of the kernel before it in the stream
+// (normally the split-KV attention, which lets it start during its tail): the
+// kernels wait for it with pdl_wait() before they read the partials.
+template <typename K, typename... Args>
+cudaError_t launch_dependent(K kernel, int64_t grid, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <typename T, int D>
 cudaError_t run(const void *po, const float *pl, int32_t P, int64_t rows, void *out, float *ol,
                 cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
-  if (rows < kRowWarpMaxRows) {
-    const int64_t grid = ceil_div(rows, kThreads / 32);
-    lse_combine_rowwarp_kernel<T, D><<<(unsigned)grid, kThreads, 0, st>>>(
-        static_cast<const T *>(po), pl, P, rows, static_cast<T *>(out), ol);
-    return cudaGetLastError();
-  }
+  const T *p = static_cast<const T *>(po);
+  T *o = static_cast<T *>(out);
+  if (rows < kRowWarpMaxRows)
+    return launch_dependent(lse_combine_rowwarp_kernel<T, D>, ceil_div(rows, kThreads / 32), st, p, pl, P, rows, o, ol);
   using Sh = CombineShape<T, D>;
   const int64_t rows_per_block = (kThreads / 32) * Sh::kRowsPerWarp;
-  const int64_t grid = ceil_div(rows, rows_per_block);
-  lse_combine_kernel<T, D><<<(unsigned)grid, kThreads, 0, st>>>(
-      static_cast<const T *>(po), pl, P, rows, static_cast<T *>(out), ol);
-  return cudaGetLastError();
+  return launch_dependent(lse_combine_kernel<T, D>, ceil_div(rows, rows_per_block), st, p, pl, P, rows, o, ol);
 }
 
 }  // namespace
