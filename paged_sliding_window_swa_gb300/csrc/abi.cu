@@ -83,6 +83,7 @@ cudaError_t dispatch_attention(const AttnArgs &a, cudaStream_t st) {
   if (tc_pair_supported(a)) return launch_attention_tc_pair(a, st);
   if (tc_supported(a)) return launch_attention_tc(a, st);
   if (decode_supported(a)) return launch_attention_decode(a, st);
+  if (tc_small_supported(a)) return launch_attention_tc_small(a, st);
   return launch_attention_simt(a, st);
 }
 

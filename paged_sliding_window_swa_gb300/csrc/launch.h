@@ -78,7 +78,8 @@ cudaError_t launch_lse_combine(const void *po, const float *pl, int32_t num_spli
                                int64_t num_tokens, int32_t num_heads, int32_t head_dim,
                                int32_t dtype, void *out, float *out_lse, cudaStream_t st);
 
-// General CUDA-core attention: any supported dtype / head_dim, split or not.
+// General CUDA-core attention: any supported dtype / head_dim, split or not
+// (what no tensor-core kernel takes: a GQA group that does not divide 128).
 cudaError_t launch_attention_simt(const AttnArgs &a, cudaStream_t st);
 
 // Split-KV decode: bf16, few query tokens per sequence, K/V staged with cp.async.
@@ -92,5 +93,10 @@ cudaError_t launch_attention_tc(const AttnArgs &a, cudaStream_t st);
 // The same for head_dim 128 with two query tiles per work item.
 bool tc_pair_supported(const AttnArgs &a);
 cudaError_t launch_attention_tc_pair(const AttnArgs &a, cudaStream_t st);
+
+// tcgen05 / TMEM attention for everything else: bf16 or fp32 (fp32 as bf16
+// hi + lo operand pairs), any head_dim, split or not.
+bool tc_small_supported(const AttnArgs &a);
+cudaError_t launch_attention_tc_small(const AttnArgs &a, cudaStream_t st);
 
 }  // namespace swa

@@ -140,6 +140,15 @@ def test_output_aligned_to_16_bytes_only(D, err):
     assert err.item() == 0
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_group_of_three_all_rows(dtype, err):
+    """A GQA group that does not divide the 128-row tile (the CUDA-core kernel's case)."""
+    lay = W.random_small(77, head_dim=128, block_size=16, group=3, dtype=dtype, max_seqs=3, max_ctx=300,
+                         max_q=200, window=100, with_ranges=True)
+    assert lay.num_heads_q == 3 * lay.num_heads_kv
+    _check(lay, _all_rows(lay), err=err)
+
+
 def test_unused_cache_rows_never_reach_the_output(err):
     """Spare blocks and page tails hold NaN; the output must stay finite and exact."""
     for seed in range(4):
