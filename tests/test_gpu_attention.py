@@ -149,6 +149,34 @@ def test_group_of_three_all_rows(dtype, err):
     _check(lay, _all_rows(lay), err=err)
 
 
+@pytest.mark.parametrize("dtype,D,G,P,max_q", [
+    ("fp32", 256, 2, 1, 200),    # 32-key tiles (fp32 operand pairs at head_dim 256)
+    ("fp32", 128, 4, 3, 150),    # fp32 split partials, then the merge
+    ("bf16", 64, 32, 1, 120),    # a GQA group only the general tensor-core kernel takes
+    ("bf16", 128, 1, 4, 300),    # split-KV prefill with more rows than the decode kernel takes
+    ("bf16", 256, 8, 2, 260)])
+def test_general_tensor_core_kernel_shapes(dtype, D, G, P, max_q, err):
+    """Shapes that run on the general tcgen05 kernel, every row against the oracle
+    (split cases through lse_combine)."""
+    from paged_sliding_window_swa_gb300 import lse_combine
+    lay = W.random_small(400 + D + G + P, head_dim=D, group=G, dtype=dtype, max_seqs=3, max_ctx=600,
+                         max_q=max_q, window=int(np.random.default_rng(D * G).choice([0, 64, 300])),
+                         with_ranges=True, num_splits=P)
+    q, k, v, d = gpu_inputs(lay, data_seed=5)
+    rows = _all_rows(lay)
+    if P == 1:
+        out, lse = run_attention(lay, q, k, v, d, err=err)
+    else:
+        po, pl = run_attention(lay, q, k, v, d, err=err)
+        out, lse = lse_combine(po, pl)
+    ro, rl = oracle_rows(lay, q, k, v, rows)
+    e_out, e_lse = max_errors(out, lse, ro, rl, rows)
+    assert e_out <= atol_for(lay), e_out
+    assert e_lse <= LSE_ATOL, e_lse
+    torch.cuda.synchronize()
+    assert err.item() == 0
+
+
 def test_unused_cache_rows_never_reach_the_output(err):
     """Spare blocks and page tails hold NaN; the output must stay finite and exact."""
     for seed in range(4):
