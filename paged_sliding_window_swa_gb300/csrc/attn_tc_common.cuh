@@ -1,8 +1,9 @@
-// Pieces shared by the tensor-core attention kernels (attention_tc.cu and
-// attention_tc_pair.cu): the work items (a query block, or a pair of
-// consecutive query blocks, of one sequence and one kv head), the union of
-// their rows' visible intervals, the per-row interval a softmax thread needs,
-// and the host-side TMA descriptor helpers.
+// Pieces shared by the tensor-core attention kernels (attention_tc.cu,
+// attention_tc_pair.cu, attention_tc_small.cu): the work items (a query block,
+// or a pair of consecutive query blocks, of one sequence and one kv head), the
+// union of their rows' visible intervals, the item records the scheduler warps
+// publish, the per-row interval a softmax thread needs, and the host-side TMA
+// descriptor helpers.
 #pragma once
 
 #include <climits>
@@ -66,38 +67,6 @@ __device__ inline void union_keys(const AttnArgs &a, const Item &it, int emax, i
   kmax = min(max(base_hi(it.q_hi, a.window, it.causal, it.seq_len), emax), it.seq_len - 1);
 }
 
-// Ranges scanned by lanes `start`, `start + step`, ...; `warp_reduce`
-// combines the lanes.
-__device__ inline void block_keys(const AttnArgs &a, const Item &it, int start, int step, bool warp_reduce,
-                                  int &kmin, int &kmax) {
-  int emax = -1, smin = INT_MAX;
-  if (a.mm_ranges != nullptr) {
-    const int32_t *rg = a.mm_ranges + (int64_t)it.s * a.max_mm_ranges * 2;
-    const int clamp = a.window > 0 ? it.q_lo - a.window + 1 : INT_MIN;
-    for (int i = start; i < a.max_mm_ranges; i += step) {
-      const int s0 = __ldg(rg + 2 * i), e0 = __ldg(rg + 2 * i + 1);
-      if (s0 < e0 && s0 <= it.q_hi && e0 >= it.q_lo) {
-        emax = max(emax, e0);
-        smin = min(smin, max(s0, clamp));
-      }
-    }
-  }
-  if (warp_reduce) {
-    emax = __reduce_max_sync(0xffffffffu, emax);
-    smin = __reduce_min_sync(0xffffffffu, smin);
-  }
-  union_keys(a, it, emax, smin, kmin, kmax);
-}
-
-// Next valid item of this CTA's stream after `item` (false at the end).
-__device__ inline bool next_item(const AttnArgs &a, int &item, int stride, int n_items, int bq, Item &it) {
-  for (item += stride; item < n_items; item += stride) {
-    int32_t eb;
-    if (decode_item(a, item, bq, it, eb)) return true;
-  }
-  return false;
-}
-
 // What a softmax thread needs for one item: the item's tile range and its
 // row's visible interval [klo, khi] (empty for rows past the query length).
 struct RowSetup {
@@ -108,66 +77,7 @@ struct RowSetup {
   bool row_valid;
 };
 
-// One pass of the warp over the sequence's ranges yields both the block union
-// and every lane's own interval: a range is tested against the warp's 32 rows
-// only when it meets their span (ballot), which is rarely more than once.
-// Same rule as the visible interval of a single query: a valid range holding q
-// moves the right edge to its end and the left edge to its clamped start.
-template <int N>
-__device__ inline void row_setup(const AttnArgs &a, const Item &it, int row, int G, int lane, RowSetup &rs) {
-  rs.it = it;
-  const int wrow0 = row - lane;
-  const int wq_lo = it.ctx + it.qpos_lo + wrow0 / G;
-  const int wq_hi = it.ctx + it.qpos_lo + (wrow0 + 31) / G;
-  const int qpos = it.qpos_lo + row / G;
-  const int q = it.ctx + qpos;
-  int emax = -1, rhi = -1, smin = INT_MAX, rlo = INT_MAX;
-  if (a.mm_ranges != nullptr) {
-    const int32_t *rg = a.mm_ranges + (int64_t)it.s * a.max_mm_ranges * 2;
-    const int bclamp = a.window > 0 ? it.q_lo - a.window + 1 : INT_MIN;
-    const int rclamp = a.window > 0 ? q - a.window + 1 : INT_MIN;
-    for (int b = 0; b < a.max_mm_ranges; b += 32) {
-      int s0 = 0, e0 = -1;
-      if (b + lane < a.max_mm_ranges) {
-        s0 = __ldg(rg + 2 * (b + lane));
-        e0 = __ldg(rg + 2 * (b + lane) + 1);
-      }
-      const bool valid = s0 < e0;
-      if (valid && s0 <= it.q_hi && e0 >= it.q_lo) {
-        emax = max(emax, e0);
-        smin = min(smin, max(s0, bclamp));
-      }
-      uint32_t m = __ballot_sync(0xffffffffu, valid && s0 <= wq_hi && e0 >= wq_lo);
-      while (m != 0) {
-        const int src = __ffs(m) - 1;
-        m &= m - 1;
-        const int s1 = __shfl_sync(0xffffffffu, s0, src), e1 = __shfl_sync(0xffffffffu, e0, src);
-        if (s1 <= q && q <= e1) {
-          rhi = max(rhi, e1);
-          rlo = min(rlo, max(s1, rclamp));
-        }
-      }
-    }
-    emax = __reduce_max_sync(0xffffffffu, emax);
-    smin = __reduce_min_sync(0xffffffffu, smin);
-  }
-  int kmin, kmax;
-  union_keys(a, it, emax, smin, kmin, kmax);
-  rs.tile_lo = kmin / N;
-  rs.n_tiles = kmax / N - rs.tile_lo + 1;
-  rs.row_valid = qpos < it.qlen;
-  if (rs.row_valid) {
-    rs.klo = max(0, min(base_lo(q, a.window, a.chunk_size, a.chunk_lookback), rlo));
-    rs.khi = min(max(base_hi(q, a.window, it.causal, it.seq_len), rhi), it.seq_len - 1);
-    rs.out_row = (int64_t)(it.qstart + qpos) * a.hq + it.hk * G + row % G;
-  } else {
-    rs.klo = 1;
-    rs.khi = 0;
-    rs.out_row = 0;
-  }
-}
-
-// An item as the Q-loading producer decoded it, published in a ring of
+// An item as the scheduler warp decoded it, published in a ring of
 // kRecSlots records in shared memory for the MMA issuers and the softmax, so
 // that they do not repeat the decode (a chain of dependent global loads) at
 // every item boundary.  n_tiles 0 marks the end of the CTA's stream.  The
@@ -182,8 +92,8 @@ struct ItemRec {
   int rs[kRecRanges], re[kRecRanges];
 };
 
-// Whole warp, warp-uniform item: the item's tile range (the union of
-// block_keys) and the image ranges that meet its rows, the i-th of them kept
+// Whole warp, warp-uniform item: the item's tile range (the union of its
+// rows' intervals, union_keys) and the image ranges that meet its rows, the i-th of them kept
 // by lane i < kRecRanges in (rs, re); nr counts all of them.
 template <int N>
 __device__ inline void block_keys_rec(const AttnArgs &a, const Item &it, int lane, int &tile_lo, int &n_tiles,
@@ -248,7 +158,10 @@ __device__ inline void write_rec(ItemRec &r, const Item &it, int tile_lo, int n_
 
 // A softmax thread's RowSetup from a record: its row's interval from the
 // record's ranges, or, for a record that could not hold them all, from a scan
-// of the sequence's ranges by the warp (same rule as row_setup).  `qoff`: the
+// of the sequence's ranges by the warp: a range is tested against the warp's
+// 32 rows only when it meets their span (ballot).  Same rule as the visible
+// interval of a single query: a valid range holding q moves the right edge to
+// its end and the left edge to its clamped start.  `qoff`: the
 // position of the thread's query tile within the item (0, or bq for the
 // second tile of a pair).
 __device__ inline void row_setup_rec(const AttnArgs &a, const ItemRec &r, int row, int G, int lane,
