@@ -333,9 +333,14 @@ def run_e2e(args, step, flops, barrier, stream, world, dev):
     rows into the paged cache by slot (swa_kv_cache_write), computes the tile
     bounds and the attention, and copies out and lse back to the host.  The
     work is cut per request on three streams (host->device, compute,
-    device->host) so request r's copies overlap request r-1's kernels.  The
-    last step's host output is compared with the device-resident step's."""
-    swa, lay, d = step.swa, step.lay, step.d
+    device->host) so request r's copies overlap request r-1's kernels, and
+    consecutive steps are pipelined as a serving loop runs them: the device
+    copies of a step's inputs and outputs alternate between two sets, so step
+    i+1's host->device copies run while step i computes and copies its output
+    back; a set is refilled only after the step two back has finished reading
+    it (events).  The last step's host output is compared with the
+    device-resident step's."""
+    swa, lay = step.swa, step.lay
     qsl = [int(x) for x in lay.query_start_loc]
     R = lay.num_seqs
     slots = step.slots[:lay.num_tokens].long()
@@ -343,20 +348,27 @@ def run_e2e(args, step, flops, barrier, stream, world, dev):
     v_flat = step.v.view(-1, lay.num_heads_kv, lay.head_dim)
     host = {"q": step.q.cpu().pin_memory(), "k_new": k_flat[slots].cpu().pin_memory(),
             "v_new": v_flat[slots].cpu().pin_memory()}
-    meta = {key: t.cpu().pin_memory() for key, t in d.items() if t is not None}
-    dev_new = {"k_new": torch.empty_like(host["k_new"], device=dev), "v_new": torch.empty_like(host["v_new"], device=dev)}
+    meta = {key: t.cpu().pin_memory() for key, t in step.d.items() if t is not None}
     out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     lse_h = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + list(meta.values()))
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    sets = []
+    for _ in range(2):
+        sets.append({"d": {key: torch.empty_like(t, device=dev) for key, t in meta.items()},
+                     "q": torch.empty_like(step.q), "k_new": torch.empty_like(host["k_new"], device=dev),
+                     "v_new": torch.empty_like(host["v_new"], device=dev), "out": torch.empty_like(step.out),
+                     "lse": torch.empty_like(step.lse), "in_free": None, "out_free": None})
     # per-request views of the batch (request r alone, its query rows start at 0)
     sub_qsl = [torch.tensor([0, qsl[r + 1] - qsl[r]], dtype=torch.int32, device=dev) for r in range(R)]
     s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    mm = meta.get("mm_ranges") is not None
 
-    def e2e_step():
-        start = torch.cuda.Event()
-        start.record(stream)
-        s_h2d.wait_event(start)
+    def e2e_step(i):
+        S = sets[i % 2]
+        d = S["d"]
+        if S["in_free"] is not None:
+            s_h2d.wait_event(S["in_free"])              # the step two back no longer reads this set
         got_meta, got = torch.cuda.Event(), []
         with torch.cuda.stream(s_h2d):
             for key, t in meta.items():
@@ -364,47 +376,57 @@ def run_e2e(args, step, flops, barrier, stream, world, dev):
             got_meta.record(s_h2d)
             for r in range(R):
                 a, b = qsl[r], qsl[r + 1]
-                step.q[a:b].copy_(host["q"][a:b], non_blocking=True)
-                dev_new["k_new"][a:b].copy_(host["k_new"][a:b], non_blocking=True)
-                dev_new["v_new"][a:b].copy_(host["v_new"][a:b], non_blocking=True)
+                S["q"][a:b].copy_(host["q"][a:b], non_blocking=True)
+                S["k_new"][a:b].copy_(host["k_new"][a:b], non_blocking=True)
+                S["v_new"][a:b].copy_(host["v_new"][a:b], non_blocking=True)
                 e = torch.cuda.Event()
                 e.record(s_h2d)
                 got.append(e)
         stream.wait_event(got_meta)
-        step.feeders()                                   # slot mapping + tile bounds, all requests
+        if S["out_free"] is not None:
+            stream.wait_event(S["out_free"])             # its output was copied back
+        swa.swa_slot_mapping(d["query_start_loc"], d["positions"], d["block_table"], lay.block_size,
+                             lay.max_num_tokens, out=step.slots, err=step.err, stream=stream)
+        swa.swa_tile_bounds(d["query_start_loc"], d["seq_lens"], context_lens=d["context_lens"],
+                            mm_ranges=d["mm_ranges"] if mm else None, window=lay.window, causal=lay.causal,
+                            tile_size=step.TILE, block_q=step.BLOCK_Q, max_qblocks_per_seq=step.maxb,
+                            out=step.bounds, err=step.err, stream=stream)
         done = []
         for r in range(R):
             a, b = qsl[r], qsl[r + 1]
             stream.wait_event(got[r])
-            swa.swa_kv_cache_write(dev_new["k_new"][a:b], dev_new["v_new"][a:b], step.slots[a:b], step.k, step.v,
+            swa.swa_kv_cache_write(S["k_new"][a:b], S["v_new"][a:b], step.slots[a:b], step.k, step.v,
                                    err=step.err, stream=stream)
-            mm = d["mm_ranges"]
             swa.swa_mm_paged_attention(
-                step.q[a:b], step.k, step.v, d["block_table"][r:r + 1], sub_qsl[r], d["seq_lens"][r:r + 1],
-                context_lens=d["context_lens"][r:r + 1], mm_ranges=None if mm is None else mm[r:r + 1],
+                S["q"][a:b], step.k, step.v, d["block_table"][r:r + 1], sub_qsl[r], d["seq_lens"][r:r + 1],
+                context_lens=d["context_lens"][r:r + 1], mm_ranges=d["mm_ranges"][r:r + 1] if mm else None,
                 max_query_len=b - a, window=lay.window, causal=lay.causal, scale=lay.scale,
-                out=step.out[a:b], lse=step.lse[a:b], err=step.err, stream=stream)
+                out=S["out"][a:b], lse=S["lse"][a:b], err=step.err, stream=stream)
             e = torch.cuda.Event()
             e.record(stream)
             done.append(e)
+        S["in_free"] = done[-1]
         with torch.cuda.stream(s_d2h):
             for r in range(R):
                 a, b = qsl[r], qsl[r + 1]
                 s_d2h.wait_event(done[r])
-                out_h[a:b].copy_(step.out[a:b], non_blocking=True)
-                lse_h[a:b].copy_(step.lse[a:b], non_blocking=True)
+                out_h[a:b].copy_(S["out"][a:b], non_blocking=True)
+                lse_h[a:b].copy_(S["lse"][a:b], non_blocking=True)
         back = torch.cuda.Event()
         back.record(s_d2h)
-        stream.wait_event(back)
+        S["out_free"] = back
+        return back
 
     ref_out = step.out.clone()
-    e2e_step()
+    stream.wait_event(e2e_step(0))
+    stream.wait_event(e2e_step(1))
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, min(args.steps, 10))
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    for i in range(e2e_steps):
+        last = e2e_step(i)
+    stream.wait_event(last)
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
@@ -413,7 +435,8 @@ def run_e2e(args, step, flops, barrier, stream, world, dev):
     return {"value": round(job_rate(flops, world, e2e_ms) / 1e12, 3), "unit": UNIT,
             "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "step": "per request on three streams: H2D of q/k_new/v_new, swa_kv_cache_write + "
-                    "swa_mm_paged_attention, D2H of out/lse; slot mapping and tile bounds once per step",
+                    "swa_mm_paged_attention, D2H of out/lse; slot mapping and tile bounds once per step; "
+                    "consecutive steps pipelined over two sets of device buffers",
             "matches_device_step": same}
 
 
