@@ -291,6 +291,60 @@ def test_decode_split_kv_sampled(err):
     assert err.item() == 0
 
 
+def test_split_attention_and_merge_replay_in_a_cuda_graph(err):
+    """Split-KV attention followed by the merge (a programmatic dependent launch),
+    captured into a CUDA graph with all prefill kernels of the library and replayed:
+    bit-identical to the same calls made eagerly."""
+    from paged_sliding_window_swa_gb300 import lse_combine
+    lay = W.random_small(77, head_dim=128, block_size=16, group=4, max_seqs=3, max_ctx=1500, max_q=1,
+                         num_splits=8, with_ranges=False)
+    q, k, v, d = gpu_inputs(lay, data_seed=9)
+    P = lay.num_splits
+    po = torch.empty((P,) + tuple(q.shape), dtype=q.dtype, device=q.device)
+    pl = torch.empty((P,) + tuple(q.shape[:2]), dtype=torch.float32, device=q.device)
+    mo = torch.empty_like(q)
+    ml = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    lay2 = W.random_small(12, head_dim=256, block_size=32, group=2, max_seqs=2, max_ctx=400, max_q=300,
+                          window=200, with_ranges=True)
+    q2, k2, v2, d2 = gpu_inputs(lay2, data_seed=4)
+    o2 = torch.empty_like(q2)
+    l2 = torch.empty(q2.shape[:2], dtype=torch.float32, device=q2.device)
+
+    def calls():
+        swa.swa_mm_paged_attention(q, k, v, d["block_table"], d["query_start_loc"], d["seq_lens"],
+                                   context_lens=d["context_lens"], max_query_len=lay.max_query_len,
+                                   window=lay.window, causal=lay.causal, scale=lay.scale, num_splits=P,
+                                   splits_per_seq=d["splits_per_seq"], partial_out=po, partial_lse=pl, err=err)
+        lse_combine(po, pl, out=mo, out_lse=ml)
+        swa.swa_mm_paged_attention(q2, k2, v2, d2["block_table"], d2["query_start_loc"], d2["seq_lens"],
+                                   context_lens=d2["context_lens"], mm_ranges=d2["mm_ranges"],
+                                   max_query_len=lay2.max_query_len, window=lay2.window, causal=lay2.causal,
+                                   scale=lay2.scale, out=o2, lse=l2, err=err)
+
+    calls()
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (mo, ml, o2, l2)]
+    for t in (mo, ml, o2, l2):
+        t.fill_(7)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        calls()                                    # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        calls()
+    for t in (mo, ml, o2, l2):
+        t.fill_(7)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for got, want in zip((mo, ml, o2, l2), ref):
+        assert torch.equal(got, want)
+    assert err.item() == 0
+
+
 def test_repeated_calls_are_bit_identical(err):
     """No atomics in the arithmetic: any run-to-run difference is a race."""
     lay = W.gemma_like()
