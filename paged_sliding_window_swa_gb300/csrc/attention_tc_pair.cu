@@ -25,7 +25,8 @@
 // Sixteen warps; setmaxnreg moves registers from warps 0-7 (64 each) to the
 // softmax warpgroups (192 each):
 //   warp 0      K producer; warps 4-6 V producers (a unit's page boxes are
-//               dealt over them, one TMA box per page and chunk)
+//               dealt over them, one TMA box per page and chunk); warp 4 also
+//               writes each item's O out (below)
 //   warp 1      QK issuer, Q loads and TMEM owner: QK_A(t), QK_B(t) per key
 //               tile, each after the previous scores were loaded from S; an
 //               item's Q copy once the previous item's last QK is done
@@ -35,6 +36,11 @@
 //   warp 2      no role
 //   warps 8-11  softmax of tile A, warps 12-15 softmax of tile B: thread i of
 //               a warpgroup owns row i (TMEM lane i) of its tile.
+// At the end of an item, once both tiles' last PVs are done, the V ring is
+// idle (its producers wait for the hand-off below before the next item's
+// units), so the softmax warpgroups normalise O_A and O_B into it as bf16 in
+// the output map's swizzled boxes, and V warp 4 writes them out with TMA
+// stores (rows of a tile that runs past its sequence: plain 16-byte copies).
 // The code is kept small on purpose (32-bit counters, shifts for the
 // power-of-two page size, no runtime division in the loops): at this size the
 // SM's instruction cache decides how fast the rarely taken paths (item
@@ -71,6 +77,7 @@ struct PairCfg {
   static constexpr int OFF_K = 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + KSU * UNIT;
   static constexpr int OFF_CTRL = OFF_V + VSU * UNIT;
+  static constexpr int O_CHUNK = M * 128;            // bytes of one staged 64-column chunk of a tile's O
   static constexpr int TM_O = 0;                     // O_X at X * D
   static constexpr int TM_S = 2 * D;                 // the shared S buffer
   static constexpr int TM_P = 2 * D + N;             // P_X at TM_P + X * N / 2
@@ -83,6 +90,7 @@ struct PairCfg {
                 "the register split can only hand over what the launch allocated");
   static_assert(KSU <= kMaxUnits && VSU <= kMaxUnits && KSU >= 2 && VSU >= 4, "ring sizes");
   static_assert(KSU == VSU, "the producers share one ring walk");
+  static_assert(2 * CH * O_CHUNK <= VSU * UNIT, "both tiles' O (bf16) are staged in the V ring");
 };
 
 struct PairCtrl {
@@ -95,12 +103,55 @@ struct PairCtrl {
   uint64_t stall;                        // never signalled: the watchdog test's stalled wait
   uint64_t rec_full[kRecSlots];          // item record ord published at [ord % kRecSlots]
   uint64_t rec_empty[kRecSlots];         // ... and read by every consumer warp
+  uint64_t ostage_full;                  // both tiles' O staged in the V ring
+  uint64_t ostage_free;                  // the staged O has been read: the V ring may be refilled
   ItemRec rec[kRecSlots];
   uint32_t tmem_base;
   int abort;
 };
 
 constexpr int pair_smem_bytes() { return PairCfg::OFF_CTRL + (int)sizeof(PairCtrl); }
+
+
+// V warp 4: an item's O (both tiles), staged in the V ring by the softmax
+// (bf16, tile X at 2 X O_CHUNK, 64-column chunks of 128 rows, 128-byte
+// swizzle), to the output; the ring is released (`free_bar`) once read, unless
+// this is the CTA's last item.  A tile whose rows all lie inside the sequence
+// goes out as TMA stores by lane 0; any other is copied by the warp, for the
+// rows of the sequence only.  `tok`: tile A's first token, `ntok[X]`: tile X's
+// tokens inside the sequence.
+__device__ inline void store_staged_pair(const CUtensorMap *tm_o, int o_tma, const AttnArgs &a, uint32_t v_s,
+                                         int G, int bq, int hk, int tok, int ntok0, int ntok1, int lane, bool last,
+                                         uint32_t free_bar) {
+  using C = PairCfg;
+  bool tma = false;
+  for (int x = 0; x < 2; ++x) {
+    const int ntok = x ? ntok1 : ntok0;
+    if (ntok <= 0) continue;
+    const uint32_t base = v_s + (uint32_t)(x * C::CH * C::O_CHUNK);
+    if (o_tma && ntok == bq) {
+      if (lane == 0)
+        for (int c = 0; c < C::CH; ++c) tma_store_3d(tm_o, base + c * C::O_CHUNK, c * 64, hk * G, tok + x * bq);
+      tma = true;
+      continue;
+    }
+    const int lg = 31 - __clz(G);
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+    for (int i = lane; i < (ntok << lg) * C::CH * 8; i += 32) {   // (row, 16-byte piece)
+      const int r = i / (C::CH * 8), p = i % (C::CH * 8);
+      const int c = p >> 3, j = p & 7;
+      const uint4 v = ld_shared_v4(base + (uint32_t)(c * C::O_CHUNK + r * 128 + ((j ^ (r & 7)) << 4)));
+      const int64_t orow = (int64_t)(tok + x * bq + (r >> lg)) * a.hq + hk * G + (r & (G - 1));
+      *reinterpret_cast<uint4 *>(out + orow * C::D + p * 8) = v;
+    }
+  }
+  if (lane == 0 && tma) bulk_commit();
+  __syncwarp();
+  if (lane == 0 && !last) {
+    if (tma) bulk_wait_read<0>();
+    mbar_arrive(free_bar);
+  }
+}
 
 // A ring position: slot and the parity of its current fill.
 struct RingPos {
@@ -117,7 +168,8 @@ struct RingPos {
 template <bool NEG>
 __global__ void __launch_bounds__(PairCfg::THREADS, 1)
 attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const int G, const int n_items) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const AttnArgs a, const int G, const int n_items, const int o_tma) {
   using C = PairCfg;
   extern __shared__ __align__(1024) uint8_t dsm_ptr[];
   const uint32_t dsm = smem_u32(dsm_ptr);
@@ -152,6 +204,8 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       mbar_init(smem_u32(&ctl.o_item[x]), 1);
     }
     mbar_init(smem_u32(&ctl.s_free), 128);
+    mbar_init(smem_u32(&ctl.ostage_full), 256);
+    mbar_init(smem_u32(&ctl.ostage_free), 1);
     for (int i = 0; i < kRecSlots; ++i) {
       mbar_init(smem_u32(&ctl.rec_full[i]), 1);
       mbar_init(smem_u32(&ctl.rec_empty[i]), C::REC_READERS);
@@ -163,6 +217,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tma_prefetch_map(&tm_q);
     tma_prefetch_map(&tm_k);
     tma_prefetch_map(&tm_v);
+    if (o_tma) tma_prefetch_map(&tm_o);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl.tmem_base), C::TM_COLS);
@@ -198,7 +253,10 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int lg_bs = 31 - __clz(a.block_size);
     int u_base = 0;                                     // units issued by this warp before this item
     bool ok = true;
-    for (int ord = 0;; ++ord) {
+    // V warps: the previous item's output tiles (kv head, tile A's first token, tokens of A and B in the sequence)
+    int prev_hk = 0, prev_tok = 0, prev_n0 = 0, prev_n1 = 0;
+    int ord = 0;
+    for (;; ++ord) {
       // the item's record (n_tiles 0: the end of the stream)
       const int rs = ord % kRecSlots;
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.rec_full[rs]), (uint32_t)((ord / kRecSlots) & 1),
@@ -209,6 +267,18 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl.rec_empty[rs]));
       if (n_tiles == 0) break;
+      if (is_v && ord > 0) {
+        // The previous item's O is staged in the V ring once both of its
+        // tiles' last PVs are done: V warp 4 stores it and frees the ring
+        if (share == 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.ostage_full), (uint32_t)((ord - 1) & 1), abort_flag, wl));
+          if (!ok) break;
+          store_staged_pair(&tm_o, o_tma, a, v_s, G, bq, prev_hk, prev_tok, prev_n0, prev_n1, lane, false,
+                            smem_u32(&ctl.ostage_free));
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.ostage_free), (uint32_t)((ord - 1) & 1), abort_flag, wl));
+        if (!ok) break;
+      }
       const int total_boxes = (n_tiles * C::N) / R;
       const int32_t *bt = a.block_table + (int64_t)it.s * a.bt_stride;
       auto resolve = [&](int b) -> int {                // slot of the first key of box b
@@ -258,6 +328,18 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       }
       u_base += ul;
       if (!ok) break;
+      prev_hk = it.hk;
+      prev_tok = it.qstart + it.qpos_lo;
+      prev_n0 = max(0, min(bq, it.qlen - it.qpos_lo));
+      prev_n1 = max(0, min(bq, it.qlen - it.qpos_lo - bq));
+    }
+    if (is_v && share == 0) {
+      // the last item's O
+      if (ok && ord > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.ostage_full), (uint32_t)((ord - 1) & 1), abort_flag, wl));
+        if (ok) store_staged_pair(&tm_o, o_tma, a, v_s, G, bq, prev_hk, prev_tok, prev_n0, prev_n1, lane, true, 0u);
+      }
+      if (lane == 0) bulk_wait_all();                   // every store has landed before the CTA exits
     }
     if (!ok && lane == 0) {
       *abort_flag = 1;
@@ -609,29 +691,35 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const int64_t out_row = cur.out_row;
       ++n_done;
       if (!next_rec()) { ok = false; break; }
-      // the item's last PV_x (one o_item phase per item)
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item[x]), (uint32_t)((n_done - 1) & 1), abort_flag, wl));
+      // the item's last PVs of both tiles (one o_item phase per tile and item):
+      // the V ring, where O is staged, is then free of both tiles' V units
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.o_item[x]), (uint32_t)((n_done - 1) & 1), abort_flag, wl) &&
+                                   mbar_wait(smem_u32(&ctl.o_item[x ^ 1]), (uint32_t)((n_done - 1) & 1), abort_flag, wl));
       if (!ok) break;
-      // epilogue: O / l -> bf16, 64 columns per pass, 32-byte stores.  The
-      // next item's first PV_x overwrites O_x only after this thread's P for
-      // it (published after these loads completed).
+      // epilogue: O / l -> bf16 rows in the V ring (the V producers wait for
+      // ostage_free), tile X's two 64-column chunks at 2 X O_CHUNK, laid out as
+      // the output map's boxes with the 128-byte swizzle; V warp 4 stores them.
+      // The next item's first PV_x overwrites O_x only after this thread's P
+      // for it (published after these loads completed).
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + out_row * C::D;
 #pragma unroll 1
       for (int c = 0; c < C::D / 64; ++c) {
         uint32_t r[64];
         tmem_ld32(o_col + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(r));
         tmem_ld32(o_col + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
         tmem_wait_ld();
-        if (row_valid) {
-          uint32_t w[32];
+        const uint32_t rb = v_s + (uint32_t)((x * C::CH + c) * C::O_CHUNK + row * 128);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) w[e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) st_global_v8(o + 64 * c + 16 * e, w + 8 * e);
-        }
+        for (int j = 0; j < 8; ++j)
+          st_shared_v4(rb + ((uint32_t)(j ^ (row & 7)) << 4),
+                       pack_bf16(__uint_as_float(r[8 * j]) * inv, __uint_as_float(r[8 * j + 1]) * inv),
+                       pack_bf16(__uint_as_float(r[8 * j + 2]) * inv, __uint_as_float(r[8 * j + 3]) * inv),
+                       pack_bf16(__uint_as_float(r[8 * j + 4]) * inv, __uint_as_float(r[8 * j + 5]) * inv),
+                       pack_bf16(__uint_as_float(r[8 * j + 6]) * inv, __uint_as_float(r[8 * j + 7]) * inv));
       }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&ctl.ostage_full));
       if (row_valid && a.lse != nullptr) a.lse[out_row] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
       tc_fence_before();
     }
@@ -665,6 +753,12 @@ cudaError_t run_pair(const AttnArgs &a, cudaStream_t st) {
       !make_map(&mv, a.v_cache, C::D, a.hkv, slots, C::D * esz, (uint64_t)a.hkv * C::D * esz, 64, 1,
                 (uint32_t)min(a.block_size, C::VU_KEYS)))
     return cudaErrorInvalidValue;
+  // the output through the same box shape as Q (TMA stores of whole tiles);
+  // an output the map cannot describe is written with plain stores
+  CUtensorMap mo;
+  memset(&mo, 0, sizeof(mo));
+  const int o_tma = make_map(&mo, a.out, C::D, a.hq, a.num_tokens, C::D * esz, (uint64_t)a.hq * C::D * esz, 64, G, bq)
+                        ? 1 : 0;
   constexpr int smem = pair_smem_bytes();
   static_assert(smem <= 227 * 1024, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(attn_tc_pair_kernel<NEG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -678,17 +772,13 @@ cudaError_t run_pair(const AttnArgs &a, cudaStream_t st) {
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, attn_tc_pair_kernel<NEG>) != cudaSuccess || fa.numRegs != C::LAUNCH_REGS)
     return cudaErrorInvalidConfiguration;
-  attn_tc_pair_kernel<NEG><<<grid, C::THREADS, smem, st>>>(mq, mk, mv, a, G, (int)items);
+  attn_tc_pair_kernel<NEG><<<grid, C::THREADS, smem, st>>>(mq, mk, mv, mo, a, G, (int)items, o_tma);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-// The epilogue's 32-byte stores want a 32-byte aligned output (the library
-// only asks for 16); other outputs take the CUDA-core path.
-bool tc_pair_supported(const AttnArgs &a) {
-  return a.head_dim == 128 && (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 && tc_prefill_ok(a);
-}
+bool tc_pair_supported(const AttnArgs &a) { return a.head_dim == 128 && tc_prefill_ok(a); }
 
 cudaError_t launch_attention_tc_pair(const AttnArgs &a, cudaStream_t st) {
   // the sign of the scale is a template argument, as in attention_tc.cu

@@ -194,12 +194,6 @@ __device__ inline void tmem_st16(uint32_t taddr, const uint32_t *r) {
         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
-// 32-byte global store (8 words; the address must be 32-byte aligned).
-__device__ inline void st_global_v8(void *p, const uint32_t *w) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-               : "memory");
-}
 
 // 16-byte shared-memory load and store.
 __device__ inline uint4 ld_shared_v4(uint32_t saddr) {

@@ -119,8 +119,8 @@ def test_many_image_ranges_per_tile_all_rows(D, G, window, causal, err):
 @pytest.mark.parametrize("D", [128, 256])
 def test_output_aligned_to_16_bytes_only(D, err):
     """The library asks for 16-byte aligned outputs; one that is not 32-byte aligned
-    must give the same rows as the oracle (the head_dim-128 tensor-core kernel's
-    32-byte stores are not used for it)."""
+    must give the same rows as the oracle (the output tensor map and the plain
+    copies of partial tiles need 16 bytes only)."""
     lay = W.random_small(300 + D, head_dim=D, block_size=32, group=2, max_seqs=3, max_ctx=400, max_q=300,
                          window=200, with_ranges=True)
     q, k, v, d = gpu_inputs(lay, data_seed=3)
