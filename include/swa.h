@@ -290,6 +290,10 @@ int swa_mm_paged_attention(const void *q, const void *k_cache, const void *v_cac
  *   out_lse      fp32 [num_tokens, num_heads] or NULL
  * Host errors: NULL pointers, num_splits < 1, num_tokens < 0, num_heads < 1,
  *   head_dim not in {64, 128, 256}, unsupported dtype, misaligned pointers.
+ * Launch: as a programmatic dependent of the work enqueued before it on the
+ *   stream (it may start during the tail of a preceding kernel and waits for
+ *   that kernel's completion before reading the partials); the ordering
+ *   towards everything else in the stream is unchanged, inside CUDA graphs too.
  */
 int lse_combine(const void *partial_out, const float *partial_lse, int32_t num_splits,
                 int64_t num_tokens, int32_t num_heads, int32_t head_dim, int32_t dtype,
