@@ -177,6 +177,37 @@ def test_general_tensor_core_kernel_shapes(dtype, D, G, P, max_q, err):
     assert err.item() == 0
 
 
+@pytest.mark.parametrize("seed", range(60))
+def test_random_layout_sweep(seed, err):
+    """Random dtype, head_dim, GQA group, split count, window, causal flag, image ranges,
+    page size and lengths (up to 3000 tokens of context and 700 queries per sequence):
+    every kernel the dispatch can choose, against the oracle on up to 2500 rows."""
+    from paged_sliding_window_swa_gb300 import lse_combine
+    rng = np.random.default_rng(9000 + seed)
+    D = int(rng.choice([64, 128, 256]))
+    G = int(rng.choice([1, 2, 4, 8, 16]))
+    dtype = "fp32" if rng.random() < 0.2 else "bf16"
+    P = int(rng.choice([1, 1, 1, 2, 5]))
+    lay = W.random_small(9000 + seed, head_dim=D, group=G, dtype=dtype, max_seqs=int(rng.integers(1, 4)),
+                         max_ctx=int(rng.choice([50, 900, 3000])), max_q=int(rng.choice([1, 40, 300, 700])),
+                         num_splits=P)
+    q, k, v, d = gpu_inputs(lay, data_seed=seed)
+    rows = _all_rows(lay)
+    if len(rows) > 2500:
+        rows = [rows[i] for i in sorted(rng.choice(len(rows), 2500, replace=False))]
+    if P == 1:
+        out, lse = run_attention(lay, q, k, v, d, err=err)
+    else:
+        po, pl = run_attention(lay, q, k, v, d, err=err)
+        out, lse = lse_combine(po, pl)
+    ro, rl = oracle_rows(lay, q, k, v, rows)
+    e_out, e_lse = max_errors(out, lse, ro, rl, rows)
+    assert e_out <= atol_for(lay), e_out
+    assert e_lse <= LSE_ATOL, e_lse
+    torch.cuda.synchronize()
+    assert err.item() == 0
+
+
 def test_unused_cache_rows_never_reach_the_output(err):
     """Spare blocks and page tails hold NaN; the output must stay finite and exact."""
     for seed in range(4):
