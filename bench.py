@@ -545,11 +545,12 @@ def run_extras(dev, pk):
 
     # chunked prefill over cached context (head_dim 128, GQA 4), causal and non-causal, and
     # causal with chunked lookback (chunks of 2048, one chunk back) and alternating
-    # per-sequence causal flags
+    # per-sequence causal flags; the causal layout again at head_dim 64
     chunk_lay = dataclasses.replace(W.chunked_prefill(True), name="chunked_prefill-chunk2048-lookback1-mixed",
                                     chunk_size=2048, chunk_lookback=1,
                                     seq_causal=np.array([s % 2 for s in range(8)], np.int32))
-    for lay in (W.chunked_prefill(True), W.chunked_prefill(False), chunk_lay):
+    d64_lay = dataclasses.replace(W.chunked_prefill(True), name="chunked_prefill-head_dim64", head_dim=64)
+    for lay in (W.chunked_prefill(True), W.chunked_prefill(False), chunk_lay, d64_lay):
         q, k, v = W.make_tensors(lay, device=dev)
         d = W.device_layout(lay, dev)
         out = torch.empty_like(q)

@@ -1,9 +1,9 @@
-// Tensor-core prefill attention for head_dim 128 with two query tiles per
-// work item (same mask and pruning as attention_tc.cu: vLLM PR #53147
+// Tensor-core prefill attention for head_dim 128 and 64 with two query tiles
+// per work item (same mask and pruning as attention_tc.cu: vLLM PR #53147
 // summary, implementation items 1-2 and the compute_tile_loop_bounds excerpt).
 //
-// At head_dim 128 the tensor memory holds the two O accumulators, one S
-// buffer and the two tiles' P, so an item is a PAIR of consecutive 128-row
+// At head_dim 128 (and 64) the tensor memory holds the two O accumulators, one
+// S buffer and the two tiles' P, so an item is a PAIR of consecutive 128-row
 // query tiles A and B of one sequence and kv head (2 x 128/G positions x G
 // heads).  Every K/V tile is staged once for both, and each query tile has
 // its own softmax warpgroup that owns whole rows: no max exchange between
@@ -16,11 +16,13 @@
 // for its softmax to finish or for its PV: while one softmax warpgroup works
 // on its scores the tensor pipe runs the other tile's QK and the PVs.
 //
-// Shared memory: Q_A and Q_B (32 KB each, TMA, 128-byte swizzle, K-major) and
-// two rings of 16 KB units: a K unit holds one 64-column half of head_dim for
-// the 128 keys of a tile, a V unit all 128 columns for one 64-key half.  TMEM
-// (512 columns): O_A [0,128), O_B [128,256), S [256,384), P_A [384,448),
-// P_B [448,512) (P as bf16 pairs).
+// Shared memory: Q_A and Q_B (D x 256 B each, TMA, 128-byte swizzle, K-major)
+// and two rings of 16 KB units.  At head_dim 128 a K unit holds one 64-column
+// half of head_dim for the 128 keys of a tile and a V unit all 128 columns for
+// one 64-key half (rings of 5 + 5 units); at head_dim 64 one K unit and one V
+// unit cover a tile (rings of 6 + 6).  TMEM (512 columns): O_A [0,D),
+// O_B [D,2D), S [2D,2D+128), P_A and P_B 64 columns each after S (P as bf16
+// pairs).
 //
 // Sixteen warps; setmaxnreg moves registers from warps 0-7 (64 each) to the
 // softmax warpgroups (192 each):
@@ -55,12 +57,14 @@ namespace {
 
 using namespace tc;
 
+template <int D_, int RING_>
 struct PairCfg {
-  static constexpr int D = 128;
+  static constexpr int D = D_;
   static constexpr int N = 128;                      // keys per tile
   static constexpr int M = 128;                      // rows per query tile
   static constexpr int CH = D / 64;                  // 128-byte column chunks per row
-  static constexpr int KSU = 5, VSU = 5;             // ring slots (16 KB units)
+  static constexpr int KSU = RING_, VSU = RING_;     // ring slots (16 KB units)
+  static constexpr int UPT = CH;                     // K units and V units per key tile
   static constexpr int VW = 3;                       // V producer warps 4 .. 4 + VW - 1
   static constexpr int THREADS = 512;
   static constexpr int LAUNCH_REGS = 128;
@@ -71,7 +75,7 @@ struct PairCfg {
   static constexpr int Q_BYTES = M * D * 2;
   static constexpr int UNIT = 16384;                 // bytes of a K or V unit
   static constexpr int KU_CHUNK = N * 128;           // a K unit is one chunk of 128 keys
-  static constexpr int VU_KEYS = N / 2;              // keys per V unit
+  static constexpr int VU_KEYS = N / UPT;            // keys per V unit
   static constexpr int VU_CHUNK = VU_KEYS * 128;     // bytes per chunk of a V unit
   static constexpr int OFF_Q = 0;                    // Q_A, then Q_B
   static constexpr int OFF_K = 2 * Q_BYTES;
@@ -91,6 +95,7 @@ struct PairCfg {
   static_assert(KSU <= kMaxUnits && VSU <= kMaxUnits && KSU >= 2 && VSU >= 4, "ring sizes");
   static_assert(KSU == VSU, "the producers share one ring walk");
   static_assert(2 * CH * O_CHUNK <= VSU * UNIT, "both tiles' O (bf16) are staged in the V ring");
+  static_assert((D == 64 || D == 128) && UPT <= 2 && VU_KEYS * D * 2 == UNIT && N * 128 == UNIT, "16 KB units");
 };
 
 struct PairCtrl {
@@ -110,20 +115,21 @@ struct PairCtrl {
   int abort;
 };
 
-constexpr int pair_smem_bytes() { return PairCfg::OFF_CTRL + (int)sizeof(PairCtrl); }
+template <class C>
+constexpr int pair_smem_bytes() { return C::OFF_CTRL + (int)sizeof(PairCtrl); }
 
 
 // V warp 4: an item's O (both tiles), staged in the V ring by the softmax
-// (bf16, tile X at 2 X O_CHUNK, 64-column chunks of 128 rows, 128-byte
+// (bf16, tile X at CH X O_CHUNK, 64-column chunks of 128 rows, 128-byte
 // swizzle), to the output; the ring is released (`free_bar`) once read, unless
 // this is the CTA's last item.  A tile whose rows all lie inside the sequence
 // goes out as TMA stores by lane 0; any other is copied by the warp, for the
 // rows of the sequence only.  `tok`: tile A's first token, `ntok[X]`: tile X's
 // tokens inside the sequence.
+template <class C>
 __device__ inline void store_staged_pair(const CUtensorMap *tm_o, int o_tma, const AttnArgs &a, uint32_t v_s,
                                          int G, int bq, int hk, int tok, int ntok0, int ntok1, int lane, bool last,
                                          uint32_t free_bar) {
-  using C = PairCfg;
   bool tma = false;
   for (int x = 0; x < 2; ++x) {
     const int ntok = x ? ntok1 : ntok0;
@@ -165,12 +171,11 @@ struct RingPos {
   }
 };
 
-template <bool NEG>
-__global__ void __launch_bounds__(PairCfg::THREADS, 1)
+template <class C, bool NEG>
+__global__ void __launch_bounds__(C::THREADS, 1)
 attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const AttnArgs a, const int G, const int n_items, const int o_tma) {
-  using C = PairCfg;
   extern __shared__ __align__(1024) uint8_t dsm_ptr[];
   const uint32_t dsm = smem_u32(dsm_ptr);
   PairCtrl &ctl = *reinterpret_cast<PairCtrl *>(dsm_ptr + C::OFF_CTRL);
@@ -245,7 +250,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int share = is_v ? warp - 4 : 0;
     const int SU = is_v ? C::VSU : C::KSU;
     const CUtensorMap *map = is_v ? &tm_v : &tm_k;
-    const int unit_keys = is_v ? C::VU_KEYS : C::N;     // K units: 128 keys, V units: 64 keys
+    const int unit_keys = is_v ? C::VU_KEYS : C::N;     // K units: 128 keys, V units: 128 / UPT keys
     const int R = min(a.block_size, unit_keys);         // rows per box
     const int boxes = unit_keys / R;                    // boxes per unit (per chunk)
     const int uch = is_v ? C::CH : 1;                   // chunks per unit
@@ -273,7 +278,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (share == 0) {
           ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.ostage_full), (uint32_t)((ord - 1) & 1), abort_flag, wl));
           if (!ok) break;
-          store_staged_pair(&tm_o, o_tma, a, v_s, G, bq, prev_hk, prev_tok, prev_n0, prev_n1, lane, false,
+          store_staged_pair<C>(&tm_o, o_tma, a, v_s, G, bq, prev_hk, prev_tok, prev_n0, prev_n1, lane, false,
                             smem_u32(&ctl.ostage_free));
         }
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.ostage_free), (uint32_t)((ord - 1) & 1), abort_flag, wl));
@@ -295,7 +300,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       int batch = 0;
       int prv = oob, cur = resolve(lane), nxt = resolve(32 + lane);
       int ul = 0;
-      for (; ul < 2 * n_tiles; ++ul) {                 // unit ul of this item: tile ul/2, half ul%2
+      for (; ul < C::UPT * n_tiles; ++ul) {            // unit ul of this item: tile ul / UPT, part ul % UPT
         const int u = u_base + ul;
         const int slot_i = (int)(u % SU);
         if (u >= SU) {
@@ -304,13 +309,13 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                           mbar_wait(empty, (uint32_t)(((u / SU) - 1) & 1), abort_flag, wl));
           if (!ok) break;
         }
-        const int t = ul >> 1, half = ul & 1;
+        const int t = ul / C::UPT, half = ul % C::UPT;
         const uint32_t full = smem_u32(is_v ? &ctl.v_full[slot_i] : &ctl.k_full[slot_i]);
         const uint32_t dst = (is_v ? v_s : k_s) + slot_i * C::UNIT;
         if (share == 0 && lane == 0) mbar_expect_tx(full, C::UNIT);
         __syncwarp();
-        // K: unit = 64-column half `half` of tile t's 128 keys; V: key half `half`
-        const int b0 = is_v ? (2 * t + half) * boxes : t * boxes;
+        // K: unit = 64-column chunk `half` of tile t's 128 keys; V: key part `half`
+        const int b0 = is_v ? (C::UPT * t + half) * boxes : t * boxes;
         while (b0 + boxes - 1 >= (batch + 1) * 32) {    // warp-uniform batch advance
           prv = cur;
           cur = nxt;
@@ -337,7 +342,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       // the last item's O
       if (ok && ord > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.ostage_full), (uint32_t)((ord - 1) & 1), abort_flag, wl));
-        if (ok) store_staged_pair(&tm_o, o_tma, a, v_s, G, bq, prev_hk, prev_tok, prev_n0, prev_n1, lane, true, 0u);
+        if (ok) store_staged_pair<C>(&tm_o, o_tma, a, v_s, G, bq, prev_hk, prev_tok, prev_n0, prev_n1, lane, true, 0u);
       }
       if (lane == 0) bulk_wait_all();                   // every store has landed before the CTA exits
     }
@@ -384,16 +389,16 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (!ok) break;
         tc_fence_after();
         for (int j = 0; ok && j < n; ++j) {
-          const RingPos k0 = kp;                        // the tile's two K units
+          const RingPos k0 = kp;                        // the tile's K units (one per 64 columns)
           RingPos k1 = kp;
-          k1.next(C::KSU);
+          if (C::UPT > 1) k1.next(C::KSU);
           for (int x = 0; ok && x < 2; ++x) {
             if (n_qk > 0) {
               ok = mbar_wait(smem_u32(&ctl.s_free), (uint32_t)((n_qk - 1) & 1), abort_flag, wl);
               if (!ok) break;
               tc_fence_after();
             }
-            for (int half = 0; ok && half < 2; ++half) {  // K unit = 64-column half of head_dim
+            for (int half = 0; ok && half < C::UPT; ++half) {  // K unit = one 64-column chunk of head_dim
               const RingPos &kh = half ? k1 : k0;
               if (x == 0) {
                 ok = mbar_wait(smem_u32(&ctl.k_full[kh.slot]), kh.phase, abort_flag, wl);
@@ -444,12 +449,12 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         for (int j = 0; ok && j < n_tiles; ++j, tpar ^= 1u) {
           const RingPos v0 = vp;
           RingPos v1 = vp;
-          v1.next(C::VSU);
+          if (C::UPT > 1) v1.next(C::VSU);
           for (int x = 0; ok && x < 2; ++x) {
             ok = mbar_wait(smem_u32(&ctl.p_full[x]), tpar, abort_flag, wl);
             if (!ok) break;
             tc_fence_after();
-            for (int half = 0; ok && half < 2; ++half) {  // V unit = 64-key half of the tile
+            for (int half = 0; ok && half < C::UPT; ++half) {  // V unit = N / UPT keys of the tile
               const RingPos &vh = half ? v1 : v0;
               if (x == 0) {
                 ok = mbar_wait(smem_u32(&ctl.v_full[vh.slot]), vh.phase, abort_flag, wl);
@@ -633,13 +638,13 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (x == 0 && kt0 + N > it.seq_len) {
           // keys past the sequence end: their V rows may hold anything; zero
           // them before P_A(t) is published (PV_B(t) follows PV_A(t)).  V unit
-          // 2t + half is the latest fill of its slot (tile t-1's units sit in
+          // UPT t + half is the latest fill of its slot (tile t-1's units sit in
           // other slots, which PV_B(t-1) may still read), so its v_full parity
           // is unambiguous.
-          for (int half = 0; half < 2 && ok; ++half) {
+          for (int half = 0; half < C::UPT && ok; ++half) {
             const int k0 = kt0 + half * C::VU_KEYS;
             if (k0 + C::VU_KEYS <= it.seq_len) continue;
-            const uint32_t u = 2u * (uint32_t)t + half;
+            const uint32_t u = (uint32_t)C::UPT * (uint32_t)t + half;
             const int slot = (int)(u % C::VSU);
             ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl.v_full[slot]), (u / C::VSU) & 1u, abort_flag,
                                                    wl));
@@ -650,7 +655,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             for (int i = sid; i < C::CH * C::VU_KEYS * 8; i += 128) {   // 16-byte pieces: chunk, row, piece
               const int r = (i >> 3) & (C::VU_KEYS - 1);
               if (r >= r0)
-                *reinterpret_cast<uint4 *>(unit + (i >> 9) * C::VU_CHUNK + r * 128 + (i & 7) * 16) =
+                *reinterpret_cast<uint4 *>(unit + (i / (C::VU_KEYS * 8)) * C::VU_CHUNK + r * 128 + (i & 7) * 16) =
                     make_uint4(0, 0, 0, 0);
             }
           }
@@ -697,7 +702,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                                    mbar_wait(smem_u32(&ctl.o_item[x ^ 1]), (uint32_t)((n_done - 1) & 1), abort_flag, wl));
       if (!ok) break;
       // epilogue: O / l -> bf16 rows in the V ring (the V producers wait for
-      // ostage_free), tile X's two 64-column chunks at 2 X O_CHUNK, laid out as
+      // ostage_free), tile X's 64-column chunks at CH X O_CHUNK, laid out as
       // the output map's boxes with the 128-byte swizzle; V warp 4 stores them.
       // The next item's first PV_x overwrites O_x only after this thread's P
       // for it (published after these loads completed).
@@ -739,9 +744,8 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 }
 
 // ------------------------------------------------------------------ host side
-template <bool NEG>
+template <class C, bool NEG>
 cudaError_t run_pair(const AttnArgs &a, cudaStream_t st) {
-  using C = PairCfg;
   const int G = a.hq / a.hkv;
   const int bq = C::M / G;
   CUtensorMap mq, mk, mv;
@@ -759,9 +763,9 @@ cudaError_t run_pair(const AttnArgs &a, cudaStream_t st) {
   memset(&mo, 0, sizeof(mo));
   const int o_tma = make_map(&mo, a.out, C::D, a.hq, a.num_tokens, C::D * esz, (uint64_t)a.hq * C::D * esz, 64, G, bq)
                         ? 1 : 0;
-  constexpr int smem = pair_smem_bytes();
+  constexpr int smem = pair_smem_bytes<C>();
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_pair_kernel<NEG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_pair_kernel<C, NEG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t items = (a.num_tokens / (2 * bq) + a.num_seqs) * (int64_t)a.hkv;
   const int sms = sm_count();
@@ -770,19 +774,23 @@ cudaError_t run_pair(const AttnArgs &a, cudaStream_t st) {
   // The register split hands over exactly the launch allocation: a kernel built
   // with another per-thread count would wait forever in setmaxnreg.inc.
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, attn_tc_pair_kernel<NEG>) != cudaSuccess || fa.numRegs != C::LAUNCH_REGS)
+  if (cudaFuncGetAttributes(&fa, attn_tc_pair_kernel<C, NEG>) != cudaSuccess || fa.numRegs != C::LAUNCH_REGS)
     return cudaErrorInvalidConfiguration;
-  attn_tc_pair_kernel<NEG><<<grid, C::THREADS, smem, st>>>(mq, mk, mv, mo, a, G, (int)items, o_tma);
+  attn_tc_pair_kernel<C, NEG><<<grid, C::THREADS, smem, st>>>(mq, mk, mv, mo, a, G, (int)items, o_tma);
   return cudaGetLastError();
 }
 
+using Pair128 = PairCfg<128, 5>;   // K and V rings of 5 units
+using Pair64 = PairCfg<64, 6>;     // Q tiles of 16 KB leave room for 6 + 6
+
 }  // namespace
 
-bool tc_pair_supported(const AttnArgs &a) { return a.head_dim == 128 && tc_prefill_ok(a); }
+bool tc_pair_supported(const AttnArgs &a) { return (a.head_dim == 128 || a.head_dim == 64) && tc_prefill_ok(a); }
 
 cudaError_t launch_attention_tc_pair(const AttnArgs &a, cudaStream_t st) {
   // the sign of the scale is a template argument, as in attention_tc.cu
-  return a.scale < 0.f ? run_pair<true>(a, st) : run_pair<false>(a, st);
+  if (a.head_dim == 64) return a.scale < 0.f ? run_pair<Pair64, true>(a, st) : run_pair<Pair64, false>(a, st);
+  return a.scale < 0.f ? run_pair<Pair128, true>(a, st) : run_pair<Pair128, false>(a, st);
 }
 
 }  // namespace swa

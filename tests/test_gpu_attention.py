@@ -83,7 +83,8 @@ def test_random_small_all_rows(seed, err):
 
 
 @pytest.mark.parametrize("D,B,G", [(128, 16, 2), (256, 16, 2), (128, 16, 4), (256, 32, 1),
-                                   (128, 64, 8), (64, 128, 4), (128, 128, 16)])
+                                   (128, 64, 8), (64, 128, 4), (128, 128, 16), (64, 16, 2), (64, 32, 16),
+                                   (64, 64, 1)])
 def test_shapes_all_rows(D, B, G, err):
     lay = W.random_small(100 + D + B + G, head_dim=D, block_size=B, group=G, max_seqs=3, max_ctx=700,
                          max_q=300, window=int(np.random.default_rng(D + B).choice([48, 300])),
@@ -92,7 +93,7 @@ def test_shapes_all_rows(D, B, G, err):
 
 
 @pytest.mark.parametrize("D,G,window,causal", [(256, 2, 48, True), (256, 1, 300, False), (128, 2, 300, True),
-                                              (128, 4, 48, False)])
+                                              (128, 4, 48, False), (64, 4, 300, True), (64, 8, 48, False)])
 def test_many_image_ranges_per_tile_all_rows(D, G, window, causal, err):
     """Dozens of short, partly overlapping image ranges: a 128-row tile meets more of
     them than an item record holds, so the softmax scans the sequence's ranges itself."""
@@ -116,7 +117,7 @@ def test_many_image_ranges_per_tile_all_rows(D, G, window, causal, err):
     _check(lay, _all_rows(lay), err=err)
 
 
-@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("D", [64, 128, 256])
 def test_output_aligned_to_16_bytes_only(D, err):
     """The library asks for 16-byte aligned outputs; one that is not 32-byte aligned
     must give the same rows as the oracle (the output tensor map and the plain
