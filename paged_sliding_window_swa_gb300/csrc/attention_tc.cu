@@ -284,7 +284,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                              abort_flag, wl));
       if (!ok) break;
       const Item it = ctl.rec[rs].it;
-      const int tile_lo = ctl.rec[rs].tile_lo, n_tiles = ctl.rec[rs].n_tiles;
+      const int key_lo = ctl.rec[rs].key_lo, n_tiles = ctl.rec[rs].n_tiles;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl.rec_empty[rs]));
       if (n_tiles == 0) break;
@@ -303,7 +303,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const int total_boxes = (n_tiles * C::N) / R;
       const int32_t *bt = a.block_table + (int64_t)it.s * a.bt_stride;
       auto resolve = [&](int b) -> int {                // slot of the first key of box b
-        const int k = tile_lo * C::N + b * R;
+        const int k = key_lo + b * R;
         int slot = oob;
         if (b < total_boxes && k < it.seq_len) {
           const int page = k >> lg_bs;
@@ -493,13 +493,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // of the slowest reader.
     bool ok = true;
     int ord = 0;
-    auto publish = [&](const Item &it, int tile_lo, int n_tiles, int nr, int rrs, int rre) -> bool {
+    auto publish = [&](const Item &it, int key_lo, int n_tiles, int nr, int rrs, int rre) -> bool {
       const int rs = ord % kRecSlots;
       if (ord >= kRecSlots &&
           !__all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(&ctl.rec_empty[rs]), (uint32_t)(((ord / kRecSlots) - 1) & 1),
                                              abort_flag, wl)))
         return false;
-      write_rec(ctl.rec[rs], it, tile_lo, n_tiles, nr, rrs, rre, lane);
+      write_rec(ctl.rec[rs], it, key_lo, n_tiles, nr, rrs, rre, lane);
       if (lane == 0) mbar_arrive(smem_u32(&ctl.rec_full[rs]));
       ++ord;
       return true;
@@ -511,9 +511,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (eb != 0 && lane == 0) report(a.err, eb);
         continue;
       }
-      int tile_lo, n_tiles, nr, rrs, rre;
-      block_keys_rec<C::N>(a, it, lane, tile_lo, n_tiles, nr, rrs, rre);
-      ok = publish(it, tile_lo, n_tiles, nr, rrs, rre);
+      int key_lo, n_tiles, nr, rrs, rre;
+      block_keys_rec<C::N>(a, it, lane, key_lo, n_tiles, nr, rrs, rre);
+      ok = publish(it, key_lo, n_tiles, nr, rrs, rre);
     }
     if (ok) ok = publish(Item{}, 0, 0, 0, 0, -1);         // the end of the stream
     if (!ok && lane == 0) {
@@ -559,11 +559,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     bool ok = next_rec();
     while (ok && have) {
       const Item &it = cur.it;
-      const int tile_lo = cur.tile_lo, n_tiles = cur.n_tiles;
+      const int key_lo = cur.key_lo, n_tiles = cur.n_tiles;
       const int klo = cur.klo, khi = cur.khi;
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < n_tiles; ++j, ++t) {
-        const int kt0 = (tile_lo + j) * C::N;
+        const int kt0 = key_lo + j * C::N;
         const int kc0 = kt0 + h * NH;                    // key of this warpgroup's first column
         const int sb = (int)(t % C::NS);                 // S buffer of tile t
         ok = mbar_wait(smem_u32(&ctl.s_full[sb]), (uint32_t)((t / C::NS) & 1), abort_flag, wl);

@@ -71,7 +71,7 @@ __device__ inline void union_keys(const AttnArgs &a, const Item &it, int emax, i
 // row's visible interval [klo, khi] (empty for rows past the query length).
 struct RowSetup {
   Item it;
-  int tile_lo, n_tiles;
+  int key_lo, n_tiles;
   int klo, khi;
   int64_t out_row;
   bool row_valid;
@@ -87,16 +87,20 @@ constexpr int kRecSlots = 4;
 constexpr int kRecRanges = 4;
 struct ItemRec {
   Item it;
-  int tile_lo, n_tiles;
+  int key_lo, n_tiles;                 // key tiles [key_lo + j N, key_lo + (j + 1) N), j < n_tiles
   int nr;
   int rs[kRecRanges], re[kRecRanges];
 };
 
-// Whole warp, warp-uniform item: the item's tile range (the union of its
-// rows' intervals, union_keys) and the image ranges that meet its rows, the i-th of them kept
-// by lane i < kRecRanges in (rs, re); nr counts all of them.
+// Whole warp, warp-uniform item: the item's key tiles (N keys each, covering
+// the union of its rows' intervals, union_keys) and the image ranges that meet
+// its rows, the i-th of them kept by lane i < kRecRanges in (rs, re); nr counts
+// all of them.  The first tile starts at the union's first key rounded down to
+// min(page size, N), not to a multiple of N: every page box a tile loads then
+// still lies in one page, and a window of W keys seen from b positions takes
+// ceil((W + b - 1 + page - 1) / N) tiles instead of up to one more.
 template <int N>
-__device__ inline void block_keys_rec(const AttnArgs &a, const Item &it, int lane, int &tile_lo, int &n_tiles,
+__device__ inline void block_keys_rec(const AttnArgs &a, const Item &it, int lane, int &key_lo, int &n_tiles,
                                       int &nr, int &rs, int &re) {
   int emax = -1, smin = INT_MAX;
   nr = 0;
@@ -134,13 +138,13 @@ __device__ inline void block_keys_rec(const AttnArgs &a, const Item &it, int lan
   }
   int kmin, kmax;
   union_keys(a, it, emax, smin, kmin, kmax);
-  tile_lo = kmin / N;
-  n_tiles = kmax / N - tile_lo + 1;
+  key_lo = kmin & -min(a.block_size, N);             // page sizes are powers of two
+  n_tiles = (kmax - key_lo) / N + 1;
 }
 
 // Whole warp: writes the record (n_tiles 0: the end of the stream).  The
 // caller publishes it afterwards with one release (an mbarrier arrive).
-__device__ inline void write_rec(ItemRec &r, const Item &it, int tile_lo, int n_tiles, int nr, int rs, int re,
+__device__ inline void write_rec(ItemRec &r, const Item &it, int key_lo, int n_tiles, int nr, int rs, int re,
                                  int lane) {
   if (lane < nr && lane < kRecRanges) {
     r.rs[lane] = rs;
@@ -148,7 +152,7 @@ __device__ inline void write_rec(ItemRec &r, const Item &it, int tile_lo, int n_
   }
   if (lane == 0) {
     r.it = it;
-    r.tile_lo = tile_lo;
+    r.key_lo = key_lo;
     r.n_tiles = n_tiles;
     r.nr = nr <= kRecRanges ? nr : -1;
   }
@@ -168,7 +172,7 @@ __device__ inline void row_setup_rec(const AttnArgs &a, const ItemRec &r, int ro
                                      RowSetup &rs, int qoff = 0) {
   rs.it = r.it;
   rs.it.qpos_lo += qoff;
-  rs.tile_lo = r.tile_lo;
+  rs.key_lo = r.key_lo;
   rs.n_tiles = r.n_tiles;
   const Item &it = rs.it;
   const int qpos = it.qpos_lo + row / G;
