@@ -109,6 +109,7 @@ struct Cfg {
   static constexpr int TM_S = D;
   static constexpr uint32_t TM_COLS = 512;
   static constexpr uint32_t IDESC_QK = idesc_bf16(128, N, false);
+  static constexpr uint32_t IDESC_QK_HALF = idesc_bf16(128, N / 2, false);   // an item's last tile, first half
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
   static_assert(D + NS * N <= 512, "TMEM budget");
   static_assert((NSW == 2 || NSW == 4) && NS >= 2 && NS <= 3, "softmax warpgroups, S buffers");
@@ -388,7 +389,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int rs = ord % kRecSlots;
         ok = mbar_wait(smem_u32(&ctl.rec_full[rs]), (uint32_t)((ord / kRecSlots) & 1), abort_flag, wl);
         if (!ok) break;
-        const int n = ctl.rec[rs].n_tiles;
+        const int n = ctl.rec[rs].n_tiles, hl = ctl.rec[rs].half_last;
         const int q_hk = ctl.rec[rs].it.hk, q_tok = ctl.rec[rs].it.qstart + ctl.rec[rs].it.qpos_lo;
         mbar_arrive(smem_u32(&ctl.rec_empty[rs]));
         if (n == 0) break;
@@ -411,6 +412,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc_fence_after();
           }
           const uint32_t d = tmem + C::TM_S + (uint32_t)sb * C::N;
+          // the item's last tile: only its first N / 2 keys when no row sees the rest
+          const uint32_t idesc = (j == n - 1 && hl) ? C::IDESC_QK_HALF : C::IDESC_QK;
           for (int half = 0; ok && half < 2; ++half) {
             const uint32_t u = 2u * (uint32_t)t + half;
             const int slot = (int)(u % C::KSU);
@@ -423,7 +426,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int kk = 0; kk < C::D / 32; ++kk) {    // 16-column steps over this half of head_dim
               const uint32_t off = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;   // chunk, then 32 B in the swizzle row
               const uint32_t offk = (kk >> 2) * C::KU_CHUNK + (kk & 3) * 32;
-              mma_ss(d, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + offk, 16, 1024), C::IDESC_QK,
+              mma_ss(d, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + offk, 16, 1024), idesc,
                      (half > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(smem_u32(&ctl.k_empty[slot]));
@@ -452,12 +455,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // the item's record (n_tiles 0: the end of the stream)
         ok = mbar_wait(smem_u32(&ctl.rec_full[ord % kRecSlots]), (uint32_t)((ord / kRecSlots) & 1), abort_flag, wl);
         if (!ok) break;
-        const int n_tiles = ctl.rec[ord % kRecSlots].n_tiles;
+        const int n_tiles = ctl.rec[ord % kRecSlots].n_tiles, hl = ctl.rec[ord % kRecSlots].half_last;
         mbar_arrive(smem_u32(&ctl.rec_empty[ord % kRecSlots]));
         if (n_tiles == 0) break;
         for (int j = 0; ok && j < n_tiles; ++j, ++t) {
           const int sb = (int)(t % C::NS);
           ok = mbar_wait(smem_u32(&ctl.p_full[sb]), (uint32_t)((t / C::NS) & 1), abort_flag, wl);
+          // keys of the tile that take part: the first N / 2 of an item's last tile when half_last
+          const int lim = (j == n_tiles - 1 && hl) ? C::N / 2 : C::N;
           for (int half = 0; ok && half < 2; ++half) {
             const uint32_t u = 2u * (uint32_t)t + half;
             const int slot = (int)(u % C::VSU);
@@ -468,8 +473,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint32_t vb = v_s + slot * C::UNIT;
 #pragma unroll
             for (int kk = 0; kk < C::VU_KEYS / 16; ++kk)
-              mma_ts(tmem + C::TM_O, p_t + kk * 8, smem_desc_sw128(vb + kk * 16 * 128, C::VU_CHUNK, 1024), C::IDESC_PV,
-                     (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
+              if (half * C::VU_KEYS + kk * 16 < lim)
+                mma_ts(tmem + C::TM_O, p_t + kk * 8, smem_desc_sw128(vb + kk * 16 * 128, C::VU_CHUNK, 1024), C::IDESC_PV,
+                       (j > 0 || half > 0 || kk > 0) ? 1u : 0u);
             mma_commit(smem_u32(&ctl.v_empty[slot]));
           }
           if (!ok) break;
@@ -493,13 +499,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // of the slowest reader.
     bool ok = true;
     int ord = 0;
-    auto publish = [&](const Item &it, int key_lo, int n_tiles, int nr, int rrs, int rre) -> bool {
+    auto publish = [&](const Item &it, int key_lo, int n_tiles, int hl, int nr, int rrs, int rre) -> bool {
       const int rs = ord % kRecSlots;
       if (ord >= kRecSlots &&
           !__all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(&ctl.rec_empty[rs]), (uint32_t)(((ord / kRecSlots) - 1) & 1),
                                              abort_flag, wl)))
         return false;
-      write_rec(ctl.rec[rs], it, key_lo, n_tiles, nr, rrs, rre, lane);
+      write_rec(ctl.rec[rs], it, key_lo, n_tiles, hl, nr, rrs, rre, lane);
       if (lane == 0) mbar_arrive(smem_u32(&ctl.rec_full[rs]));
       ++ord;
       return true;
@@ -511,11 +517,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (eb != 0 && lane == 0) report(a.err, eb);
         continue;
       }
-      int key_lo, n_tiles, nr, rrs, rre;
-      block_keys_rec<C::N>(a, it, lane, key_lo, n_tiles, nr, rrs, rre);
-      ok = publish(it, key_lo, n_tiles, nr, rrs, rre);
+      int key_lo, n_tiles, hl, nr, rrs, rre;
+      block_keys_rec<C::N>(a, it, lane, key_lo, n_tiles, hl, nr, rrs, rre);
+      ok = publish(it, key_lo, n_tiles, hl, nr, rrs, rre);
     }
-    if (ok) ok = publish(Item{}, 0, 0, 0, 0, -1);         // the end of the stream
+    if (ok) ok = publish(Item{}, 0, 0, 0, 0, 0, -1);         // the end of the stream
     if (!ok && lane == 0) {
       *abort_flag = 1;
       report(a.err, SWA_ERR_TIMEOUT);

@@ -492,13 +492,13 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // of the slowest reader.
     bool ok = true;
     int ord = 0;
-    auto publish = [&](const Item &it, int key_lo, int n_tiles, int nr, int rrs, int rre) -> bool {
+    auto publish = [&](const Item &it, int key_lo, int n_tiles, int hl, int nr, int rrs, int rre) -> bool {
       const int rs = ord % kRecSlots;
       if (ord >= kRecSlots &&
           !__all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(&ctl.rec_empty[rs]),
                                                    (uint32_t)(((ord / kRecSlots) - 1) & 1), abort_flag, wl)))
         return false;
-      write_rec(ctl.rec[rs], it, key_lo, n_tiles, nr, rrs, rre, lane);
+      write_rec(ctl.rec[rs], it, key_lo, n_tiles, hl, nr, rrs, rre, lane);
       if (lane == 0) mbar_arrive(smem_u32(&ctl.rec_full[rs]));
       ++ord;
       return true;
@@ -510,11 +510,11 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (eb != 0 && lane == 0) report(a.err, eb);
         continue;
       }
-      int key_lo, n_tiles, nr, rrs, rre;
-      block_keys_rec<C::N>(a, it, lane, key_lo, n_tiles, nr, rrs, rre);
-      ok = publish(it, key_lo, n_tiles, nr, rrs, rre);
+      int key_lo, n_tiles, hl, nr, rrs, rre;
+      block_keys_rec<C::N>(a, it, lane, key_lo, n_tiles, hl, nr, rrs, rre);
+      ok = publish(it, key_lo, n_tiles, hl, nr, rrs, rre);
     }
-    if (ok) ok = publish(Item{}, 0, 0, 0, 0, -1);         // the end of the stream
+    if (ok) ok = publish(Item{}, 0, 0, 0, 0, 0, -1);         // the end of the stream
     if (!ok && lane == 0) {
       *abort_flag = 1;
       report(a.err, SWA_ERR_TIMEOUT);

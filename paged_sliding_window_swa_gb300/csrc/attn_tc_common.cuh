@@ -88,6 +88,7 @@ constexpr int kRecRanges = 4;
 struct ItemRec {
   Item it;
   int key_lo, n_tiles;                 // key tiles [key_lo + j N, key_lo + (j + 1) N), j < n_tiles
+  int half_last;                       // 1: no row sees a key in the last tile's second half
   int nr;
   int rs[kRecRanges], re[kRecRanges];
 };
@@ -99,9 +100,11 @@ struct ItemRec {
 // min(page size, N), not to a multiple of N: every page box a tile loads then
 // still lies in one page, and a window of W keys seen from b positions takes
 // ceil((W + b - 1 + page - 1) / N) tiles instead of up to one more.
+// `half_last`: the union ends in the first N / 2 keys of the last tile, so its
+// MMAs need only those (the softmax masks the rest of the tile anyway).
 template <int N>
 __device__ inline void block_keys_rec(const AttnArgs &a, const Item &it, int lane, int &key_lo, int &n_tiles,
-                                      int &nr, int &rs, int &re) {
+                                      int &half_last, int &nr, int &rs, int &re) {
   int emax = -1, smin = INT_MAX;
   nr = 0;
   rs = 0;
@@ -140,12 +143,13 @@ __device__ inline void block_keys_rec(const AttnArgs &a, const Item &it, int lan
   union_keys(a, it, emax, smin, kmin, kmax);
   key_lo = kmin & -min(a.block_size, N);             // page sizes are powers of two
   n_tiles = (kmax - key_lo) / N + 1;
+  half_last = kmax - (key_lo + (n_tiles - 1) * N) < N / 2 ? 1 : 0;
 }
 
 // Whole warp: writes the record (n_tiles 0: the end of the stream).  The
 // caller publishes it afterwards with one release (an mbarrier arrive).
-__device__ inline void write_rec(ItemRec &r, const Item &it, int key_lo, int n_tiles, int nr, int rs, int re,
-                                 int lane) {
+__device__ inline void write_rec(ItemRec &r, const Item &it, int key_lo, int n_tiles, int half_last, int nr,
+                                 int rs, int re, int lane) {
   if (lane < nr && lane < kRecRanges) {
     r.rs[lane] = rs;
     r.re[lane] = re;
@@ -153,6 +157,7 @@ __device__ inline void write_rec(ItemRec &r, const Item &it, int key_lo, int n_t
   if (lane == 0) {
     r.it = it;
     r.key_lo = key_lo;
+    r.half_last = half_last;
     r.n_tiles = n_tiles;
     r.nr = nr <= kRecRanges ? nr : -1;
   }
