@@ -22,7 +22,8 @@
 // one 64-key half (rings of 5 + 5 units); at head_dim 64 one K unit and one V
 // unit cover a tile (rings of 6 + 6).  TMEM (512 columns): O_A [0,D),
 // O_B [D,2D), S [2D,2D+128), P_A and P_B 64 columns each after S (P as bf16
-// pairs).
+// pairs).  At head_dim 64 there is room for one S buffer per tile (S_A, S_B),
+// so each QK waits only for its own tile's previous score load.
 //
 // Sixteen warps; setmaxnreg moves registers from warps 0-7 (64 each) to the
 // softmax warpgroups (192 each):
@@ -83,12 +84,15 @@ struct PairCfg {
   static constexpr int OFF_CTRL = OFF_V + VSU * UNIT;
   static constexpr int O_CHUNK = M * 128;            // bytes of one staged 64-column chunk of a tile's O
   static constexpr int TM_O = 0;                     // O_X at X * D
-  static constexpr int TM_S = 2 * D;                 // the shared S buffer
-  static constexpr int TM_P = 2 * D + N;             // P_X at TM_P + X * N / 2
+  // one S buffer per query tile where TMEM has room (head_dim 64), else one
+  // shared by the two tiles
+  static constexpr bool SEP_S = 2 * D + 3 * N <= 512;
+  static constexpr int TM_S = 2 * D;                 // S_X at TM_S + X * N (SEP_S), else the shared S
+  static constexpr int TM_P = 2 * D + (SEP_S ? 2 : 1) * N;   // P_X at TM_P + X * N / 2
   static constexpr uint32_t TM_COLS = 512;
   static constexpr uint32_t IDESC_QK = idesc_bf16(128, N, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
-  static_assert(2 * D + N + 2 * (N / 2) <= 512, "TMEM budget");
+  static_assert(2 * D + (SEP_S ? 2 : 1) * N + 2 * (N / 2) <= 512, "TMEM budget");
   static_assert(LAUNCH_REGS * THREADS <= 65536 && (65536 / THREADS) >= LAUNCH_REGS, "launch registers");
   static_assert(256 * LOW_REGS + 256 * HIGH_REGS <= LAUNCH_REGS * THREADS,
                 "the register split can only hand over what the launch allocated");
@@ -102,7 +106,7 @@ struct PairCtrl {
   uint64_t q_full, q_empty;
   uint64_t k_full[kMaxUnits], k_empty[kMaxUnits], v_full[kMaxUnits], v_empty[kMaxUnits];
   uint64_t s_full[2], p_full[2];         // per query tile X: S holds QK_X(t), P_X(t) published
-  uint64_t s_free;                       // the last QK's scores were loaded: S may be overwritten
+  uint64_t s_free[2];                    // scores loaded: S (S_X with one buffer per tile) may be overwritten
   uint64_t o_full[2], o_item[2];         // PV_X(t) complete; the item's last PV_X complete
   uint64_t drain, drain2;
   uint64_t stall;                        // never signalled: the watchdog test's stalled wait
@@ -208,7 +212,8 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       mbar_init(smem_u32(&ctl.o_full[x]), 1);
       mbar_init(smem_u32(&ctl.o_item[x]), 1);
     }
-    mbar_init(smem_u32(&ctl.s_free), 128);
+    mbar_init(smem_u32(&ctl.s_free[0]), 128);
+    mbar_init(smem_u32(&ctl.s_free[1]), 128);
     mbar_init(smem_u32(&ctl.ostage_full), 256);
     mbar_init(smem_u32(&ctl.ostage_free), 1);
     for (int i = 0; i < kRecSlots; ++i) {
@@ -393,8 +398,11 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           RingPos k1 = kp;
           if (C::UPT > 1) k1.next(C::KSU);
           for (int x = 0; ok && x < 2; ++x) {
-            if (n_qk > 0) {
-              ok = mbar_wait(smem_u32(&ctl.s_free), (uint32_t)((n_qk - 1) & 1), abort_flag, wl);
+            if (C::SEP_S ? n_qk > 1 : n_qk > 0) {
+              // shared S: the previous QK's scores (the other tile's) were loaded;
+              // S_X: this tile's previous scores were loaded
+              ok = C::SEP_S ? mbar_wait(smem_u32(&ctl.s_free[x]), (uint32_t)(((n_qk >> 1) - 1) & 1), abort_flag, wl)
+                            : mbar_wait(smem_u32(&ctl.s_free[0]), (uint32_t)((n_qk - 1) & 1), abort_flag, wl);
               if (!ok) break;
               tc_fence_after();
             }
@@ -409,7 +417,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
               const uint32_t kb = k_s + kh.slot * C::UNIT;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)              // 16-column steps over the 64 columns
-                mma_ss(tmem + C::TM_S, smem_desc_sw128(qa + kk * 32, 16, 1024),
+                mma_ss(tmem + C::TM_S + (C::SEP_S ? (uint32_t)x * C::N : 0u), smem_desc_sw128(qa + kk * 32, 16, 1024),
                        smem_desc_sw128(kb + kk * 32, 16, 1024), C::IDESC_QK, (half > 0 || kk > 0) ? 1u : 0u);
               if (x == 1) mma_commit(smem_u32(&ctl.k_empty[kh.slot]));
             }
@@ -533,7 +541,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int sid = threadIdx.x - 256 - 128 * x;         // 0 .. 127 within the warpgroup
     const int row = 32 * (warp & 3) + lane;              // TMEM lane of this thread
     const uint32_t lane_t = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t s_col = tmem + lane_t + C::TM_S;
+    const uint32_t s_col = tmem + lane_t + C::TM_S + (C::SEP_S ? (uint32_t)x * N : 0u);
     const uint32_t p_col = tmem + lane_t + C::TM_P + (uint32_t)x * (N / 2);
     const uint32_t o_col = tmem + lane_t + C::TM_O + (uint32_t)x * C::D;
     const float asl2 = fmaxf(fabsf(a.scale * kLog2e), 1.17549435e-38f);
@@ -572,7 +580,7 @@ attn_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           tmem_ld32_red<NEG>(s_col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c), lred[c]);
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(smem_u32(&ctl.s_free));             // S may take the other tile's next QK
+        mbar_arrive(smem_u32(&ctl.s_free[C::SEP_S ? x : 0]));   // S may take the next QK
         float xv[N];
         float mx;
         if (__all_sync(0xffffffffu, klo <= kt0 && khi >= kt0 + N - 1)) {

@@ -390,7 +390,7 @@ def test_repeated_calls_are_bit_identical(err):
     assert err.item() == 0
 
 
-@pytest.mark.parametrize("D,scale", [(256, -0.07), (128, -0.11), (256, 0.0), (128, 0.3)])
+@pytest.mark.parametrize("D,scale", [(256, -0.07), (128, -0.11), (256, 0.0), (128, 0.3), (64, -0.09), (64, 0.0)])
 def test_scale_sign_and_zero_all_rows(D, scale, err):
     """Any finite scale: a negative one (the max is taken on -S), zero (every
     visible key weighs the same) and a large one, on the tensor-core path."""
