@@ -14,9 +14,9 @@ bounded sample of the same workload instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 (N > 1: launched by torchrun, one independent replica per GPU.)
-``--workload chunked_prefill`` runs the causal chunked-prefill layout (head_dim
-128) as the step instead, for profiling that kernel; the default line is the
-Gemma-like one.
+``--workload chunked_prefill`` (``chunked_prefill_d64``) runs the causal
+chunked-prefill layout at head_dim 128 (64) as the step instead, for profiling
+that kernel; the default line is the Gemma-like one.
 """
 import os
 
@@ -267,7 +267,12 @@ def job_rate(units_per_rank, world, ms):
 def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    lay = W.gemma_like(num_requests=args.requests) if args.workload == "gemma_like" else W.chunked_prefill(True)
+    if args.workload == "gemma_like":
+        lay = W.gemma_like(num_requests=args.requests)
+    elif args.workload == "chunked_prefill":
+        lay = W.chunked_prefill(True)
+    else:
+        lay = dataclasses.replace(W.chunked_prefill(True), name="chunked_prefill-head_dim64", head_dim=64)
     step = PrefillStep(lay, dev)
     pairs = visible_pairs_per_head(lay)
     flops = 4.0 * lay.head_dim * lay.num_heads_q * pairs
@@ -812,8 +817,10 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads and bandwidth sweeps")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the step's kernels one by one instead of replaying CUDA graphs")
-    ap.add_argument("--workload", default="gemma_like", choices=["gemma_like", "chunked_prefill"],
-                    help="the step's layout (gemma_like = the benchmark; chunked_prefill = profiling case)")
+    ap.add_argument("--workload", default="gemma_like",
+                    choices=["gemma_like", "chunked_prefill", "chunked_prefill_d64"],
+                    help="the step's layout (gemma_like = the benchmark; the chunked-prefill layouts at "
+                         "head_dim 128 and 64 = profiling cases)")
     ap.add_argument("--requests", type=int, default=4, choices=[1, 2, 3, 4],
                     help="Gemma-like requests per step (4 = the benchmark; fewer = profiling case)")
     args = ap.parse_args()
