@@ -1,7 +1,7 @@
 """Parity at the full workload sizes, in the launch configuration the benchmark
 times: every row of two heads plus 4096 random (token, head) rows of the
-Gemma-like prefill, the chunked prefill (causal and not) and the split-KV
-decode, against the fp64 oracle.  Besides the max-abs bar (2e-2 for bf16),
+Gemma-like prefill, the chunked prefill (causal and not, and causal at
+head_dim 64) and the split-KV decode, against the fp64 oracle.  Besides the max-abs bar (2e-2 for bf16),
 each test bounds the RMS error relative to the RMS of the oracle's output
 (outputs of N(0, 1) data at W = 1024 are only a few hundredths in size) and
 prints max-abs / RMS too.  The max-abs error itself is set by the bf16
@@ -57,6 +57,20 @@ def test_gemma_like_two_full_heads():
 @pytest.mark.parametrize("causal", [True, False])
 def test_chunked_prefill_two_full_heads(causal):
     lay = W.chunked_prefill(causal)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q, k, v, d = gpu_inputs(lay)
+    out, lse = run_attention(lay, q, k, v, d, err=err)
+    rows = _rows(lay, heads=(0, lay.num_heads_q - 1), n_random=4096)
+    ro, rl = oracle_rows(lay, q, k, v, rows)
+    _compare(out, lse, ro, rl, rows, lay.name)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+
+
+def test_chunked_prefill_head_dim_64_two_full_heads():
+    """The causal chunked-prefill layout at head_dim 64 (the benchmark's extra line)."""
+    import dataclasses
+    lay = dataclasses.replace(W.chunked_prefill(True), name="chunked_prefill-head_dim64", head_dim=64)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     q, k, v, d = gpu_inputs(lay)
     out, lse = run_attention(lay, q, k, v, d, err=err)
