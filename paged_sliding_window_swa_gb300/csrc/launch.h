@@ -90,12 +90,12 @@ cudaError_t launch_attention_decode(const AttnArgs &a, cudaStream_t st);
 bool tc_supported(const AttnArgs &a);
 cudaError_t launch_attention_tc(const AttnArgs &a, cudaStream_t st);
 
-// The same for head_dim 128 with two query tiles per work item.
+// The same for head_dim 128 and 64 with two query tiles per work item.
 bool tc_pair_supported(const AttnArgs &a);
 cudaError_t launch_attention_tc_pair(const AttnArgs &a, cudaStream_t st);
 
 // tcgen05 / TMEM attention for everything else: bf16 or fp32 (fp32 as bf16
-// hi + lo operand pairs), any head_dim, split or not.
+// hi + lo operand pairs), head_dim 64, 128 or 256, split or not.
 bool tc_small_supported(const AttnArgs &a);
 cudaError_t launch_attention_tc_small(const AttnArgs &a, cudaStream_t st);
 
