@@ -220,3 +220,35 @@ def test_chunked_prefill_workload_modes_sampled(err):
     for s in range(lay.num_seqs):
         edges += [qsl[s], qsl[s] + 127, qsl[s] + 128, qsl[s + 1] - 1]
     _check(lay, sample_rows(lay, 300, extra_tokens=edges), err)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_layouts_with_chunks_and_per_sequence_causal(seed, err):
+    """Random layouts (dtype, head_dim, GQA group, split count, window, images, page
+    size, lengths) with chunked lookback (chunks of 32-2048, 0-3 back) and random
+    per-sequence causal flags, up to 2000 rows each against the oracle."""
+    rng = np.random.default_rng(30000 + seed)
+    D = int(rng.choice([64, 128, 256]))
+    G = int(rng.choice([1, 2, 4, 8, 16]))
+    dtype = "fp32" if rng.random() < 0.15 else "bf16"
+    P = int(rng.choice([1, 1, 1, 2, 5]))
+    window = int(rng.choice([1, 7, 64, 200, 1000]))      # chunked lookback needs a window
+    lay = W.random_small(30000 + seed, head_dim=D, group=G, dtype=dtype, max_seqs=int(rng.integers(1, 4)),
+                         max_ctx=int(rng.choice([50, 900, 3000])), max_q=int(rng.choice([1, 40, 300, 700])),
+                         window=window, num_splits=P)
+    lay = replace(lay, chunk_size=int(rng.choice([32, 128, 512, 2048])), chunk_lookback=int(rng.choice([0, 1, 3])),
+                  seq_causal=rng.integers(0, 2, size=lay.num_seqs).astype(np.int32))
+    q, k, v, d = gpu_inputs(lay, data_seed=seed)
+    rows = _all_rows(lay)
+    if len(rows) > 2000:
+        rows = [rows[i] for i in sorted(rng.choice(len(rows), 2000, replace=False))]
+    if P == 1:
+        out, lse = run_attention(lay, q, k, v, d, err=err)
+    else:
+        po, pl = run_attention(lay, q, k, v, d, err=err)
+        out, lse = swa.lse_combine(po, pl)
+    ro, rl = oracle_rows(lay, q, k, v, rows)
+    e_out, e_lse = max_errors(out, lse, ro, rl, rows)
+    assert e_out <= atol_for(lay) and e_lse <= LSE_ATOL, (e_out, e_lse)
+    torch.cuda.synchronize()
+    assert err.item() == 0
