@@ -2,19 +2,20 @@
 // per work item (same mask and pruning as attention_tc.cu: vLLM PR #53147
 // summary, implementation items 1-2 and the compute_tile_loop_bounds excerpt).
 //
-// At head_dim 128 (and 64) the tensor memory holds the two O accumulators, one
-// S buffer and the two tiles' P, so an item is a PAIR of consecutive 128-row
-// query tiles A and B of one sequence and kv head (2 x 128/G positions x G
-// heads).  Every K/V tile is staged once for both, and each query tile has
-// its own softmax warpgroup that owns whole rows: no max exchange between
-// warpgroups.  The key loop covers the 128-key tiles of the union of the
-// pair's rows.
+// At head_dim 128 the tensor memory holds the two O accumulators, one S
+// buffer and the two tiles' P (at head_dim 64, one S buffer per tile), so an
+// item is a PAIR of consecutive 128-row query tiles A and B of one sequence
+// and kv head (2 x 128/G positions x G heads).  Every K/V tile is staged once
+// for both, and each query tile has its own softmax warpgroup that owns whole
+// rows: no max exchange between warpgroups.  The key loop covers the 128-key
+// tiles of the union of the pair's rows.
 //
-// The S buffer is shared: QK_A(t) and QK_B(t) take turns in it, and each QK
-// waits only until the other tile's softmax has LOADED the previous scores
-// (s_free).  P goes to a region of its own, so a tile's next QK never waits
-// for its softmax to finish or for its PV: while one softmax warpgroup works
-// on its scores the tensor pipe runs the other tile's QK and the PVs.
+// At head_dim 128 the S buffer is shared: QK_A(t) and QK_B(t) take turns in
+// it, and each QK waits only until the other tile's softmax has LOADED the
+// previous scores (s_free).  P goes to a region of its own, so a tile's next
+// QK never waits for its softmax to finish or for its PV: while one softmax
+// warpgroup works on its scores the tensor pipe runs the other tile's QK and
+// the PVs.
 //
 // Shared memory: Q_A and Q_B (D x 256 B each, TMA, 128-byte swizzle, K-major)
 // and two rings of 16 KB units.  At head_dim 128 a K unit holds one 64-column
