@@ -507,6 +507,9 @@ def report_line(args, lay, step, flops, pairs, ms_per_step, attn_ms, feed_ms, cl
             "frac": round(achieved / pk["bf16_tflops"], 4),
             "traffic": kernel_traffic(args.requests) if args.workload == "gemma_like" else None,
             "peak_source": f"{pk['source']} bf16 dense (burst)",
+            "peak_sustained": pk["bf16_tflops_sustained"],
+            "frac_sustained": (round(achieved / pk["bf16_tflops_sustained"], 4)
+                               if pk.get("bf16_tflops_sustained") else None),
             "avg_launch_ms": round(attn_avg, 4),
         },
         "feeders_ms": round(statistics.mean(feed_ms), 4),
