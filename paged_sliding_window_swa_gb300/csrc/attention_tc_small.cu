@@ -1,6 +1,6 @@
 // Tensor-core (tcgen05 / TMEM) attention for the shapes the two fast kernels
-// do not take: fp32 inputs, head_dim 64, and split-KV partitions with many
-// query rows.  Same mask and pruning as
+// do not take: fp32 inputs, split-KV partitions with many query rows, and GQA
+// groups of 32 to 128 (head_dim 64, 128 or 256).  Same mask and pruning as
 // attention_tc.cu (vLLM PR #53147 summary, implementation items 1-2 and the
 // compute_tile_loop_bounds excerpt); split partitions as in the split-KV
 // decode (MLA DCP decode study notes, section 1.1).
