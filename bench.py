@@ -119,7 +119,7 @@ def kernel_traffic(num_requests):
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one attention launch (ncu, 1 pass)
-MEASURED_TRAFFIC = {"kernel_sha": "1e51a5d60c518219", "requests": 4, "bytes": (1085.4 + 518.0) * 1e6}
+MEASURED_TRAFFIC = {"kernel_sha": "1e51a5d60c518219", "requests": 4, "bytes": (1085.5 + 518.4) * 1e6}
 
 
 def peaks():
